@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark of the Gated-DeltaNet mixer on GB300. It prints one JSON line.
+
+The headline workload is batched decode at scale: the 30 GDN layers of the
+40-layer stack, each with its own seeded parameters and fp32 states (15 GiB),
+run on B=256 sequences. One step is one token for every sequence through all
+30 layers, as 30 calls of gdn_decode_step. ``value`` is decode tokens/s: B x
+steps / device time, with the inputs already resident in HBM.
+
+The same run also times the T=4096 bf16 prefill (one gdn_prefill call) and
+reports it under "prefill".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N>1 (launched with torchrun) every rank runs its own replica of the
+workload ("replicas only": the mixer has no exchange step). value is the
+total over ranks, divided by the slowest rank's time. ``--impl reference``
+times the fp64 CPU oracle on the host cores on a bounded sample of the same
+workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tok/s @T=4096; decode tok/s @B=256; % of HBM/TC roofline"
+LAYERS, BATCH, PREFILL_T, CHUNK = 30, 256, 4096, 64
+NOMINAL_HBM_GBS = 8000.0
+
+# Algorithmic bytes of one decode token through one layer (bf16 activations,
+# fp32 state, bf16 output): the state is read and written once (2 x 32 x 128 x
+# 128 x 4), the conv_state is read and written once (2 x 3 x 8192 x 2), and the
+# inputs qkv, z, alpha and beta are read and out written once (16384 + 8192 +
+# 128 + 8192). The layer's parameters (conv_w 131072, A_log, dt_bias and norm_w
+# 768) are read once per launch.
+DECODE_BYTES_PER_TOKEN_LAYER = 4_194_304 + 98_304 + 32_896
+DECODE_PARAM_BYTES_PER_LAUNCH = 131_840
+# Algorithmic FLOPs of the chunked prefill per token: the dense contractions
+# K K^T and Q K^T once per K-head; T V, T (Gamma K), W S, Q S, the intra-chunk
+# (M o Q K^T) V_new and the state update K^T V_new per V-head, with C=64.
+PREFILL_FLOP_PER_TOKEN = 5_242_880
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode launch (B=256),
+# from the ncu capture summarised in profiles/; None until a capture of the
+# current kernel exists.
+DECODE_TRAFFIC_PER_LAUNCH = None
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the GPU works."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.idx)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if any(a <= r[0] <= b for a, b in self.windows)]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def setup_decode(torch, I, ops, dev, n_inputs):
+    layers = []
+    for layer in range(LAYERS):
+        seed = I.seed_of(3, layer)
+        lp = I.layer_params(seed).to(dev)
+        conv, S = I.initial_states(seed, BATCH, torch.bfloat16, device=dev)
+        st = I.streams(seed, BATCH, torch.bfloat16, device=dev, lead=(n_inputs,))
+        out = torch.empty(BATCH, I.D_INNER, dtype=torch.bfloat16, device=dev)
+        layers.append(dict(lp=lp, cp=ops.make_params(lp), conv=conv, S=S, st=st, out=out))
+    return layers
+
+
+def decode_step(ops, layers, i):
+    for L in layers:
+        st = L["st"]
+        ops.decode_step(None, st.qkv[i], st.z[i], st.alpha[i], st.beta[i], L["conv"], L["S"], L["out"],
+                        cparams=L["cp"])
+
+
+def run_gpu(args, rank, world, dev):
+    import torch
+    import torch.distributed as dist
+
+    from gated_deltanet_linear_02_gb300 import build as gbuild
+    from gated_deltanet_linear_02_gb300 import inputs as I
+    from gated_deltanet_linear_02_gb300 import ops
+
+    if rank == 0 or not os.path.exists(ops.LIB_PATH):
+        gbuild.build()
+    if world > 1:
+        dist.barrier()
+    hbm_peak, tc_peak, tc_sust, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()]))
+    sampler.start()
+
+    def barrier_sync():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---------------- decode @ B=256 over 30 layers (headline)
+    n_inputs = 8
+    layers = setup_decode(torch, I, ops, dev, n_inputs)
+    for w in range(args.warmup):
+        decode_step(ops, layers, w % n_inputs)
+    barrier_sync()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for k in range(args.steps):
+        decode_step(ops, layers, k % n_inputs)
+    ev1.record(stream)
+    barrier_sync()
+    sampler.mark(t_wall0, time.time())
+    dec_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    launches = LAYERS * args.steps
+    per_launch_s = dec_ms / 1e3 / launches
+    bytes_per_launch = BATCH * DECODE_BYTES_PER_TOKEN_LAYER + DECODE_PARAM_BYTES_PER_LAUNCH
+    achieved = bytes_per_launch / per_launch_s / 1e9
+    dec_tok_s = world * BATCH * args.steps / (dec_ms / 1e3)
+
+    # ---------------- e2e: the same decode through the C ABI from pinned host buffers
+    host_in = []
+    for L in layers:
+        st = L["st"]
+        host_in.append([t[0].cpu().pin_memory() for t in (st.qkv, st.z, st.alpha, st.beta)])
+    dev_in = [[torch.empty_like(t, device=dev) for t in h] for h in host_in]
+    host_out = [torch.empty(BATCH, I.D_INNER, dtype=torch.bfloat16).pin_memory() for _ in layers]
+    h2d = sum(t.numel() * t.element_size() for h in host_in for t in h)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for L, h, d, ho in zip(layers, host_in, dev_in, host_out):
+            for src, dst in zip(h, d):
+                dst.copy_(src, non_blocking=True)
+            ops.decode_step(None, d[0], d[1], d[2], d[3], L["conv"], L["S"], L["out"], cparams=L["cp"])
+            ho.copy_(L["out"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier_sync()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    ev1.record(stream)
+    barrier_sync()
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    e2e_tok_s = world * BATCH * args.steps / (e2e_ms / 1e3)
+    del layers, host_in, dev_in, host_out
+    torch.cuda.empty_cache()
+
+    # ---------------- prefill @ T=4096 (bf16, zero initial state)
+    seed = I.seed_of(2)
+    lp = I.layer_params(seed).to(dev)
+    cp = ops.make_params(lp)
+    st = I.streams(seed, PREFILL_T, torch.bfloat16, device=dev)
+    cu = I.cu_seqlens([PREFILL_T]).to(dev)
+    out = torch.empty(PREFILL_T, I.D_INNER, dtype=torch.bfloat16, device=dev)
+    cs_out = torch.empty(1, I.KCONV - 1, I.C_CONV, dtype=torch.bfloat16, device=dev)
+    S_out = torch.empty(1, I.HV, I.DV, I.DK, dtype=torch.float32, device=dev)
+    ws = torch.empty(ops.prefill_workspace_size(1, PREFILL_T, torch.bfloat16, 0), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)      # > L2 (129 MB)
+
+    def prefill_call():
+        ops.prefill(None, st.qkv, st.z, st.alpha, st.beta, cu, out, None, cs_out, None, S_out, chunk_size=0,
+                    workspace=ws, cparams=cp)
+
+    for _ in range(args.warmup):
+        prefill_call()
+    barrier_sync()
+    times = []
+    t_wall0 = time.time()
+    for _ in range(args.steps):
+        flush.fill_(1)                                   # evict L2 between timed calls
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        prefill_call()
+        b.record(stream)
+        times.append((a, b))
+    barrier_sync()
+    sampler.mark(t_wall0, time.time())
+    pf_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))
+    assert ops.prefill_device_error(ws) == ops.GDN_OK
+    pf_tok_s = world * PREFILL_T / (pf_ms / 1e3)
+    pf_tflops = PREFILL_FLOP_PER_TOKEN * PREFILL_T / (pf_ms / 1e3) / 1e12
+    clocks = sampler.stop()
+
+    return dict(dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
+                bytes_per_launch=bytes_per_launch, launches=launches, e2e_tok_s=e2e_tok_s, e2e_ms=e2e_ms,
+                h2d=h2d, d2h=d2h, pf_ms=pf_ms, pf_tok_s=pf_tok_s, pf_tflops=pf_tflops, hbm_peak=hbm_peak,
+                tc_peak=tc_peak, peak_src=peak_src, clocks=clocks)
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_decode_sample(n_seq: int, threads: int):
+    """The fp64 oracle on a bounded sample of the decode workload: one token for
+    n_seq sequences through all 30 layers (each layer with its own seeded
+    parameters and random states), threads over sequences. Returns (seconds, tokens)."""
+    import numpy as np
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+
+    from gated_deltanet_linear_02_gb300 import inputs as I
+    from oracle import oracle
+
+    # Timing does not depend on the values, so a few distinct sequences per
+    # layer stand in for all n_seq (the oracle copies its inputs on every call).
+    nd = min(n_seq, 4)
+    per_layer = []
+    for layer in range(LAYERS):
+        seed = I.seed_of(3, layer)
+        lp = I.layer_params(seed)
+        P = oracle.Params.of(lp.conv_w, lp.A_log, lp.dt_bias, lp.norm_w, lp.l2_eps, lp.norm_eps)
+        conv, S = I.initial_states(seed, nd, torch.bfloat16)
+        st = I.streams(seed, nd, torch.bfloat16)
+        per_layer.append((P, conv.double().numpy(), np.swapaxes(S.double().numpy(), -1, -2).copy(),
+                          [t.double().numpy() for t in (st.qkv, st.z, st.alpha, st.beta)]))
+
+    def one_seq(b):
+        b %= nd
+        for P, conv, S, (qkv, z, al, be) in per_layer:
+            oracle.gdn_sequence(P, qkv[b:b + 1], z[b:b + 1], al[b:b + 1], be[b:b + 1], conv[b], S[b])
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one_seq, range(n_seq)))
+    return time.perf_counter() - t0, n_seq
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(n_seq=None):
+    from oracle import oracle
+    oracle.build()
+    threads = host_threads()
+    n_seq = n_seq or max(16, 8 * threads)
+    secs, toks = oracle_decode_sample(n_seq, threads)
+    return {"value": toks / secs, "unit": "tok/s", "cores": threads, "kind": "oracle",
+            "sample": f"one decode token through all 30 layers for {n_seq} of the 256 sequences "
+                      f"(fp64 oracle, {threads} threads over sequences), {secs:.1f} s wall"}
+
+
+# ------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import oracle
+        oracle.build()
+        threads = host_threads()
+        n_seq = max(16, 2 * threads)
+        for _ in range(args.warmup):
+            oracle_decode_sample(n_seq, threads)
+        tot_s = tot_tok = 0.0
+        for _ in range(args.steps):
+            s, t = oracle_decode_sample(n_seq, threads)
+            tot_s += s
+            tot_tok += t
+        v = tot_tok / tot_s
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_s / args.steps * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic",
+                "config": {"workload": "decode_30L_B256_bf16", "layers": LAYERS, "batch": BATCH,
+                           "parallelism": "replicas"},
+                "cpu_baseline": {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                                 "sample": f"per step: one decode token through all 30 layers for {n_seq} "
+                                           f"sequences, {threads} threads"},
+                "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    r = run_gpu(args, rank, world, dev)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    frac = r["achieved"] / r["hbm_peak"]
+    line = {
+        "metric": METRIC, "value": r["dec_tok_s"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["dec_ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "decode_30L_B256_bf16", "layers": LAYERS, "batch": BATCH,
+                   "activations": "bf16", "state": "fp32", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (15 GiB of state touched per step)"},
+        "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
+                     "frac": frac, "traffic": DECODE_TRAFFIC_PER_LAUNCH,
+                     "kernel": "decode_step_kernel<bf16,bf16>",
+                     "peak_source": f"{r['peak_src']} (MEASURED_PEAKS.json hbm_gbs)" if r["peak_src"] == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": r["bytes_per_launch"],
+                     "launch_us": r["per_launch_s"] * 1e6,
+                     "frac_of_nominal_8TBs": r["achieved"] / NOMINAL_HBM_GBS},
+        "cpu_baseline": cpu,
+        "e2e": {"value": r["e2e_tok_s"], "unit": "tok/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"] / args.steps},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "prefill": {"workload": "prefill_T4096_bf16", "value": r["pf_tok_s"], "unit": "tok/s",
+                    "ms_per_call": r["pf_ms"], "l2": "flushed between timed calls",
+                    "roofline": {"bound": "tensor", "achieved": r["pf_tflops"], "peak": r["tc_peak"],
+                                 "unit": "TFLOP/s", "frac": r["pf_tflops"] / r["tc_peak"],
+                                 "algorithmic_flop_per_call": PREFILL_FLOP_PER_TOKEN * PREFILL_T}},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+// gdn_api.cu -- the C ABI declared in include/gdn.h: argument checks and
+// dispatch to the kernels. Nothing here allocates or synchronises (except
+// gdn_prefill_device_error, which is documented to).
+#include <stdio.h>
+#include <string.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+cudaError_t launch_conv_step(const float *, const void *, void *, void *, int, gdn_dtype, cudaStream_t);
+cudaError_t launch_decode_step(const gdn_params *, const void *, const void *, const void *, const void *,
+                               void *, float *, void *, int, gdn_dtype, gdn_dtype, cudaStream_t);
+size_t scan_workspace_bytes(int T_total);
+cudaError_t launch_prefill_scan(const gdn_params *, const void *, const void *, const void *, const void *,
+                                const int32_t *, int, int, const void *, void *, const float *, float *,
+                                void *, gdn_dtype, gdn_dtype, void *, cudaStream_t);
+}  // namespace gdn
+
+using namespace gdn;
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+gdn_status fail(gdn_status s, const char *what)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+    return s;
+}
+
+gdn_status cuda_fail(cudaError_t e, const char *where)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+    return GDN_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void *p) { return p != nullptr && aligned16(p); }
+bool ok_opt_ptr(const void *p) { return p == nullptr || aligned16(p); }
+bool ok_dtype(gdn_dtype d) { return d == GDN_F32 || d == GDN_BF16; }
+
+gdn_status check_params(const gdn_params *p)
+{
+    if (p == nullptr) return fail(GDN_ERR_INVALID_ARG, "params is NULL");
+    if (!ok_ptr(p->conv_w) || !ok_ptr(p->A_log) || !ok_ptr(p->dt_bias) || !ok_ptr(p->norm_w))
+        return fail(GDN_ERR_INVALID_ARG, "a parameter pointer is NULL or not 16-byte aligned");
+    if (!(p->norm_eps >= 0.0f) || !(p->l2_eps >= 0.0f))
+        return fail(GDN_ERR_INVALID_ARG, "epsilons must be >= 0");
+    return GDN_OK;
+}
+
+constexpr int MAX_B = 65535;
+constexpr int MAX_N = 65535;
+constexpr int MAX_T = 1 << 24;
+constexpr size_t WS_HEADER = 256;   // device error word lives here
+
+int resolve_chunk(int chunk_size, gdn_dtype act)
+{
+    (void)act;
+    if (chunk_size == 0) return 1;
+    return chunk_size;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+const char *gdn_last_error(void) { return g_last_error; }
+
+const char *gdn_status_string(gdn_status s)
+{
+    switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    }
+    return "GDN_STATUS_UNKNOWN";
+}
+
+gdn_status gdn_conv_step(const float *conv_w, const void *qkv_in, void *qkv_out, void *conv_state, int B,
+                         gdn_dtype act, void *stream)
+{
+    if (!ok_dtype(act)) return fail(GDN_ERR_INVALID_ARG, "unknown activation dtype");
+    if (B < 0 || B > MAX_B) return fail(GDN_ERR_INVALID_ARG, "B out of range [0, 65535]");
+    if (B == 0) return GDN_OK;
+    if (!ok_ptr(conv_w) || !ok_ptr(qkv_in) || !ok_ptr(qkv_out) || !ok_ptr(conv_state))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    if (qkv_in == qkv_out) return fail(GDN_ERR_INVALID_ARG, "qkv_out may not alias qkv_in");
+    cudaError_t e = launch_conv_step(conv_w, qkv_in, qkv_out, conv_state, B, act, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_conv_step");
+}
+
+gdn_status gdn_decode_step(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
+                           const void *beta, void *conv_state, float *ssm_state, void *out, int B,
+                           gdn_dtype act, gdn_dtype out_dt, void *stream)
+{
+    if (!ok_dtype(act) || !ok_dtype(out_dt)) return fail(GDN_ERR_INVALID_ARG, "unknown dtype");
+    if (B < 0 || B > MAX_B) return fail(GDN_ERR_INVALID_ARG, "B out of range [0, 65535]");
+    if (B == 0) return GDN_OK;
+    gdn_status st = check_params(p);
+    if (st != GDN_OK) return st;
+    if (!ok_ptr(qkv) || !ok_ptr(z) || !ok_ptr(alpha) || !ok_ptr(beta) || !ok_ptr(conv_state) ||
+        !ok_ptr(ssm_state) || !ok_ptr(out))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    cudaError_t e = launch_decode_step(p, qkv, z, alpha, beta, conv_state, ssm_state, out, B, act, out_dt,
+                                       (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_decode_step");
+}
+
+size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_size)
+{
+    if (N < 0 || N > MAX_N || T_total < 0 || T_total > MAX_T || !ok_dtype(act)) return 0;
+    const int ch = resolve_chunk(chunk_size, act);
+    size_t body = 0;
+    if (ch == 1) body = scan_workspace_bytes(T_total);
+    else return 0;
+    return WS_HEADER + ((body + 255) & ~(size_t)255);
+}
+
+gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, const void *alpha, const void *beta,
+                       const int32_t *cu_seqlens, int N, int T_total, const void *conv_state_in,
+                       void *conv_state_out, const float *ssm_state_in, float *ssm_state_out, void *out,
+                       gdn_dtype act, gdn_dtype out_dt, int chunk_size, void *workspace, size_t ws_bytes,
+                       void *stream)
+{
+    if (!ok_dtype(act) || !ok_dtype(out_dt)) return fail(GDN_ERR_INVALID_ARG, "unknown dtype");
+    if (N < 0 || N > MAX_N) return fail(GDN_ERR_INVALID_ARG, "N out of range [0, 65535]");
+    if (T_total < 0 || T_total > MAX_T) return fail(GDN_ERR_INVALID_ARG, "T_total out of range [0, 2^24]");
+    if (N == 0) {
+        if (T_total != 0) return fail(GDN_ERR_INVALID_ARG, "T_total > 0 with no sequences");
+        return GDN_OK;
+    }
+    const int ch = resolve_chunk(chunk_size, act);
+    if (ch != 1) return fail(GDN_ERR_UNSUPPORTED, "chunk_size must be 0 or 1 in this build");
+    gdn_status st = check_params(p);
+    if (st != GDN_OK) return st;
+    if (!ok_ptr(cu_seqlens) || (T_total > 0 && (!ok_ptr(qkv) || !ok_ptr(z) || !ok_ptr(alpha) ||
+                                                !ok_ptr(beta) || !ok_ptr(out))))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    if (!ok_opt_ptr(conv_state_in) || !ok_opt_ptr(conv_state_out) || !ok_opt_ptr(ssm_state_in) ||
+        !ok_opt_ptr(ssm_state_out))
+        return fail(GDN_ERR_INVALID_ARG, "a state pointer is not 16-byte aligned");
+    const size_t need = gdn_prefill_workspace_size(N, T_total, act, ch);
+    if (workspace == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(GDN_ERR_WORKSPACE, "workspace missing, misaligned (256 B) or too small");
+    void *body = static_cast<char *>(workspace) + WS_HEADER;
+    cudaStream_t s = (cudaStream_t)stream;
+    // The error word reflects the most recent call on this workspace.
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int), s);
+    if (e == cudaSuccess)
+        e = launch_prefill_scan(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
+                                ssm_state_in, ssm_state_out, out, act, out_dt, body, s);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_prefill");
+}
+
+gdn_status gdn_prefill_device_error(void *workspace, void *stream)
+{
+    if (!ok_ptr(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace is NULL or misaligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned int word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && word != 0) e = cudaMemsetAsync(workspace, 0, sizeof(word), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_prefill_device_error");
+    return word == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,191 @@
+"""Thin ctypes binding of libgdn.so (include/gdn.h), with the same names.
+
+This layer only marshals arguments. It checks the tensors' shapes, dtypes,
+devices and contiguity, passes their device pointers and the current CUDA
+stream, and turns a non-OK status into ``GdnError``. Every step of the mixer
+runs in the library's CUDA kernels. If the library is missing, loading fails
+loudly: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import inputs as _inp
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = range(6)
+GDN_F32, GDN_BF16 = 0, 1
+_DT = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
+
+HV, HK, DK, DV, KC, CC, DI = _inp.HV, _inp.HK, _inp.DK, _inp.DV, _inp.KCONV, _inp.C_CONV, _inp.D_INNER
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}" + (f" ({detail})" if detail else ""))
+
+
+class gdn_params(ctypes.Structure):
+    _fields_ = [("conv_w", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("norm_w", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("l2_eps", ctypes.c_float)]
+
+
+_lib = None
+_vp, _int, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgdn.so. Raises if it has not been built: the mixer has
+    no CPU or library fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        L.gdn_conv_step.restype = _int
+        L.gdn_conv_step.argtypes = [_vp, _vp, _vp, _vp, _int, _int, _vp]
+        L.gdn_decode_step.restype = _int
+        L.gdn_decode_step.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 7 + [_int, _int, _int, _vp]
+        L.gdn_prefill.restype = _int
+        L.gdn_prefill.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 5 + [_int, _int] + [_vp] * 5 + \
+            [_int, _int, _int, _vp, _sz, _vp]
+        L.gdn_prefill_workspace_size.restype = _sz
+        L.gdn_prefill_workspace_size.argtypes = [_int, _int, _int, _int]
+        L.gdn_prefill_device_error.restype = _int
+        L.gdn_prefill_device_error.argtypes = [_vp, _vp]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_status_string.argtypes = [_int]
+        L.gdn_last_error.restype = ctypes.c_char_p
+        L.gdn_last_error.argtypes = []
+        L.gdn_abi_version.restype = _int
+        L.gdn_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().gdn_status_string(int(s)).decode()
+
+
+def last_error() -> str:
+    return lib().gdn_last_error().decode()
+
+
+def abi_version() -> int:
+    return lib().gdn_abi_version()
+
+
+def _check(status: int, where: str):
+    if status != GDN_OK:
+        raise GdnError(status, where, last_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _ptr(t: torch.Tensor | None, name: str, shape=None, dtype=None, device=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def make_params(p) -> gdn_params:
+    """gdn_params from anything with conv_w, A_log, dt_bias, norm_w fp32 CUDA
+    tensors and norm_eps, l2_eps floats (e.g. inputs.LayerParams)."""
+    return gdn_params(_ptr(p.conv_w, "conv_w", (CC, KC), torch.float32),
+                      _ptr(p.A_log, "A_log", (HV,), torch.float32),
+                      _ptr(p.dt_bias, "dt_bias", (HV,), torch.float32),
+                      _ptr(p.norm_w, "norm_w", (DV,), torch.float32),
+                      float(p.norm_eps), float(p.l2_eps))
+
+
+def _act_dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise ValueError(f"activation dtype {t.dtype} unsupported (float32 or bfloat16)")
+    return _DT[t.dtype]
+
+
+def conv_step(conv_w, qkv_in, qkv_out, conv_state, stream=None):
+    """gdn_conv_step: qkv_out = SiLU(causal conv(conv_state, qkv_in)); conv_state shifts."""
+    B = qkv_in.shape[0]
+    act = _act_dtype(qkv_in)
+    st = lib().gdn_conv_step(_ptr(conv_w, "conv_w", (CC, KC), torch.float32),
+                             _ptr(qkv_in, "qkv_in", (B, CC)), _ptr(qkv_out, "qkv_out", (B, CC), qkv_in.dtype),
+                             _ptr(conv_state, "conv_state", (B, KC - 1, CC), qkv_in.dtype), B, act,
+                             _stream(stream))
+    _check(st, "gdn_conv_step")
+
+
+def decode_step(params, qkv, z, alpha, beta, conv_state, ssm_state, out, stream=None,
+                cparams: gdn_params | None = None):
+    """gdn_decode_step: one token for B sequences, states updated in place."""
+    B = qkv.shape[0]
+    dt = qkv.dtype
+    act = _act_dtype(qkv)
+    od = _act_dtype(out)
+    cp = cparams if cparams is not None else make_params(params)
+    st = lib().gdn_decode_step(ctypes.byref(cp), _ptr(qkv, "qkv", (B, CC)), _ptr(z, "z", (B, DI), dt),
+                               _ptr(alpha, "alpha", (B, HV), dt), _ptr(beta, "beta", (B, HV), dt),
+                               _ptr(conv_state, "conv_state", (B, KC - 1, CC), dt),
+                               _ptr(ssm_state, "ssm_state", (B, HV, DV, DK), torch.float32),
+                               _ptr(out, "out", (B, DI)), B, act, od, _stream(stream))
+    _check(st, "gdn_decode_step")
+
+
+def prefill_workspace_size(N: int, T_total: int, act=torch.bfloat16, chunk_size: int = 0) -> int:
+    return int(lib().gdn_prefill_workspace_size(int(N), int(T_total), _DT[act], int(chunk_size)))
+
+
+def prefill(params, qkv, z, alpha, beta, cu_seqlens, out, conv_state_in=None, conv_state_out=None,
+            ssm_state_in=None, ssm_state_out=None, chunk_size: int = 0, workspace=None, stream=None,
+            cparams: gdn_params | None = None):
+    """gdn_prefill over N packed sequences (cu_seqlens: int32 CUDA [N+1]).
+    Allocates the workspace through torch when none is given."""
+    T = qkv.shape[0]
+    N = cu_seqlens.shape[0] - 1
+    dt = qkv.dtype
+    act = _act_dtype(qkv)
+    od = _act_dtype(out)
+    need = prefill_workspace_size(N, T, dt, chunk_size)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=qkv.device)
+    cp = cparams if cparams is not None else make_params(params)
+    st = lib().gdn_prefill(ctypes.byref(cp), _ptr(qkv, "qkv", (T, CC)), _ptr(z, "z", (T, DI), dt),
+                           _ptr(alpha, "alpha", (T, HV), dt), _ptr(beta, "beta", (T, HV), dt),
+                           _ptr(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32), N, T,
+                           _ptr(conv_state_in, "conv_state_in", (N, KC - 1, CC), dt),
+                           _ptr(conv_state_out, "conv_state_out", (N, KC - 1, CC), dt),
+                           _ptr(ssm_state_in, "ssm_state_in", (N, HV, DV, DK), torch.float32),
+                           _ptr(ssm_state_out, "ssm_state_out", (N, HV, DV, DK), torch.float32),
+                           _ptr(out, "out", (T, DI)), act, od, int(chunk_size),
+                           _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                           _stream(stream))
+    _check(st, "gdn_prefill")
+    return workspace
+
+
+def prefill_device_error(workspace, stream=None) -> int:
+    """Synchronises the stream; GDN_OK or GDN_ERR_TIMEOUT for the last prefill on this workspace."""
+    return lib().gdn_prefill_device_error(_ptr(workspace, "workspace"), _stream(stream))

@@ -1,0 +1,170 @@
+/*
+ * gdn.h -- C ABI of libgdn, the Gated-DeltaNet token mixer for GB300 (sm_103a).
+ *
+ * The operation is the SSM block of "qwen35moe -- Forward-Pass Design
+ * (Pantheon port)". These calls cover its section "SSM block -- Gated-Delta-Net"
+ * from the already-projected streams up to, but not including, the ssm_out
+ * projection:
+ *   causal conv1d (k=4, with conv_state) + SiLU over the 8192-channel q|k|v
+ *   stream; split into q[16x128], k[16x128], v[32x128]; L2-normalise q and k
+ *   per head; GQA repeat 16 -> 32 with V-head vh reading K-head vh % 16
+ *   (watch-list item on the interleaved repeat); decay g = -exp(A_log) *
+ *   softplus(alpha + dt_bias) and beta = sigmoid(beta) (section "Decay gate");
+ *   the per-token delta-rule recurrence (a)-(d) with read-after-write and one
+ *   1/sqrt(128) scale (section "Per-token recurrence"); and
+ *   gated = RMSNorm(y, ssm_norm) * silu(z) (section "Output path").
+ *
+ * Fixed dimensions (section "Config (mini)"): 32 V-heads, 16 K-heads, head dim
+ * 128 for keys and values, conv width 4, 8192 conv channels, d_inner 4096.
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor pointer is caller-owned DEVICE memory, dense, row-major, and
+ *    16-byte aligned. The library never allocates, frees or keeps a pointer
+ *    after a call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Every call only enqueues work on that stream and returns; no call
+ *    synchronises, except gdn_prefill_device_error, which says so.
+ *  - Activations (qkv, z, alpha, beta, conv_state) all use one dtype `act`;
+ *    `out_dt` is the dtype of `out`. Parameters and the SSM state are fp32.
+ *  - The SSM state of one (sequence, V-head) is the page's S[i][j] (i = key
+ *    index, j = value index) stored TRANSPOSED: ssm_state[..][j][i], with the
+ *    key index contiguous, 128 x 128 fp32 = 64 KiB.
+ *  - conv_state[n] holds the last 3 raw (pre-conv) inputs of sequence n,
+ *    oldest row first, [3][8192] in the activation dtype.
+ *  - Invalid arguments return a status and enqueue nothing. Nothing throws,
+ *    aborts or traps. GDN_ERR_CUDA means a launch was rejected by the runtime;
+ *    gdn_last_error() then describes it.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+#define GDN_NUM_V_HEADS 32
+#define GDN_NUM_K_HEADS 16
+#define GDN_HEAD_DIM 128
+#define GDN_CONV_K 4
+#define GDN_CONV_CHANNELS 8192
+#define GDN_D_INNER 4096
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad enum     */
+    GDN_ERR_UNSUPPORTED = 2,   /* well-formed request this build does not serve   */
+    GDN_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required      */
+    GDN_ERR_CUDA = 4,          /* the CUDA runtime rejected a launch              */
+    GDN_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up              */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Per-layer parameters: device pointers to fp32 tensors, plus two epsilons.
+ * Page tensor names in brackets. */
+typedef struct {
+    const float *conv_w;   /* [8192][4] (ssm_conv1d.weight); tap 3 multiplies the
+                              current token, taps 0..2 the conv_state rows
+                              oldest-first. The page lists no conv bias.       */
+    const float *A_log;    /* [32]; the decay uses -exp(A_log) (ssm_a)          */
+    const float *dt_bias;  /* [32] (ssm_dt.bias)                                */
+    const float *norm_w;   /* [128] (ssm_norm.weight), shared by all V-heads and
+                              applied as w, not 1 + w                          */
+    float norm_eps;        /* RMSNorm epsilon: y * (mean(y^2) + eps)^-1/2       */
+    float l2_eps;          /* L2 epsilon: x * (sum(x^2) + eps)^-1/2             */
+} gdn_params;
+
+/*
+ * gdn_conv_step -- the conv part alone, for one token of B sequences.
+ * Section "Causal conv1d": qkv_out[b][c] = SiLU(sum_m conv_w[c][m] * win[m])
+ * where win = (conv_state[b][0..2][c], qkv_in[b][c]); then conv_state[b]
+ * shifts by one token (row 0 drops out, qkv_in[b] becomes row 2).
+ *   conv_w      [8192][4] fp32
+ *   qkv_in      [B][8192] act          qkv_out [B][8192] act (may not alias qkv_in)
+ *   conv_state  [B][3][8192] act, updated in place
+ * B == 0 is a no-op. Errors: GDN_ERR_INVALID_ARG.
+ */
+gdn_status gdn_conv_step(const float *conv_w, const void *qkv_in, void *qkv_out,
+                         void *conv_state, int B, gdn_dtype act, void *stream);
+
+/*
+ * gdn_decode_step -- one token for each of B independent sequences, the whole
+ * mixer fused: conv -> split -> L2 -> GQA -> gates -> recurrence -> gated norm.
+ * Each (sequence, V-head) state is read once and written once.
+ *   p           layer parameters
+ *   qkv         [B][8192] act          z          [B][4096] act
+ *   alpha, beta [B][32] act (raw logits; the gates are computed inside)
+ *   conv_state  [B][3][8192] act, updated in place
+ *   ssm_state   [B][32][128 j][128 i] fp32, updated in place
+ *   out         [B][4096] out_dt, head-major (out[b][vh*128 + j])
+ * 1 <= B <= 65535 (B == 0 is a no-op). Errors: GDN_ERR_INVALID_ARG, GDN_ERR_CUDA.
+ */
+gdn_status gdn_decode_step(const gdn_params *p, const void *qkv, const void *z,
+                           const void *alpha, const void *beta, void *conv_state,
+                           float *ssm_state, void *out, int B, gdn_dtype act,
+                           gdn_dtype out_dt, void *stream);
+
+/*
+ * gdn_prefill -- N packed sequences of total length T_total, each run through
+ * the whole mixer token by token in order, with state carried in and out.
+ *   cu_seqlens      DEVICE int32 [N+1]: cu[0] = 0, cu[n] <= cu[n+1], cu[N] =
+ *                   T_total; sequence n owns rows [cu[n], cu[n+1]). Empty
+ *                   sequences are allowed (their states pass through).
+ *   qkv [T_total][8192], z [T_total][4096], alpha/beta [T_total][32]   act
+ *   conv_state_in   [N][3][8192] act, or NULL for all-zero initial conv state
+ *   conv_state_out  [N][3][8192] act, or NULL to skip; may alias conv_state_in
+ *   ssm_state_in    [N][32][128][128] fp32 (transposed as above), or NULL = 0
+ *   ssm_state_out   [N][32][128][128] fp32, or NULL to skip; may alias the input
+ *   out             [T_total][4096] out_dt
+ *   chunk_size      0 = library choice; 1 = exact per-token scan (fp32 math,
+ *                   any act); 64 = chunked WY/UT form on tensor cores (act must
+ *                   be GDN_BF16). The chunked form is an exact re-association
+ *                   of the same recurrence; the two differ only by rounding.
+ *                   Library choice: GDN_F32 -> 1, GDN_BF16 -> 64.
+ *   workspace       DEVICE scratch of at least gdn_prefill_workspace_size(...)
+ *                   bytes, 256-byte aligned; contents need no initialisation
+ *                   and are clobbered. Calls that share a workspace must be
+ *                   ordered on one stream.
+ * 0 <= N <= 65535, 0 <= T_total <= 2^24. cu_seqlens is read on the device only;
+ * a cu_seqlens that breaks the rules above gives unspecified results for the
+ * offending sequences but never touches memory outside the stated extents.
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE,
+ * GDN_ERR_CUDA. A bounded device wait that gives up is reported afterwards by
+ * gdn_prefill_device_error on the same workspace.
+ */
+gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
+                       const void *beta, const int32_t *cu_seqlens, int N, int T_total,
+                       const void *conv_state_in, void *conv_state_out,
+                       const float *ssm_state_in, float *ssm_state_out, void *out,
+                       gdn_dtype act, gdn_dtype out_dt, int chunk_size, void *workspace,
+                       size_t ws_bytes, void *stream);
+
+/* Bytes of workspace gdn_prefill needs for these sizes (0 if the arguments are
+ * invalid; never 0 for valid ones). Pure host arithmetic. */
+size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_size);
+
+/* Synchronises `stream`, then reads and clears the device error word that
+ * gdn_prefill keeps at the start of `workspace`: GDN_OK, or GDN_ERR_TIMEOUT if a
+ * bounded device-side wait gave up since the word was last cleared. */
+gdn_status gdn_prefill_device_error(void *workspace, void *stream);
+
+/* Human-readable name of a status (static storage). */
+const char *gdn_status_string(gdn_status s);
+
+/* Text of the last GDN_ERR_CUDA / GDN_ERR_INVALID_ARG seen by the calling host
+ * thread (thread-local, static storage; "" if none). */
+const char *gdn_last_error(void);
+
+/* GDN_ABI_VERSION of the built library. */
+int gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,148 @@
+"""The C ABI without a GPU.
+
+These tests check that libgdn.so loads and exports every function
+include/gdn.h declares, and that the host-side argument checks reject bad
+calls before any CUDA work. No call here reaches the device: every case
+fails a check first, which the status and message confirm.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from gated_deltanet_linear_02_gb300 import build, ops
+    build.build()
+    return ops
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(gdn_[a-z_0-9]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gdn_conv_step", "gdn_decode_step", "gdn_prefill", "gdn_prefill_workspace_size",
+              "gdn_prefill_device_error", "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ops):
+    L = ops.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), f"{n} declared in gdn.h but not exported by libgdn.so"
+
+
+def test_exports_are_c_symbols(ops):
+    # extern "C": the dynamic symbol table holds the plain names (no C++ mangling)
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", ops.LIB_PATH], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in declared_functions():
+        assert n in syms
+
+
+def test_version_and_status_strings(ops):
+    assert ops.abi_version() == 1
+    assert ops.status_string(ops.GDN_OK) == "GDN_OK"
+    assert ops.status_string(ops.GDN_ERR_TIMEOUT) == "GDN_ERR_TIMEOUT"
+    assert ops.status_string(99) == "GDN_STATUS_UNKNOWN"
+
+
+def test_workspace_size_arithmetic(ops):
+    L = ops.lib()
+    # per-token bytes of the exact scan path: x (8192) + gates (64) + y (4096) fp32, plus a 256 B header
+    for T in (0, 1, 64, 4096):
+        body = 4 * (8192 + 64 + 4096) * T
+        assert L.gdn_prefill_workspace_size(1, T, ops.GDN_F32, 1) == 256 + ((body + 255) // 256) * 256
+    assert L.gdn_prefill_workspace_size(-1, 10, ops.GDN_F32, 1) == 0
+    assert L.gdn_prefill_workspace_size(1, -1, ops.GDN_F32, 1) == 0
+    assert L.gdn_prefill_workspace_size(1, 10, 7, 1) == 0
+    assert L.gdn_prefill_workspace_size(1, 10, ops.GDN_F32, 3) == 0
+    assert L.gdn_prefill_workspace_size(70000, 10, ops.GDN_F32, 1) == 0
+
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced: every case fails a host check first
+MIS = 0x10004           # misaligned
+
+
+def _params(ops, **kw):
+    p = ops.gdn_params(FAKE, FAKE, FAKE, FAKE, 1e-6, 1e-6)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_decode_argument_checks(ops):
+    L = ops.lib()
+    p = _params(ops)
+    ok_args = [FAKE] * 7
+    call = lambda pp, args, B, act=ops.GDN_BF16, od=ops.GDN_F32: L.gdn_decode_step(
+        ctypes.byref(pp) if pp is not None else None, *args, B, act, od, None)
+    assert call(p, ok_args, 0) == ops.GDN_OK                                # empty batch: no-op
+    assert call(p, ok_args, -1) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, ok_args, 65536) == ops.GDN_ERR_INVALID_ARG
+    assert call(None, ok_args, 4) == ops.GDN_ERR_INVALID_ARG
+    assert "params" in ops.last_error()
+    assert call(p, ok_args, 4, act=5) == ops.GDN_ERR_INVALID_ARG
+    for i in range(7):
+        bad = list(ok_args)
+        bad[i] = 0
+        assert call(p, bad, 4) == ops.GDN_ERR_INVALID_ARG
+        bad[i] = MIS
+        assert call(p, bad, 4) == ops.GDN_ERR_INVALID_ARG
+    assert call(_params(ops, conv_w=MIS), ok_args, 4) == ops.GDN_ERR_INVALID_ARG
+    assert call(_params(ops, norm_eps=-1.0), ok_args, 4) == ops.GDN_ERR_INVALID_ARG
+    assert call(_params(ops, l2_eps=float("nan")), ok_args, 4) == ops.GDN_ERR_INVALID_ARG
+
+
+def test_conv_step_argument_checks(ops):
+    L = ops.lib()
+    assert L.gdn_conv_step(FAKE, FAKE, FAKE + 16, FAKE + 32, 0, ops.GDN_BF16, None) == ops.GDN_OK
+    assert L.gdn_conv_step(FAKE, FAKE, FAKE, FAKE + 32, 3, ops.GDN_BF16, None) == ops.GDN_ERR_INVALID_ARG
+    assert L.gdn_conv_step(None, FAKE, FAKE + 16, FAKE + 32, 3, ops.GDN_BF16, None) == ops.GDN_ERR_INVALID_ARG
+    assert L.gdn_conv_step(FAKE, FAKE, FAKE + 16, FAKE + 32, 3, 2, None) == ops.GDN_ERR_INVALID_ARG
+
+
+def test_prefill_argument_checks(ops):
+    L = ops.lib()
+    p = _params(ops)
+
+    def call(N=2, T=100, chunk=1, act=ops.GDN_F32, ws=FAKE, ws_bytes=1 << 40, cu=FAKE, ins=(None,) * 4,
+             streams=(FAKE,) * 4, out=FAKE, pp=p):
+        return L.gdn_prefill(ctypes.byref(pp), *streams, cu, N, T, *ins, out, act, ops.GDN_F32, chunk, ws,
+                             ws_bytes, None)
+
+    assert call(N=0, T=0) == ops.GDN_OK
+    assert call(N=0, T=5) == ops.GDN_ERR_INVALID_ARG
+    assert call(N=-1) == ops.GDN_ERR_INVALID_ARG
+    assert call(T=-1) == ops.GDN_ERR_INVALID_ARG
+    assert call(T=(1 << 24) + 1) == ops.GDN_ERR_INVALID_ARG
+    assert call(N=65536) == ops.GDN_ERR_INVALID_ARG
+    assert call(chunk=7) == ops.GDN_ERR_UNSUPPORTED
+    assert call(cu=None) == ops.GDN_ERR_INVALID_ARG
+    assert call(out=MIS) == ops.GDN_ERR_INVALID_ARG
+    assert call(out=None) == ops.GDN_ERR_INVALID_ARG
+    assert call(streams=(FAKE, None, FAKE, FAKE)) == ops.GDN_ERR_INVALID_ARG
+    assert call(ins=(MIS, None, None, None)) == ops.GDN_ERR_INVALID_ARG
+    assert call(ws=None) == ops.GDN_ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == ops.GDN_ERR_WORKSPACE          # not 256-byte aligned
+    need = L.gdn_prefill_workspace_size(2, 100, ops.GDN_F32, 1)
+    assert call(ws_bytes=need - 1) == ops.GDN_ERR_WORKSPACE
+    assert "workspace" in ops.last_error()
+
+
+def test_binding_refuses_cpu_tensors(ops):
+    import torch
+    from gated_deltanet_linear_02_gb300 import inputs
+    lp = inputs.layer_params(1)
+    with pytest.raises(ValueError):
+        ops.make_params(lp)           # CPU tensors: the binding only passes device memory
