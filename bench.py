@@ -253,7 +253,7 @@ def run_gpu(args, rank, world, dev):
     barrier_sync()
     sampler.mark(t_wall0, time.time())
     pf_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))
-    assert ops.prefill_device_error(ws) == ops.GDN_OK
+    assert ops.device_error() == ops.GDN_OK
     pf_tok_s = world * PREFILL_T / (pf_ms / 1e3)
     pf_tflops = PREFILL_FLOP_PER_TOKEN * PREFILL_T / (pf_ms / 1e3) / 1e12
     clocks = sampler.stop()
@@ -321,6 +321,48 @@ def cpu_baseline(n_seq=None):
 
 # ------------------------------------------------------------------- main
 
+def profile_case(args):
+    """A small, self-contained run of one path for profilers: no JSON line, no
+    clocks, a few launches on a few GB. ``--case decode``: --layers layers of
+    gdn_decode_step on --batch sequences; ``--case prefill``: gdn_prefill on one
+    sequence of --T tokens."""
+    import torch
+
+    from gated_deltanet_linear_02_gb300 import build as gbuild
+    from gated_deltanet_linear_02_gb300 import inputs as I
+    from gated_deltanet_linear_02_gb300 import ops
+    gbuild.build()
+    dev = torch.device("cuda", 0)
+    n = args.warmup + args.steps
+    if args.case == "decode":
+        Ls = []
+        for layer in range(args.layers):
+            seed = I.seed_of(3, layer)
+            lp = I.layer_params(seed).to(dev)
+            conv, S = I.initial_states(seed, args.batch, torch.bfloat16, device=dev)
+            st = I.streams(seed, args.batch, torch.bfloat16, device=dev, lead=(1,))
+            out = torch.empty(args.batch, I.D_INNER, dtype=torch.bfloat16, device=dev)
+            Ls.append((ops.make_params(lp), conv, S, st, out))
+        for _ in range(n):
+            for cp, conv, S, st, out in Ls:
+                ops.decode_step(None, st.qkv[0], st.z[0], st.alpha[0], st.beta[0], conv, S, out, cparams=cp)
+    else:
+        seed = I.seed_of(2)
+        lp = I.layer_params(seed).to(dev)
+        st = I.streams(seed, args.T, torch.bfloat16, device=dev)
+        cu = I.cu_seqlens([args.T]).to(dev)
+        out = torch.empty(args.T, I.D_INNER, dtype=torch.bfloat16, device=dev)
+        S_out = torch.empty(1, I.HV, I.DV, I.DK, device=dev)
+        ws = torch.empty(ops.prefill_workspace_size(1, args.T, torch.bfloat16, args.chunk), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(n):
+            ops.prefill(lp, st.qkv, st.z, st.alpha, st.beta, cu, out, ssm_state_out=S_out,
+                        chunk_size=args.chunk, workspace=ws)
+        assert ops.device_error() == ops.GDN_OK
+    torch.cuda.synchronize()
+    print(f"profile case {args.case} done: {n} iterations")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -328,7 +370,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["decode", "prefill"], default=None,
+                    help="profiling run of one path (see profile_case); prints no JSON line")
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--layers", type=int, default=1)
+    ap.add_argument("--T", type=int, default=4096)
+    ap.add_argument("--chunk", type=int, default=0)
     args = ap.parse_args()
+    if args.case is not None:
+        profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
 

@@ -1,12 +1,13 @@
 // gdn_api.cu -- the C ABI declared in include/gdn.h: argument checks and
 // dispatch to the kernels. Nothing here allocates or synchronises (except
-// gdn_prefill_device_error, which is documented to).
+// gdn_device_error, which is documented to).
 #include <stdio.h>
 #include <string.h>
 
 #include "gdn_common.cuh"
 
 namespace gdn {
+cudaError_t take_decode_error(unsigned int *word, cudaStream_t s);
 cudaError_t launch_conv_step(const float *, const void *, void *, void *, int, gdn_dtype, cudaStream_t);
 cudaError_t launch_decode_step(const gdn_params *, const void *, const void *, const void *, const void *,
                                void *, float *, void *, int, gdn_dtype, gdn_dtype, cudaStream_t);
@@ -52,7 +53,7 @@ gdn_status check_params(const gdn_params *p)
 constexpr int MAX_B = 65535;
 constexpr int MAX_N = 65535;
 constexpr int MAX_T = 1 << 24;
-constexpr size_t WS_HEADER = 256;   // device error word lives here
+constexpr size_t WS_HEADER = 256;   // keeps the workspace body 256-byte aligned
 
 int resolve_chunk(int chunk_size, gdn_dtype act)
 {
@@ -150,24 +151,17 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
         return fail(GDN_ERR_WORKSPACE, "workspace missing, misaligned (256 B) or too small");
     void *body = static_cast<char *>(workspace) + WS_HEADER;
     cudaStream_t s = (cudaStream_t)stream;
-    // The error word reflects the most recent call on this workspace.
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int), s);
-    if (e == cudaSuccess)
-        e = launch_prefill_scan(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
+    cudaError_t e = launch_prefill_scan(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
                                 ssm_state_in, ssm_state_out, out, act, out_dt, body, s);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_prefill");
 }
 
-gdn_status gdn_prefill_device_error(void *workspace, void *stream)
+gdn_status gdn_device_error(void *stream)
 {
-    if (!ok_ptr(workspace)) return fail(GDN_ERR_INVALID_ARG, "workspace is NULL or misaligned");
     cudaStream_t s = (cudaStream_t)stream;
     unsigned int word = 0;
-    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e == cudaSuccess && word != 0) e = cudaMemsetAsync(workspace, 0, sizeof(word), s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_fail(e, "gdn_prefill_device_error");
+    cudaError_t e = take_decode_error(&word, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gdn_device_error");
     return word == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
 }
 

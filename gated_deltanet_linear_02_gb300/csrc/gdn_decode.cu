@@ -2,28 +2,31 @@
 //
 // Decode is a batched, HBM-bound sweep over the fp32 states. Each 128x128
 // state of one (sequence, V-head) is 64 KiB and makes up 97% of the bytes.
-// So the kernel reads every state exactly once with 128-bit streaming loads,
-// issued before anything else. It does every other step of the SSM block on
-// chip while those loads are in flight, and writes the state back once. The
-// SSM block is the one in "qwen35moe -- Forward-Pass Design (Pantheon port)",
-// sections "Causal conv1d", "Decay gate", "Per-token recurrence" and "Output
-// path".
+// The kernel reads every state once and writes it once, and runs every other
+// step of the SSM block on chip in between. The SSM block is the one in
+// "qwen35moe -- Forward-Pass Design (Pantheon port)", sections "Causal conv1d",
+// "Decay gate", "Per-token recurrence" and "Output path".
 //
-// Work split: one CTA per (sequence, V-head), 256 threads. Warp w owns rows
-// j in [16w, 16w+16) of S^T (value index j; each row is the 128 keys i,
-// contiguous). Lane l holds keys [4l, 4l+4) of each of its rows in registers.
-// All of pred_j, delta_j and y_j depend on row j alone, so the rows need no
-// exchange, only warp-shuffle dot products.
+// The decode kernel is persistent: one CTA of 16 warps per SM. Each CTA walks
+// the work items (sequence b, K-head kh) in turn. An item covers both V-heads
+// that read K-head kh, vh = kh and vh = kh + 16 (the interleaved GQA repeat of
+// the watch-list). So the item's q/k conv channels, and their conv_state, are
+// touched by this CTA alone. No other CTA reads them, and the state shift
+// needs no cross-CTA ordering.
 //
-// V-heads vh and vh+16 read the same q/k channels, because of the interleaved
-// GQA repeat (V-head vh uses K-head vh % 16). Both CTAs must read those
-// conv_state channels before one of them shifts the state. The two CTAs form
-// a 2-CTA cluster for this: each arrives on the cluster barrier as soon as it
-// has read, and waits on it only at its very end. Then the vh < 16 CTA writes
-// the shared q/k rows. The v rows belong to one CTA and are written at once.
+// The states stream through a ring of three 64 KiB shared-memory slots. Thread
+// 0 fills them with TMA bulk copies (cp.async.bulk), which complete on one
+// mbarrier per slot, and keeps two states in flight ahead of the one being
+// computed. Warp w computes rows j in [8w, 8w+8) of S^T (value index j, whose
+// 128 keys i are contiguous). Lane l holds keys [4l, 4l+4). pred_j, delta_j and
+// y_j depend on row j alone, so a row needs only warp-shuffle dot products.
+// The updated row goes straight back to global memory with a streaming store.
+#include "gdn_async.cuh"
 #include "gdn_common.cuh"
 
 namespace gdn {
+
+__device__ unsigned int g_decode_error;   // GDN_ERR_TIMEOUT if a bounded wait gave up
 
 // ------------------------------------------------------------------ conv step
 
@@ -55,130 +58,162 @@ struct DecodeArgs {
     void *conv_state;
     float *ssm_state;
     void *out;
+    int n_items;   // B * 16
 };
 
-constexpr int DEC_THREADS = 256;
-constexpr int DEC_ROWS_PER_WARP = DV / (DEC_THREADS / 32);   // 16
+constexpr int DEC_THREADS = 512;
+constexpr int DEC_WARPS = DEC_THREADS / 32;
+constexpr int DEC_ROWS_PER_WARP = DV / DEC_WARPS;         // 8
+constexpr int DEC_SLOTS = 3;
+constexpr uint32_t STATE_BYTES = DV * DK * sizeof(float); // 64 KiB
+constexpr int DEC_COPIES = 4;                              // bulk copies per state
 
-__device__ __forceinline__ void cluster_arrive_release()
+struct DecodeSmem {
+    float slot[DEC_SLOTS][DV * DK];
+    uint64_t full[DEC_SLOTS];
+    float q[DK], k[DK], v[2][DV], y[2][DV];
+    float red[32];
+    float gate[2][2];
+    int pending[DEC_SLOTS];   // state number whose load is outstanding in each slot, or -1
+    int abort;
+};
+constexpr size_t DEC_SMEM = sizeof(DecodeSmem) + 128;   // + alignment slack
+
+// Issues the TMA load of this CTA's state number `s` (item s/2, half s%2) into
+// slot s%3. Caller: thread 0 only.
+__device__ __forceinline__ void decode_issue_load(DecodeSmem &sm, const DecodeArgs &a, int s)
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+    const int item = blockIdx.x + (s >> 1) * gridDim.x;
+    if (item >= a.n_items) return;
+    const int b = item / HK, kh = item % HK, vh = kh + HK * (s & 1);
+    const char *src = reinterpret_cast<const char *>(a.ssm_state + ((size_t)b * HV + vh) * (DV * DK));
+    const int slot = s % DEC_SLOTS;
+    sm.pending[slot] = s;
+    const uint32_t bar = smem_u32(&sm.full[slot]);
+    const uint32_t dst = smem_u32(sm.slot[slot]);
+    mbar_arrive_expect_tx(bar, STATE_BYTES);
+#pragma unroll
+    for (int c = 0; c < DEC_COPIES; ++c)
+        bulk_g2s(dst + c * (STATE_BYTES / DEC_COPIES), src + c * (STATE_BYTES / DEC_COPIES),
+                 STATE_BYTES / DEC_COPIES, bar);
 }
 
 template <typename TA, typename TO>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DEC_THREADS, 2)
-decode_step_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const DecodeArgs a)
 {
-    const int kh = blockIdx.x >> 1;          // K-head shared by the cluster pair
-    const int half = blockIdx.x & 1;         // 0: vh = kh, 1: vh = kh + 16
-    const int vh = kh + HK * half;
-    const size_t b = blockIdx.y;
+    extern __shared__ unsigned char smem_raw[];
+    DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // (1) Stream this warp's 16 state rows into registers first: 64 KiB per CTA
-    //     in flight while the prologue below runs.
-    float *S = a.ssm_state + (b * HV + vh) * (size_t)(DV * DK);
-    float4 st[DEC_ROWS_PER_WARP];
-#pragma unroll
-    for (int r = 0; r < DEC_ROWS_PER_WARP; ++r)
-        st[r] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(warp * DEC_ROWS_PER_WARP + r) * DK) + lane);
-
-    __shared__ float s_q[DK], s_k[DK], s_v[DV], s_y[DV];
-    __shared__ float s_red[16];
-    __shared__ float s_gate[2];
-
-    // (2) Causal conv + SiLU ("Causal conv1d"): thread t convolves q channel t
-    //     (t < 128) or k channel t-128 of K-head kh, and t < 128 also v channel t
-    //     of V-head vh.
-    const TA *x = static_cast<const TA *>(a.qkv) + b * CC;
-    TA *cs = static_cast<TA *>(a.conv_state) + b * (size_t)(KC - 1) * CC;
-    const int cA = (tid < DK) ? (Q_OFF + kh * DK + tid) : (K_OFF + kh * DK + tid - DK);
-    const float4 wA = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + cA);
-    const TA a0 = cs[cA], a1 = cs[CC + cA], a2 = cs[2 * CC + cA], ax = x[cA];
-    const float xA = silu_f(wA.x * to_f(a0) + wA.y * to_f(a1) + wA.z * to_f(a2) + wA.w * to_f(ax));
-    float xV = 0.0f;
-    if (tid < DV) {
-        const int cV = V_OFF + vh * DV + tid;
-        const float4 wV = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + cV);
-        const TA v0 = cs[cV], v1 = cs[CC + cV], v2 = cs[2 * CC + cV], vx = x[cV];
-        xV = silu_f(wV.x * to_f(v0) + wV.y * to_f(v1) + wV.z * to_f(v2) + wV.w * to_f(vx));
-        // v channels belong to this CTA alone: shift them now.
-        cs[cV] = v1;
-        cs[CC + cV] = v2;
-        cs[2 * CC + cV] = vx;
-    }
-    // Our reads of the shared q/k conv_state are done (their values feed xA).
-    cluster_arrive_release();
-
-    // (3) L2 norms of q and k over the head dim ("L2-normalize q and k over head
-    //     dim (not RMS)"): warps 0-3 hold q, warps 4-7 hold k.
-    {
-        const float ss = warp_sum(xA * xA);
-        if (lane == 0) s_red[warp] = ss;
-    }
     if (tid == 0) {
-        const float al = to_f(static_cast<const TA *>(a.alpha)[b * HV + vh]);
-        const float be = to_f(static_cast<const TA *>(a.beta)[b * HV + vh]);
-        float ga, gb;
-        gates_f(a.A_log[vh], a.dt_bias[vh], al, be, ga, gb);
-        s_gate[0] = ga;
-        s_gate[1] = gb;
+        for (int i = 0; i < DEC_SLOTS; ++i) {
+            mbar_init(smem_u32(&sm.full[i]), 1);
+            sm.pending[i] = -1;
+        }
+        sm.abort = 0;
+        fence_mbar_init();
     }
     __syncthreads();
-    if (tid < DK) {
-        const float inv = rsqrtf(s_red[0] + s_red[1] + s_red[2] + s_red[3] + a.l2_eps);
-        s_q[tid] = xA * inv;
-        s_v[tid] = xV;
-    } else {
-        const float inv = rsqrtf(s_red[4] + s_red[5] + s_red[6] + s_red[7] + a.l2_eps);
-        s_k[tid - DK] = xA * inv;
-    }
-    __syncthreads();
+    if (tid == 0)
+        for (int s = 0; s < DEC_SLOTS; ++s) decode_issue_load(sm, a, s);
 
-    // (4) Recurrence (a)-(d) on this warp's rows; rows are independent.
-    const float4 k4 = reinterpret_cast<const float4 *>(s_k)[lane];
-    const float4 q4 = reinterpret_cast<const float4 *>(s_q)[lane];
-    const float dec = s_gate[0], beta = s_gate[1];
     const float scale = rsqrtf((float)DK);
+    for (int m = 0;; ++m) {
+        const int item = blockIdx.x + m * gridDim.x;
+        if (item >= a.n_items) break;
+        const size_t b = item / HK;
+        const int kh = item % HK;
+
+        // ---- item prologue: conv + SiLU of the item's 512 channels (q and k of
+        //      K-head kh, v of both V-heads), state shift, L2 norms, gates.
+        {
+            int c;
+            if (tid < 128) c = Q_OFF + kh * DK + tid;
+            else if (tid < 256) c = K_OFF + kh * DK + (tid - 128);
+            else if (tid < 384) c = V_OFF + kh * DV + (tid - 256);
+            else c = V_OFF + (kh + HK) * DV + (tid - 384);
+            const TA *x = static_cast<const TA *>(a.qkv) + b * CC;
+            TA *cs = static_cast<TA *>(a.conv_state) + b * (size_t)(KC - 1) * CC;
+            const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + c);
+            const TA s0 = cs[c], s1 = cs[CC + c], s2 = cs[2 * CC + c], xc = x[c];
+            const float xh = silu_f(w.x * to_f(s0) + w.y * to_f(s1) + w.z * to_f(s2) + w.w * to_f(xc));
+            cs[c] = s1;                       // this CTA owns channel c of sequence b
+            cs[CC + c] = s2;
+            cs[2 * CC + c] = xc;
+            const float ss = warp_sum(xh * xh);
+            if (lane == 0) sm.red[warp] = ss;
+            if (tid < 2) {
+                const int vh = kh + HK * tid;
+                float ga, gb;
+                gates_f(a.A_log[vh], a.dt_bias[vh], to_f(static_cast<const TA *>(a.alpha)[b * HV + vh]),
+                        to_f(static_cast<const TA *>(a.beta)[b * HV + vh]), ga, gb);
+                sm.gate[tid][0] = ga;
+                sm.gate[tid][1] = gb;
+            }
+            __syncthreads();
+            if (tid < 128) sm.q[tid] = xh * rsqrtf(sm.red[0] + sm.red[1] + sm.red[2] + sm.red[3] + a.l2_eps);
+            else if (tid < 256) sm.k[tid - 128] = xh * rsqrtf(sm.red[4] + sm.red[5] + sm.red[6] + sm.red[7] + a.l2_eps);
+            else sm.v[(tid - 256) >> 7][tid & 127] = xh;
+            __syncthreads();
+        }
+
+        // ---- the two states of the item: recurrence (a)-(d) row by row
+        const float4 k4 = reinterpret_cast<const float4 *>(sm.k)[lane];
+        const float4 q4 = reinterpret_cast<const float4 *>(sm.q)[lane];
+        for (int h = 0; h < 2; ++h) {
+            const int s = 2 * m + h;
+            const int slot = s % DEC_SLOTS;
+            if (!mbar_wait_bounded(smem_u32(&sm.full[slot]), (uint32_t)((s / DEC_SLOTS) & 1))) sm.abort = 1;
+            __syncthreads();
+            if (sm.abort) break;
+            const int vh = kh + HK * h;
+            float *Sg = a.ssm_state + (b * HV + vh) * (size_t)(DV * DK);
+            const float dec = sm.gate[h][0], beta = sm.gate[h][1];
+            const float4 *src = reinterpret_cast<const float4 *>(sm.slot[slot]);
 #pragma unroll
-    for (int r = 0; r < DEC_ROWS_PER_WARP; ++r) {
-        const int j = warp * DEC_ROWS_PER_WARP + r;
-        float4 s = st[r];
-        s.x *= dec; s.y *= dec; s.z *= dec; s.w *= dec;                       // (a)
-        const float pred = warp_sum(s.x * k4.x + s.y * k4.y + s.z * k4.z + s.w * k4.w);   // (b)
-        const float delta = (s_v[j] - pred) * beta;
-        s.x += k4.x * delta; s.y += k4.y * delta; s.z += k4.z * delta; s.w += k4.w * delta;  // (c)
-        const float yq = warp_sum(s.x * q4.x + s.y * q4.y + s.z * q4.z + s.w * q4.w);       // (d)
-        __stcs(reinterpret_cast<float4 *>(S + (size_t)j * DK) + lane, s);
-        if (lane == 0) s_y[j] = yq * scale;
-    }
-    __syncthreads();
+            for (int r = 0; r < DEC_ROWS_PER_WARP; ++r) {
+                const int j = warp * DEC_ROWS_PER_WARP + r;
+                float4 st = src[j * (DK / 4) + lane];
+                st.x *= dec; st.y *= dec; st.z *= dec; st.w *= dec;                                   // (a)
+                const float pred = warp_sum(st.x * k4.x + st.y * k4.y + st.z * k4.z + st.w * k4.w);    // (b)
+                const float delta = (sm.v[h][j] - pred) * beta;
+                st.x += k4.x * delta; st.y += k4.y * delta; st.z += k4.z * delta; st.w += k4.w * delta; // (c)
+                const float yq = warp_sum(st.x * q4.x + st.y * q4.y + st.z * q4.z + st.w * q4.w);      // (d)
+                __stcs(reinterpret_cast<float4 *>(Sg + (size_t)j * DK) + lane, st);
+                if (lane == 0) sm.y[h][j] = yq * scale;
+            }
+            __syncthreads();                     // every warp is done reading this slot
+            if (tid == 0) {
+                sm.pending[slot] = -1;
+                fence_proxy_async_smem();
+                decode_issue_load(sm, a, s + DEC_SLOTS);
+            }
+        }
+        if (sm.abort) break;
 
-    // (5) Gated RMSNorm over this head's 128 outputs, times silu(z) ("Output path").
-    float y = 0.0f;
-    if (tid < DV) {
-        y = s_y[tid];
-        const float ss = warp_sum(y * y);
-        if (lane == 0) s_red[8 + warp] = ss;
+        // ---- gated RMSNorm of both heads, times silu(z) ("Output path")
+        if (tid < 256) {
+            const int h = tid >> 7, j = tid & 127;
+            const float y = sm.y[h][j];
+            const float ss = warp_sum(y * y);
+            if (lane == 0) sm.red[16 + warp] = ss;
+        }
+        __syncthreads();
+        if (tid < 256) {
+            const int h = tid >> 7, j = tid & 127;
+            const float *rr4 = sm.red + 16 + 4 * h;
+            const float rr = rsqrtf((rr4[0] + rr4[1] + rr4[2] + rr4[3]) * (1.0f / DV) + a.norm_eps);
+            const size_t o = b * DI + (size_t)(kh + HK * h) * DV + j;
+            const float zz = to_f(static_cast<const TA *>(a.z)[o]);
+            static_cast<TO *>(a.out)[o] = from_f<TO>(sm.y[h][j] * rr * a.norm_w[j] * silu_f(zz));
+        }
+        // the next prologue writes q/k/v/red[0..7]/gate, none of which the lines above read
     }
-    __syncthreads();
-    if (tid < DV) {
-        const float ms = (s_red[8] + s_red[9] + s_red[10] + s_red[11]) * (1.0f / DV);
-        const float rr = rsqrtf(ms + a.norm_eps);
-        const float zz = to_f(static_cast<const TA *>(a.z)[b * DI + vh * DV + tid]);
-        static_cast<TO *>(a.out)[b * DI + vh * DV + tid] = from_f<TO>(y * rr * a.norm_w[tid] * silu_f(zz));
-    }
-
-    // (6) Shift the shared q/k conv_state rows once both CTAs of the pair have read them.
-    cluster_wait_acquire();
-    if (half == 0) {
-        cs[cA] = a1;
-        cs[CC + cA] = a2;
-        cs[2 * CC + cA] = ax;
+    if (sm.abort && tid == 0) {
+        atomicExch(&g_decode_error, (unsigned int)GDN_ERR_TIMEOUT);
+        // let the copies still in flight land before the CTA's shared memory is released
+        for (int i = 0; i < DEC_SLOTS; ++i)
+            if (sm.pending[i] >= 0) mbar_wait_bounded(smem_u32(&sm.full[i]), (uint32_t)((sm.pending[i] / DEC_SLOTS) & 1));
     }
 }
 
@@ -197,6 +232,32 @@ cudaError_t launch_conv_step(const float *conv_w, const void *x_in, void *x_out,
     return cudaGetLastError();
 }
 
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+template <typename TA, typename TO>
+static cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<TA, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)DEC_SMEM);
+    if (e != cudaSuccess) return e;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return cudaErrorInvalidDevice;
+    const int grid = a.n_items < n_sm ? a.n_items : n_sm;
+    decode_step_kernel<TA, TO><<<grid, DEC_THREADS, DEC_SMEM, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode_step(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
                                const void *beta, void *conv_state, float *ssm_state, void *out, int B,
                                gdn_dtype act, gdn_dtype out_dt, cudaStream_t s)
@@ -206,15 +267,23 @@ cudaError_t launch_decode_step(const gdn_params *p, const void *qkv, const void 
     a.norm_eps = p->norm_eps; a.l2_eps = p->l2_eps;
     a.qkv = qkv; a.z = z; a.alpha = alpha; a.beta = beta;
     a.conv_state = conv_state; a.ssm_state = ssm_state; a.out = out;
-    dim3 grid(HV, B);   // x = 2*kh + half; consecutive pairs form the clusters
-    if (act == GDN_F32) {
-        if (out_dt == GDN_F32) decode_step_kernel<float, float><<<grid, DEC_THREADS, 0, s>>>(a);
-        else decode_step_kernel<float, bf16><<<grid, DEC_THREADS, 0, s>>>(a);
-    } else {
-        if (out_dt == GDN_F32) decode_step_kernel<bf16, float><<<grid, DEC_THREADS, 0, s>>>(a);
-        else decode_step_kernel<bf16, bf16><<<grid, DEC_THREADS, 0, s>>>(a);
-    }
-    return cudaGetLastError();
+    a.n_items = B * HK;
+    if (act == GDN_F32)
+        return out_dt == GDN_F32 ? launch_decode_t<float, float>(a, s) : launch_decode_t<float, bf16>(a, s);
+    return out_dt == GDN_F32 ? launch_decode_t<bf16, float>(a, s) : launch_decode_t<bf16, bf16>(a, s);
+}
+
+// Reads and clears this file's device error word (synchronous on `s`).
+cudaError_t take_decode_error(unsigned int *word, cudaStream_t s)
+{
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_decode_error, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && *word != 0)
+        e = cudaMemcpyToSymbolAsync(g_decode_error, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e;
 }
 
 }  // namespace gdn

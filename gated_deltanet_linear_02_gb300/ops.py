@@ -58,8 +58,8 @@ def lib() -> ctypes.CDLL:
             [_int, _int, _int, _vp, _sz, _vp]
         L.gdn_prefill_workspace_size.restype = _sz
         L.gdn_prefill_workspace_size.argtypes = [_int, _int, _int, _int]
-        L.gdn_prefill_device_error.restype = _int
-        L.gdn_prefill_device_error.argtypes = [_vp, _vp]
+        L.gdn_device_error.restype = _int
+        L.gdn_device_error.argtypes = [_vp]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_status_string.argtypes = [_int]
         L.gdn_last_error.restype = ctypes.c_char_p
@@ -186,6 +186,7 @@ def prefill(params, qkv, z, alpha, beta, cu_seqlens, out, conv_state_in=None, co
     return workspace
 
 
-def prefill_device_error(workspace, stream=None) -> int:
-    """Synchronises the stream; GDN_OK or GDN_ERR_TIMEOUT for the last prefill on this workspace."""
-    return lib().gdn_prefill_device_error(_ptr(workspace, "workspace"), _stream(stream))
+def device_error(stream=None) -> int:
+    """Synchronises the stream, then reads and clears the library's device error
+    word: GDN_OK, or GDN_ERR_TIMEOUT if a bounded device-side wait gave up."""
+    return lib().gdn_device_error(_stream(stream))

@@ -23,7 +23,7 @@
  *    after a call returns.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). Every call only enqueues work on that stream and returns; no call
- *    synchronises, except gdn_prefill_device_error, which says so.
+ *    synchronises, except gdn_device_error, which says so.
  *  - Activations (qkv, z, alpha, beta, conv_state) all use one dtype `act`;
  *    `out_dt` is the dtype of `out`. Parameters and the SSM state are fp32.
  *  - The SSM state of one (sequence, V-head) is the page's S[i][j] (i = key
@@ -135,7 +135,7 @@ gdn_status gdn_decode_step(const gdn_params *p, const void *qkv, const void *z,
  * offending sequences but never touches memory outside the stated extents.
  * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE,
  * GDN_ERR_CUDA. A bounded device wait that gives up is reported afterwards by
- * gdn_prefill_device_error on the same workspace.
+ * gdn_device_error.
  */
 gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
                        const void *beta, const int32_t *cu_seqlens, int N, int T_total,
@@ -148,10 +148,13 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
  * invalid; never 0 for valid ones). Pure host arithmetic. */
 size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_size);
 
-/* Synchronises `stream`, then reads and clears the device error word that
- * gdn_prefill keeps at the start of `workspace`: GDN_OK, or GDN_ERR_TIMEOUT if a
- * bounded device-side wait gave up since the word was last cleared. */
-gdn_status gdn_prefill_device_error(void *workspace, void *stream);
+/* Device-side waits (on TMA copies and tensor-core completions) are bounded:
+ * a wait that gives up leaves its kernel early, leaves that call's outputs
+ * unspecified, and records GDN_ERR_TIMEOUT in a library-wide error word of the
+ * current device. This call synchronises `stream`, then reads and clears that
+ * word: GDN_OK, or GDN_ERR_TIMEOUT if any kernel of this library on the
+ * current device gave up since the word was last cleared. */
+gdn_status gdn_device_error(void *stream);
 
 /* Human-readable name of a status (static storage). */
 const char *gdn_status_string(gdn_status s);

@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gdn_conv_step", "gdn_decode_step", "gdn_prefill", "gdn_prefill_workspace_size",
-              "gdn_prefill_device_error", "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
+              "gdn_device_error", "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
         assert n in names
 
 

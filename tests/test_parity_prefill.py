@@ -35,7 +35,7 @@ def gpu_prefill(ops, lp, st, lengths, conv0, S0, out_dtype, chunk, pass_states=T
         sout = torch.full((N, I.HV, I.DV, I.DK), float("nan"), dtype=torch.float32, device=DEV)
     ws = ops.prefill(lp.to(DEV), s.qkv, s.z, s.alpha, s.beta, cu, out, conv_state_in=cin, conv_state_out=cout,
                      ssm_state_in=sin, ssm_state_out=sout, chunk_size=chunk)
-    assert ops.prefill_device_error(ws) == ops.GDN_OK
+    assert ops.device_error() == ops.GDN_OK
     return out.cpu(), cout.cpu(), sout.cpu()
 
 
