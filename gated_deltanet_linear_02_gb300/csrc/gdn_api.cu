@@ -15,6 +15,11 @@ size_t scan_workspace_bytes(int T_total);
 cudaError_t launch_prefill_scan(const gdn_params *, const void *, const void *, const void *, const void *,
                                 const int32_t *, int, int, const void *, void *, const float *, float *,
                                 void *, gdn_dtype, gdn_dtype, void *, cudaStream_t);
+size_t chunk_workspace_bytes(int N, int T_total);
+cudaError_t launch_prefill_chunked(const gdn_params *, const void *, const void *, const void *, const void *,
+                                   const int32_t *, int, int, const void *, void *, const float *, float *, void *,
+                                   gdn_dtype, void *, cudaStream_t);
+cudaError_t take_chunk_error(unsigned int *word, cudaStream_t s);
 }  // namespace gdn
 
 using namespace gdn;
@@ -55,10 +60,11 @@ constexpr int MAX_N = 65535;
 constexpr int MAX_T = 1 << 24;
 constexpr size_t WS_HEADER = 256;   // keeps the workspace body 256-byte aligned
 
+// chunk_size 0 = library choice: the exact scan for fp32 activations, the
+// chunked tensor-core form for bf16 activations.
 int resolve_chunk(int chunk_size, gdn_dtype act)
 {
-    (void)act;
-    if (chunk_size == 0) return 1;
+    if (chunk_size == 0) return act == GDN_BF16 ? 64 : 1;
     return chunk_size;
 }
 
@@ -119,6 +125,7 @@ size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_s
     const int ch = resolve_chunk(chunk_size, act);
     size_t body = 0;
     if (ch == 1) body = scan_workspace_bytes(T_total);
+    else if (ch == 64 && act == GDN_BF16) body = chunk_workspace_bytes(N, T_total);
     else return 0;
     return WS_HEADER + ((body + 255) & ~(size_t)255);
 }
@@ -137,7 +144,9 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
         return GDN_OK;
     }
     const int ch = resolve_chunk(chunk_size, act);
-    if (ch != 1) return fail(GDN_ERR_UNSUPPORTED, "chunk_size must be 0 or 1 in this build");
+    if (ch != 1 && ch != 64) return fail(GDN_ERR_UNSUPPORTED, "chunk_size must be 0, 1 or 64");
+    if (ch == 64 && act != GDN_BF16)
+        return fail(GDN_ERR_UNSUPPORTED, "the chunked tensor-core form needs bf16 activations");
     gdn_status st = check_params(p);
     if (st != GDN_OK) return st;
     if (!ok_ptr(cu_seqlens) || (T_total > 0 && (!ok_ptr(qkv) || !ok_ptr(z) || !ok_ptr(alpha) ||
@@ -151,8 +160,13 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
         return fail(GDN_ERR_WORKSPACE, "workspace missing, misaligned (256 B) or too small");
     void *body = static_cast<char *>(workspace) + WS_HEADER;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = launch_prefill_scan(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
+    cudaError_t e;
+    if (ch == 1)
+        e = launch_prefill_scan(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
                                 ssm_state_in, ssm_state_out, out, act, out_dt, body, s);
+    else
+        e = launch_prefill_chunked(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
+                                   ssm_state_in, ssm_state_out, out, out_dt, body, s);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_prefill");
 }
 
@@ -160,9 +174,11 @@ gdn_status gdn_device_error(void *stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
     unsigned int word = 0;
+    unsigned int word2 = 0;
     cudaError_t e = take_decode_error(&word, s);
+    if (e == cudaSuccess) e = take_chunk_error(&word2, s);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_error");
-    return word == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
+    return (word | word2) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -1,0 +1,669 @@
+// gdn_chunk.cu -- chunked (WY / UT-transform) prefill on tcgen05 tensor cores,
+// for bf16 activations with fp32 state (chunk_size 64).
+//
+// The recurrence is the per-token delta rule of "qwen35moe -- Forward-Pass
+// Design (Pantheon port)", section "Per-token recurrence". The pages say only
+// that prefill may be evaluated as a token scan or reorganised into blocks
+// ("Optimizing on-device inference for Apple silicon", the section on the three
+// workload shapes). The block form used here is an exact re-association of
+// that recurrence, written out by plain algebra. Within a chunk of n <= 64
+// tokens entering with state S0, let G_r = sum_{s<=r} g_s and gamma_r = exp(G_r):
+//   L    = strict_lower(exp(G_r - G_s) k_r.k_s),   T = (I + diag(b) L)^-1 diag(b)
+//   U    = T V,  W = T diag(gamma) K,  Vnew = U - W S0   (= the per-token deltas)
+//   Y    = scale (diag(gamma) Q S0 + (Mask o Q K^T) Vnew),  Mask_rs = exp(G_r-G_s), s<=r
+//   Send = gamma_n S0 + K^T diag(exp(G_n - G_s)) Vnew
+// Every exponent is <= 0 (r >= s); the inverse decay is never formed.
+//
+// Two kernels:
+//  prep  (one CTA per (chunk, K-head); both V-heads of the GQA pair). This is
+//        the S-independent part: conv + SiLU, L2 norms, gates, K K^T and Q K^T
+//        (tf32 MMAs), the unit-lower triangular solve for T (fp32, one column
+//        per thread), then U and W (tf32 MMAs). It writes per (chunk, V-head)
+//        operand tiles to the workspace, already in the shared-memory layout
+//        the carry kernel feeds to its MMAs.
+//  carry (one CTA per (sequence, V-head)). This is the sequential chain over
+//        the chunks. The state lives in tensor memory (fp32) and as a bf16 copy
+//        in shared memory (the A operand of W S0 and Q S0). Per chunk: MMA (W S0,
+//        Q S0) -> Vnew = U - W S0 -> MMA (P Vnew, K^T Vnew into the state) ->
+//        state copy and decay -> gated RMSNorm . silu(z) of the chunk's output.
+// Operand precision: the products whose rounding reaches the tolerance budget
+// (U = T V, Q K^T, P Vnew, the state update) use tf32 operands, rounded to
+// nearest when stored. W S0 and Q S0 take bf16 operands (kind::f16). All
+// accumulation is fp32.
+#include "gdn_async.cuh"
+#include "gdn_common.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+__device__ unsigned int g_chunk_error;   // GDN_ERR_TIMEOUT if a bounded wait gave up
+
+constexpr int CH = 64;                    // chunk length
+
+// Per (chunk, V-head) blob in the workspace. W | Q~ are contiguous (one bulk
+// copy), and P | K~^T are contiguous (another bulk copy).
+constexpr uint32_t BLOB_W = 0;         // W [t][i], bf16, K-major (Kd 128)        16 KiB
+constexpr uint32_t BLOB_Q = 16384;     // Q~ = diag(gamma) Q [t][i], bf16, K-major  16 KiB
+constexpr uint32_t BLOB_P = 32768;     // P = Mask o Q K^T [t][s], tf32, K-major    16 KiB
+constexpr uint32_t BLOB_KT = 49152;    // K~^T [i][t], K~ = diag(exp(G_n-G_t)) K    32 KiB
+constexpr uint32_t BLOB_U = 81920;     // U [t][j], fp32 row-major                  32 KiB
+constexpr uint32_t BLOB_G = 114688;    // gamma_n of the chunk (fp32)
+constexpr size_t BLOB_BYTES = 114944;
+
+struct ChunkArgs {
+    const float *conv_w, *A_log, *dt_bias, *norm_w;
+    float norm_eps, l2_eps;
+    const bf16 *qkv, *z, *alpha, *beta;
+    const int32_t *cu;
+    int N, T_total, max_chunks;
+    const bf16 *cs_in;
+    const float *S_in;
+    float *S_out;
+    void *out;
+    int32_t *chunk_off;       // [N+1]: first global chunk of each sequence
+    unsigned char *blobs;     // [max_chunks][32] x BLOB_BYTES
+};
+
+__device__ __forceinline__ int cu_clamp(const int32_t *cu, int i, int lo, int hi)
+{
+    return min(max(__ldg(cu + i), lo), hi);
+}
+
+// ------------------------------------------------------------------ schedule
+// chunk_off[n] = sum over m < n of ceil(L_m / 64), clamped to max_chunks.
+__global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t *__restrict__ cu, int N, int T_total,
+                                                              int max_chunks, int32_t *__restrict__ chunk_off)
+{
+    __shared__ int part[1024];
+    const int tid = threadIdx.x;
+    const int per = (N + 1023) / 1024;
+    const int lo = min(tid * per, N), hi = min(lo + per, N);
+    int sum = 0;
+    for (int n = lo; n < hi; ++n) {
+        const int a = cu_clamp(cu, n, 0, T_total), b = cu_clamp(cu, n + 1, a, T_total);
+        sum += (b - a + CH - 1) / CH;
+    }
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int i = 0; i < 1024; ++i) {
+            const int v = part[i];
+            part[i] = run;
+            run += v;
+        }
+        chunk_off[N] = min(run, max_chunks);
+    }
+    __syncthreads();
+    int run = part[tid];
+    for (int n = lo; n < hi; ++n) {
+        chunk_off[n] = min(run, max_chunks);
+        const int a = cu_clamp(cu, n, 0, T_total), b = cu_clamp(cu, n + 1, a, T_total);
+        run += (b - a + CH - 1) / CH;
+    }
+}
+
+// -------------------------------------------------------------------- prep
+constexpr int P1_THREADS = 256;
+constexpr uint32_t S1_QS = 0;          // q^ tf32 [t][i] Kd128; later (Gamma K)^T of head 0 [i][s] Kd64
+constexpr uint32_t S1_KS = 32768;      // k^ tf32 [t][i] Kd128
+constexpr uint32_t S1_VT0 = 65536;     // v^T tf32 [j][s] Kd64, head 0
+constexpr uint32_t S1_VT1 = 98304;     //                    head 1
+constexpr uint32_t S1_LB0 = 131072;    // beta_r * L[r][s], plain fp32 [64][64], head 0
+constexpr uint32_t S1_LB1 = 147456;    //                                        head 1
+constexpr uint32_t S1_TS0 = 163840;    // T tf32 [t][s] Kd64, head 0
+constexpr uint32_t S1_TS1 = 180224;    //                     head 1
+constexpr uint32_t S1_GK1 = 196608;    // (Gamma K)^T tf32 [i][s] Kd64, head 1
+constexpr uint32_t S1_SMALL = 229376;
+struct P1Small {
+    float G[2][CH];     // chunk-local cumulative log-decay per V-head
+    float B[2][CH];     // beta
+    float gam[2][CH];   // exp(G)
+    uint64_t bar;
+    uint32_t tmem;
+    int abort;
+};
+constexpr size_t P1_SMEM = S1_SMALL + sizeof(P1Small) + 128;
+// tensor-memory columns of the prep kernel
+constexpr uint32_t T1_KK = 0, T1_QK = 64, T1_U = 128, T1_W = 256, T1_COLS = 512;
+
+template <int ES> __device__ __forceinline__ uint32_t km(int r, int k, int Kd) { return tc::kmajor_offset<ES>(r, k, Kd); }
+
+__global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkArgs a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+    P1Small &ss = *reinterpret_cast<P1Small *>(sm + S1_SMALL);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = blockIdx.x, kh = blockIdx.y;
+
+    const int n_chunks = __ldg(a.chunk_off + a.N);
+    if (g >= n_chunks) return;                         // uniform for the whole CTA
+    // sequence owning global chunk g: chunk_off[n] <= g < chunk_off[n+1]
+    int lo = 0, hi = a.N;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a.chunk_off + mid) <= g) lo = mid; else hi = mid;
+    }
+    const int n = lo;
+    const int lc = g - __ldg(a.chunk_off + n);        // chunk index inside the sequence
+    const int seq0 = cu_clamp(a.cu, n, 0, a.T_total);
+    const int seqL = cu_clamp(a.cu, n + 1, seq0, a.T_total) - seq0;
+    const int t0 = seq0 + CH * lc;
+    const int nv = max(0, min(CH, seqL - CH * lc));   // valid tokens in this chunk
+
+    float *Qs = reinterpret_cast<float *>(sm + S1_QS);
+    float *Ks = reinterpret_cast<float *>(sm + S1_KS);
+    const uint32_t sbase = smem_u32(sm);
+
+    if (warp == 0) {
+        tc::tmem_alloc(smem_u32(&ss.tmem), T1_COLS);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(&ss.bar), 1);
+        ss.abort = 0;
+        fence_mbar_init();
+    }
+
+    // ---- B. conv + SiLU of the chunk's 512 channels; raw q, k into the tf32
+    //      tiles (normalised below), v^T of both heads straight into their tiles.
+    for (int rep = 0; rep < 2; ++rep) {
+        const int li = tid + P1_THREADS * rep;       // local channel 0..511
+        const int blk = li >> 7, d = li & 127;
+        const int c = blk == 0 ? Q_OFF + kh * DK + d
+                    : blk == 1 ? K_OFF + kh * DK + d
+                    : blk == 2 ? V_OFF + kh * DV + d
+                               : V_OFF + (kh + HK) * DV + d;
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + c);
+        float xm[3];
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {                  // positions -3, -2, -1 of the chunk
+            const int pos = CH * lc - 3 + m;           // relative to the sequence start
+            float v = 0.0f;
+            if (pos >= 0) v = to_f(a.qkv[(size_t)(seq0 + pos) * CC + c]);
+            else if (a.cs_in) v = to_f(a.cs_in[((size_t)n * (KC - 1) + (pos + KC - 1)) * CC + c]);
+            xm[m] = v;
+        }
+        unsigned char *dst = blk == 0 ? sm + S1_QS : blk == 1 ? sm + S1_KS : blk == 2 ? sm + S1_VT0 : sm + S1_VT1;
+        for (int p = 0; p < CH; ++p) {
+            const float x = p < nv ? to_f(a.qkv[(size_t)(t0 + p) * CC + c]) : 0.0f;
+            const float u = w.x * xm[0] + w.y * xm[1] + w.z * xm[2] + w.w * x;
+            const float val = p < nv ? silu_f(u) : 0.0f;
+            xm[0] = xm[1]; xm[1] = xm[2]; xm[2] = x;
+            const uint32_t off = blk < 2 ? km<4>(p, d, DK) : km<4>(d, p, CH);
+            *reinterpret_cast<float *>(dst + off) = blk < 2 ? val : tc::tf32_rn(val);   // q, k rounded after the norm
+        }
+    }
+    // gates of both V-heads; padded tokens get g = 0, beta = 0
+    if (tid < 2 * CH) {
+        const int h = tid >> 6, p = tid & 63, vh = kh + HK * h;
+        float gg = 0.0f, bb = 0.0f;
+        if (p < nv) {
+            const float al = to_f(a.alpha[(size_t)(t0 + p) * HV + vh]);
+            const float be = to_f(a.beta[(size_t)(t0 + p) * HV + vh]);
+            gg = -expf(a.A_log[vh]) * softplus_f(al + a.dt_bias[vh]);
+            bb = 1.0f / (1.0f + expf(-be));
+        }
+        ss.G[h][p] = gg;
+        ss.B[h][p] = bb;
+    }
+    __syncthreads();
+
+    // ---- C. L2 norm of the 64 q rows and 64 k rows (one warp per row, 16 rows per warp)
+    for (int rr = 0; rr < 16; ++rr) {
+        const int r = warp * 16 + rr;
+        float *tile = r < CH ? Qs : Ks;
+        const int t = r & 63;
+        float4 *p4 = reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(tile) + km<4>(t, lane * 4, DK));
+        float4 v = *p4;
+        const float s2 = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+        const float inv = rsqrtf(s2 + a.l2_eps);
+        v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
+        *p4 = tc::tf32_rn(v);
+    }
+    if (lane == 0 && warp < 2) {                      // warp 0: head 0, warp 1: head 1
+        float run = 0.0f;
+        for (int p = 0; p < CH; ++p) {
+            run += ss.G[warp][p];
+            ss.G[warp][p] = run;
+        }
+    }
+    __syncthreads();
+    if (tid < 2 * CH) ss.gam[tid >> 6][tid & 63] = expf(ss.G[tid >> 6][tid & 63]);
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+
+    const uint32_t tm = ss.tmem;
+    // ---- D. K K^T and Q K^T (tf32, M=64, N=64, K=128)
+    if (tid == 0) {
+        tc::fence_after_sync();
+        const uint32_t id = tc::instr_desc(tc::FMT_TF32, CH, CH);
+        tc::mma_tile<true>(tm + T1_KK, sbase + S1_KS, DK, sbase + S1_KS, DK, DK, id, false);
+        tc::mma_tile<true>(tm + T1_QK, sbase + S1_QS, DK, sbase + S1_KS, DK, DK, id, false);
+        tc::mma_commit(smem_u32(&ss.bar));
+    }
+    if (!mbar_wait_bounded(smem_u32(&ss.bar), 0)) ss.abort = 1;
+    tc::fence_after_sync();
+
+    unsigned char *blob[2];
+    blob[0] = a.blobs + ((size_t)g * HV + kh) * BLOB_BYTES;
+    blob[1] = a.blobs + ((size_t)g * HV + kh + HK) * BLOB_BYTES;
+
+    // ---- E. P = Mask o QK^T and beta * L from the M=64 accumulators (row t in
+    //      TMEM lane 32*(t/16) + t%16), then Q~, K~^T and gamma_n.
+    {
+        const int q = warp & 3, hf = warp >> 2;
+        float kk[32], qk[32];
+        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_KK + 32 * hf), *reinterpret_cast<float(*)[16]>(kk));
+        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_KK + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(kk + 16));
+        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_QK + 32 * hf), *reinterpret_cast<float(*)[16]>(qk));
+        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_QK + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(qk + 16));
+        tc::wait_ld();
+        if (lane < 16 && !ss.abort) {
+            const int t = 16 * q + lane;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float Gt = ss.G[h][t], bt = ss.B[h][t];
+                float *Lb = reinterpret_cast<float *>(sm + (h ? S1_LB1 : S1_LB0));
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    float pv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int cc = c4 * 4 + e, s = 32 * hf + cc;
+                        const float dec = s <= t ? expf(Gt - ss.G[h][s]) : 0.0f;
+                        Lb[t * CH + s] = s < t ? bt * dec * kk[cc] : 0.0f;
+                        pv[e] = dec * qk[cc];
+                    }
+                    *reinterpret_cast<float4 *>(blob[h] + BLOB_P + km<4>(t, 32 * hf + c4 * 4, CH)) =
+                        tc::tf32_rn(make_float4(pv[0], pv[1], pv[2], pv[3]));
+                }
+            }
+        }
+    }
+    // Q~ = diag(gamma) q^ -> bf16 K-major (Kd 128), 8 elements per store
+    for (int u = tid; u < 2 * CH * 16; u += P1_THREADS) {
+        const int h = u >> 10, t = (u >> 4) & 63, i8 = u & 15;
+        const float gm = ss.gam[h][t];
+        const float4 x0 = *reinterpret_cast<const float4 *>(sm + S1_QS + km<4>(t, i8 * 8, DK));
+        const float4 x1 = *reinterpret_cast<const float4 *>(sm + S1_QS + km<4>(t, i8 * 8 + 4, DK));
+        __align__(16) bf16 o[8] = {from_f<bf16>(x0.x * gm), from_f<bf16>(x0.y * gm), from_f<bf16>(x0.z * gm),
+                                   from_f<bf16>(x0.w * gm), from_f<bf16>(x1.x * gm), from_f<bf16>(x1.y * gm),
+                                   from_f<bf16>(x1.z * gm), from_f<bf16>(x1.w * gm)};
+        *reinterpret_cast<uint4 *>(blob[h] + BLOB_Q + km<2>(t, i8 * 8, DK)) = *reinterpret_cast<const uint4 *>(o);
+    }
+    // K~^T [i][t] = exp(G_n - G_t) k^[t][i] -> tf32 K-major (Kd 64), 4 tokens per store
+    for (int u = tid; u < 2 * DK * 16; u += P1_THREADS) {
+        const int h = u >> 11, i = (u >> 4) & 127, t4 = u & 15;
+        const float Gn = ss.G[h][CH - 1];
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int t = t4 * 4 + e;
+            v[e] = expf(Gn - ss.G[h][t]) * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(t, i, DK));
+        }
+        *reinterpret_cast<float4 *>(blob[h] + BLOB_KT + km<4>(i, t4 * 4, CH)) =
+            tc::tf32_rn(make_float4(v[0], v[1], v[2], v[3]));
+    }
+    if (tid < 2) *reinterpret_cast<float *>(blob[tid] + BLOB_G) = ss.gam[tid][CH - 1];
+    tc::fence_before_sync();
+    __syncthreads();
+
+    // ---- F. T by forward substitution (threads 0..127: one column of one head)
+    //      while threads 128..255 build (Gamma K)^T of both heads.
+    if (tid < 2 * CH) {
+        const int h = tid >> 6, c = tid & 63;
+        const float *Lb = reinterpret_cast<const float *>(sm + (h ? S1_LB1 : S1_LB0));
+        float x[CH];
+#pragma unroll
+        for (int t = 0; t < CH; ++t) {
+            float acc = (t == c) ? ss.B[h][t] : 0.0f;
+#pragma unroll
+            for (int s = 0; s < t; ++s) acc = fmaf(-Lb[t * CH + s], x[s], acc);
+            x[t] = acc;
+        }
+        unsigned char *Ts = sm + (h ? S1_TS1 : S1_TS0);
+#pragma unroll
+        for (int t = 0; t < CH; ++t) *reinterpret_cast<float *>(Ts + km<4>(t, c, CH)) = tc::tf32_rn(x[t]);
+    } else {
+        for (int u = tid - 2 * CH; u < 2 * DK * 16; u += P1_THREADS - 2 * CH) {
+            const int h = u >> 11, i = (u >> 4) & 127, s4 = u & 15;
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s = s4 * 4 + e;
+                v[e] = ss.gam[h][s] * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(s, i, DK));
+            }
+            *reinterpret_cast<float4 *>(sm + (h ? S1_GK1 : S1_QS) + km<4>(i, s4 * 4, CH)) =
+                tc::tf32_rn(make_float4(v[0], v[1], v[2], v[3]));
+        }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+
+    // ---- G. U^T = V^T T^T and W^T = (Gamma K)^T T^T per head (tf32, M=128, N=64, K=64)
+    if (tid == 0 && !ss.abort) {
+        tc::fence_after_sync();
+        const uint32_t id = tc::instr_desc(tc::FMT_TF32, 128, CH);
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t ts = sbase + (h ? S1_TS1 : S1_TS0);
+            tc::mma_tile<true>(tm + T1_U + 64 * h, sbase + (h ? S1_VT1 : S1_VT0), CH, ts, CH, CH, id, false);
+            tc::mma_tile<true>(tm + T1_W + 64 * h, sbase + (h ? S1_GK1 : S1_QS), CH, ts, CH, CH, id, false);
+        }
+        tc::mma_commit(smem_u32(&ss.bar));
+    }
+    if (!ss.abort && !mbar_wait_bounded(smem_u32(&ss.bar), 1)) ss.abort = 1;
+    tc::fence_after_sync();
+
+    // ---- H. U -> blob as [t][j] fp32; W -> blob as bf16 K-major [t][i]
+    {
+        const int q = warp & 3, hf = warp >> 2;
+        const int j = 32 * q + lane;
+        for (int h = 0; h < 2; ++h) {
+            float u[32], wv[32];
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_U + 64 * h + 32 * hf), *reinterpret_cast<float(*)[16]>(u));
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_U + 64 * h + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(u + 16));
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_W + 64 * h + 32 * hf), *reinterpret_cast<float(*)[16]>(wv));
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_W + 64 * h + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(wv + 16));
+            tc::wait_ld();
+            if (!ss.abort) {
+                float *U = reinterpret_cast<float *>(blob[h] + BLOB_U);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int t = 32 * hf + e;
+                    U[t * DV + j] = u[e];
+                    *reinterpret_cast<bf16 *>(blob[h] + BLOB_W + km<2>(t, j, DK)) = from_f<bf16>(wv[e]);
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, T1_COLS);
+    if (tid == 0 && ss.abort) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------- carry
+constexpr int P2_THREADS = 256;
+constexpr uint32_t S2_SS = 0;          // S^T bf16 [j][i] Kd128 (A of W S0, Q S0)      32 KiB
+constexpr uint32_t S2_WQ = 32768;      // W | Q~ (bf16 [t][i] Kd128, 16 KiB each)
+constexpr uint32_t S2_PK = 65536;      // P (tf32 [t][s] Kd64) | K~^T (tf32 [i][t] Kd64)
+constexpr uint32_t S2_VN = 114688;     // Vnew^T tf32 [j][t] Kd64 (A of P Vnew, K^T Vnew) 32 KiB
+constexpr uint32_t S2_Y = 147456;      // y [t][j] fp32                                  32 KiB
+constexpr uint32_t S2_SMALL = 180224;
+struct P2Small {
+    uint64_t bar_wq, bar_pk, bar_m1, bar_m2;
+    uint32_t tmem;
+    int abort;
+};
+constexpr size_t P2_SMEM = S2_SMALL + sizeof(P2Small) + 128;
+constexpr uint32_t T2_WS = 0, T2_Y = 64, T2_S = 128, T2_COLS = 256;
+
+template <typename TO>
+__global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkArgs a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+    P2Small &ss = *reinterpret_cast<P2Small *>(sm + S2_SMALL);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = blockIdx.x, vh = blockIdx.y;
+    const int q = warp & 3, hf = warp >> 2;
+    const int j = 32 * q + lane;                       // TMEM lane = value index j
+    const size_t sbase_g = ((size_t)n * HV + vh) * (DV * DK);
+    const int g0 = __ldg(a.chunk_off + n);
+    const int nc = max(0, __ldg(a.chunk_off + n + 1) - g0);
+    const int seq0 = cu_clamp(a.cu, n, 0, a.T_total);
+    const int seqL = cu_clamp(a.cu, n + 1, seq0, a.T_total) - seq0;
+
+    if (nc == 0) {                                     // empty sequence: the state passes through
+        if (a.S_out)
+            for (int e = tid; e < DV * DK / 4; e += P2_THREADS) {
+                const float4 v = a.S_in ? reinterpret_cast<const float4 *>(a.S_in + sbase_g)[e]
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(a.S_out + sbase_g)[e] = v;
+            }
+        return;
+    }
+    const uint32_t sb = smem_u32(sm);
+    auto blob_of = [&](int c) { return a.blobs + ((size_t)(g0 + c) * HV + vh) * BLOB_BYTES; };
+
+    if (warp == 0) {
+        tc::tmem_alloc(smem_u32(&ss.tmem), T2_COLS);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(&ss.bar_wq), 1);
+        mbar_init(smem_u32(&ss.bar_pk), 1);
+        mbar_init(smem_u32(&ss.bar_m1), 1);
+        mbar_init(smem_u32(&ss.bar_m2), 1);
+        ss.abort = 0;
+        fence_mbar_init();
+        const unsigned char *b0 = blob_of(0);
+        mbar_arrive_expect_tx(smem_u32(&ss.bar_wq), 32768);
+        bulk_g2s(sb + S2_WQ, b0 + BLOB_W, 32768, smem_u32(&ss.bar_wq));
+        mbar_arrive_expect_tx(smem_u32(&ss.bar_pk), 49152);
+        bulk_g2s(sb + S2_PK, b0 + BLOB_P, 49152, smem_u32(&ss.bar_pk));
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    const uint32_t tm = ss.tmem;
+    tc::fence_after_sync();
+
+    // initial state: bf16 copy into shared memory, gamma_n(chunk 0) * S0 into TMEM
+    {
+        const float gam0 = *reinterpret_cast<const float *>(blob_of(0) + BLOB_G);
+        for (int cb = 0; cb < 4; ++cb) {
+            const int i0 = 64 * hf + 16 * cb;
+            float v[16];
+            if (a.S_in) {
+                const float4 *src = reinterpret_cast<const float4 *>(a.S_in + sbase_g + (size_t)j * DK + i0);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 x = src[e];
+                    v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = 0.0f;
+            }
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+                __align__(16) bf16 o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = from_f<bf16>(v[8 * h8 + e]);
+                *reinterpret_cast<uint4 *>(sm + S2_SS + km<2>(j, i0 + 8 * h8, DK)) = *reinterpret_cast<const uint4 *>(o);
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] *= gam0;
+            tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + i0), v);
+        }
+        tc::wait_st();
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+
+    const float scale = rsqrtf((float)DK);
+    const float *Yb = reinterpret_cast<const float *>(sm + S2_Y);
+    for (int c = 0; c < nc; ++c) {
+        const unsigned char *blob = blob_of(c);
+        const uint32_t par = (uint32_t)(c & 1);
+        const int nvc = max(0, min(CH, seqL - CH * c));
+        // (1) W S0 and Q S0 (bf16, M=128, N=64, K=128) into TMEM
+        if (tid == 0) {
+            tc::fence_after_sync();
+            if (!mbar_wait_bounded(smem_u32(&ss.bar_wq), par)) ss.abort = 1;
+            const uint32_t id = tc::instr_desc(tc::FMT_BF16, 128, CH);
+            tc::mma_tile<false>(tm + T2_WS, sb + S2_SS, DK, sb + S2_WQ, DK, DK, id, false);
+            tc::mma_tile<false>(tm + T2_Y, sb + S2_SS, DK, sb + S2_WQ + 16384, DK, DK, id, false);
+            tc::mma_commit(smem_u32(&ss.bar_m1));
+        }
+        // U column j, tokens [32hf, 32hf+32), while the tensor core works
+        float u[32];
+        {
+            const float *U = reinterpret_cast<const float *>(blob + BLOB_U);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = U[(32 * hf + e) * DV + j];
+        }
+        const float gam_next = (c + 1 < nc) ? *reinterpret_cast<const float *>(blob_of(c + 1) + BLOB_G) : 0.0f;
+        if (!mbar_wait_bounded(smem_u32(&ss.bar_m1), par)) ss.abort = 1;
+        tc::fence_after_sync();
+        // (2) Vnew^T = U^T - (W S0)^T -> tf32 tile
+        {
+            float d[32];
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_WS + 32 * hf), *reinterpret_cast<float(*)[16]>(d));
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_WS + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(d + 16));
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4 *>(sm + S2_VN + km<4>(j, 32 * hf + e, CH)) =
+                    tc::tf32_rn(make_float4(u[e] - d[e], u[e + 1] - d[e + 1], u[e + 2] - d[e + 2], u[e + 3] - d[e + 3]));
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (ss.abort) break;
+        // (3) Y += Vnew^T P^T and S += Vnew^T K~ (tf32)
+        if (tid == 0) {
+            tc::fence_after_sync();
+            if (c + 1 < nc) {                          // W | Q~ of the next chunk (slot free: MMA (1) is done)
+                mbar_arrive_expect_tx(smem_u32(&ss.bar_wq), 32768);
+                bulk_g2s(sb + S2_WQ, blob_of(c + 1) + BLOB_W, 32768, smem_u32(&ss.bar_wq));
+            }
+            if (!mbar_wait_bounded(smem_u32(&ss.bar_pk), par)) ss.abort = 1;
+            tc::mma_tile<true>(tm + T2_Y, sb + S2_VN, CH, sb + S2_PK, CH, CH, tc::instr_desc(tc::FMT_TF32, 128, CH),
+                               true);
+            tc::mma_tile<true>(tm + T2_S, sb + S2_VN, CH, sb + S2_PK + 16384, CH, CH,
+                               tc::instr_desc(tc::FMT_TF32, 128, 128), true);
+            tc::mma_commit(smem_u32(&ss.bar_m2));
+        }
+        if (!mbar_wait_bounded(smem_u32(&ss.bar_m2), par)) ss.abort = 1;
+        tc::fence_after_sync();
+        if (tid == 0 && c + 1 < nc) {                  // P | K~^T of the next chunk
+            mbar_arrive_expect_tx(smem_u32(&ss.bar_pk), 49152);
+            bulk_g2s(sb + S2_PK, blob_of(c + 1) + BLOB_P, 49152, smem_u32(&ss.bar_pk));
+        }
+        // (4) state: bf16 copy for the next chunk and decay by its gamma_n, or the final state out
+        for (int cb = 0; cb < 4; ++cb) {
+            const int i0 = 64 * hf + 16 * cb;
+            float v[16];
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_S + i0), v);
+            tc::wait_ld();
+            if (c + 1 < nc) {
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    __align__(16) bf16 o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = from_f<bf16>(v[8 * h8 + e]);
+                    *reinterpret_cast<uint4 *>(sm + S2_SS + km<2>(j, i0 + 8 * h8, DK)) =
+                        *reinterpret_cast<const uint4 *>(o);
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] *= gam_next;
+                tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + i0), v);
+            } else if (a.S_out) {
+                float4 *dst = reinterpret_cast<float4 *>(a.S_out + sbase_g + (size_t)j * DK + i0);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            }
+        }
+        // y of this chunk -> [t][j] buffer
+        {
+            float y[32];
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_Y + 32 * hf), *reinterpret_cast<float(*)[16]>(y));
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_Y + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(y + 16));
+            tc::wait_ld();
+            float *Yw = reinterpret_cast<float *>(sm + S2_Y);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) Yw[(32 * hf + e) * DV + j] = y[e] * scale;
+        }
+        tc::wait_st();
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (ss.abort) break;
+        // (5) gated RMSNorm . silu(z) of the chunk's tokens (warp w: tokens 8w..8w+7)
+        {
+            const float4 wn = *reinterpret_cast<const float4 *>(a.norm_w + 4 * lane);
+            for (int r = 0; r < 8; ++r) {
+                const int t = 8 * warp + r;
+                if (t >= nvc) break;
+                const float4 y4 = *reinterpret_cast<const float4 *>(Yb + t * DV + 4 * lane);
+                const float ms = warp_sum(y4.x * y4.x + y4.y * y4.y + y4.z * y4.z + y4.w * y4.w) * (1.0f / DV);
+                const float rr = rsqrtf(ms + a.norm_eps);
+                const size_t o = (size_t)(seq0 + CH * c + t) * DI + (size_t)vh * DV + 4 * lane;
+                const uint2 zr = *reinterpret_cast<const uint2 *>(a.z + o);
+                const bf16 *zz = reinterpret_cast<const bf16 *>(&zr);
+                TO *out = static_cast<TO *>(a.out) + o;
+                out[0] = from_f<TO>(y4.x * rr * wn.x * silu_f(to_f(zz[0])));
+                out[1] = from_f<TO>(y4.y * rr * wn.y * silu_f(to_f(zz[1])));
+                out[2] = from_f<TO>(y4.z * rr * wn.z * silu_f(to_f(zz[2])));
+                out[3] = from_f<TO>(y4.w * rr * wn.w * silu_f(to_f(zz[3])));
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, T2_COLS);
+    if (tid == 0 && ss.abort) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- launcher
+
+cudaError_t launch_conv_state_out_bf16(const int32_t *cu, int N, int T_total, const void *qkv, const void *cs_in,
+                                       void *cs_out, cudaStream_t s);
+
+static size_t off_blobs(int N) { return ((size_t)(N + 1) * sizeof(int32_t) + 255) & ~(size_t)255; }
+
+size_t chunk_workspace_bytes(int N, int T_total)
+{
+    const size_t max_chunks = (size_t)T_total / CH + (size_t)N;
+    return off_blobs(N) + max_chunks * HV * BLOB_BYTES;
+}
+
+cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
+                                   const void *beta, const int32_t *cu, int N, int T_total, const void *cs_in,
+                                   void *cs_out, const float *S_in, float *S_out, void *out, gdn_dtype out_dt,
+                                   void *ws_body, cudaStream_t s)
+{
+    ChunkArgs a;
+    a.conv_w = p->conv_w; a.A_log = p->A_log; a.dt_bias = p->dt_bias; a.norm_w = p->norm_w;
+    a.norm_eps = p->norm_eps; a.l2_eps = p->l2_eps;
+    a.qkv = (const bf16 *)qkv; a.z = (const bf16 *)z; a.alpha = (const bf16 *)alpha; a.beta = (const bf16 *)beta;
+    a.cu = cu; a.N = N; a.T_total = T_total;
+    a.max_chunks = T_total / CH + N;
+    a.cs_in = (const bf16 *)cs_in; a.S_in = S_in; a.S_out = S_out; a.out = out;
+    a.chunk_off = static_cast<int32_t *>(ws_body);
+    a.blobs = static_cast<unsigned char *>(ws_body) + off_blobs(N);
+
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P1_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_carry_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P2_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_carry_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P2_SMEM);
+    if (e != cudaSuccess) return e;
+
+    chunk_schedule_kernel<<<1, 1024, 0, s>>>(cu, N, T_total, a.max_chunks, a.chunk_off);
+    if (a.max_chunks > 0) chunk_prep_kernel<<<dim3(a.max_chunks, HK), P1_THREADS, P1_SMEM, s>>>(a);
+    if (out_dt == GDN_F32) chunk_carry_kernel<float><<<dim3(N, HV), P2_THREADS, P2_SMEM, s>>>(a);
+    else chunk_carry_kernel<bf16><<<dim3(N, HV), P2_THREADS, P2_SMEM, s>>>(a);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && cs_out) e = launch_conv_state_out_bf16(cu, N, T_total, qkv, cs_in, cs_out, s);
+    return e;
+}
+
+cudaError_t take_chunk_error(unsigned int *word, cudaStream_t s)
+{
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_chunk_error, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && *word != 0)
+        e = cudaMemcpyToSymbolAsync(g_chunk_error, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e;
+}
+
+}  // namespace gdn

@@ -69,9 +69,12 @@ constexpr uint32_t STATE_BYTES = DV * DK * sizeof(float); // 64 KiB
 constexpr int DEC_COPIES = 4;                              // bulk copies per state
 
 struct DecodeSmem {
-    float slot[DEC_SLOTS][DV * DK];
-    uint64_t full[DEC_SLOTS];
-    float q[DK], k[DK], v[2][DV], y[2][DV];
+    alignas(128) float slot[DEC_SLOTS][DV * DK];   // TMA destinations
+    alignas(16) float q[DK];                        // read as float4
+    alignas(16) float k[DK];
+    alignas(16) float v[2][DV];
+    alignas(16) float y[2][DV];
+    alignas(8) uint64_t full[DEC_SLOTS];
     float red[32];
     float gate[2][2];
     int pending[DEC_SLOTS];   // state number whose load is outstanding in each slot, or -1

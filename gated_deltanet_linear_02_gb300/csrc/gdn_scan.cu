@@ -289,3 +289,16 @@ cudaError_t launch_prefill_scan(const gdn_params *p, const void *qkv, const void
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// conv_state_out for the chunked path (bf16 activations); same rule as above.
+cudaError_t launch_conv_state_out_bf16(const int32_t *cu, int N, int T_total, const void *qkv, const void *cs_in,
+                                       void *cs_out, cudaStream_t s)
+{
+    conv_state_out_kernel<bf16><<<dim3(CC / 256, N), 256, 0, s>>>(cu, T_total, (const bf16 *)qkv,
+                                                                  (const bf16 *)cs_in, (bf16 *)cs_out);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,171 @@
+// gdn_tc.cuh -- 5th-generation tensor core (tcgen05) primitives as inline PTX
+// for sm_103a: tensor-memory allocation, shared-memory matrix descriptors, the
+// instruction descriptor, MMA issue and commit, TMEM loads and stores, and the
+// fences that order them against ordinary thread synchronisation.
+//
+// Operand layout used throughout libgdn: K-major, no swizzle. A tile of R rows
+// (the M or N extent) by Kd elements along K is stored as 8-row x 16-byte
+// "core matrices" (8 rows of 16 contiguous bytes, 128 bytes in all).
+// Consecutive core matrices along K are 128 bytes apart (the leading-dimension
+// byte offset, LBO). Consecutive 8-row groups are Kd * elem_size * 8 bytes
+// apart (the stride-dimension byte offset, SBO). Element (r, k) lives at
+//   (r / 8) * SBO + (k / kc) * 128 + (r % 8) * 16 + (k % kc) * elem_size,
+// with kc = 16 / elem_size (8 for bf16, 4 for tf32).
+#pragma once
+
+#include <stdint.h>
+
+#include "gdn_async.cuh"
+
+namespace gdn {
+namespace tc {
+
+// byte offset of element (r, k) in a K-major no-swizzle tile with Kd columns
+template <int ES>
+__host__ __device__ __forceinline__ uint32_t kmajor_offset(int r, int k, int Kd)
+{
+    constexpr int kc = 16 / ES;
+    return (uint32_t)((r >> 3) * (Kd * ES * 8) + (k / kc) * 128 + (r & 7) * 16 + (k % kc) * ES);
+}
+
+// Shared-memory matrix descriptor (sm_100 family): start address, LBO and SBO
+// in 16-byte units, version 1 at bits 46-47, no swizzle (layout type 0).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Descriptor of the K-slice starting at element k0 of a K-major tile with Kd
+// columns and element size ES, based at shared address `base`.
+template <int ES>
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int k0, int Kd)
+{
+    return smem_desc(base + (uint32_t)((k0 / (16 / ES)) * 128), 128u, (uint32_t)(Kd * ES * 8));
+}
+
+enum : uint32_t { FMT_F16 = 0, FMT_BF16 = 1, FMT_TF32 = 2 };
+
+// An fp32 value rounded to the nearest tf32 (10-bit mantissa). The tensor core
+// only reads the top 19 bits of a tf32 operand, which truncates it toward zero.
+// Over long sums that truncation bias grows about 3x larger than the
+// round-to-nearest error, so every tf32 operand is rounded when stored.
+__device__ __forceinline__ float tf32_rn(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ float4 tf32_rn(float4 v)
+{
+    return make_float4(tf32_rn(v.x), tf32_rn(v.y), tf32_rn(v.z), tf32_rn(v.w));
+}
+
+// Instruction descriptor: fp32 accumulator, A/B formats, both K-major, N and M.
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_fmt, int M, int N)
+{
+    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---- tensor memory
+// Allocates `ncols` columns (power of two >= 32); the base address is written
+// to *smem_dst. Must be executed by one whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t smem_dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_dst), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// ---- MMA: D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Arrives once on `bar` when every MMA issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// D (+)= A * B^T over the K extent `kd`, A and B K-major tiles with `kd`
+// columns, in steps of the instruction K (16 for bf16, 8 for tf32).
+template <bool TF32>
+__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_base, int a_kd, uint32_t b_base, int b_kd,
+                                         int kd, uint32_t idesc, bool accumulate)
+{
+    constexpr int ES = TF32 ? 4 : 2;
+    constexpr int KI = TF32 ? 8 : 16;
+    for (int k0 = 0; k0 < kd; k0 += KI) {
+        const uint64_t a = kmajor_desc<ES>(a_base, k0, a_kd);
+        const uint64_t b = kmajor_desc<ES>(b_base, k0, b_kd);
+        if (TF32) mma_tf32(d_tmem, a, b, idesc, (accumulate || k0 > 0) ? 1u : 0u);
+        else mma_f16(d_tmem, a, b, idesc, (accumulate || k0 > 0) ? 1u : 0u);
+    }
+}
+
+// ---- fences around thread synchronisation
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---- TMEM <-> registers: 32 lanes (this warp's quarter) x 16 consecutive
+// 32-bit columns; thread t gets lane (32 * (warp % 4) + t). `taddr` carries
+// the lane base in bits 31..16 and the column in bits 15..0.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                   "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                   "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+                   "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+                   "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+                   "r"(__float_as_uint(v[15]))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane, int col)
+{
+    return base + ((uint32_t)lane << 16) + (uint32_t)col;
+}
+
+}  // namespace tc
+}  // namespace gdn
