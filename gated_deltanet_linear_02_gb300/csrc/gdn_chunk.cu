@@ -186,13 +186,20 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
             xm[m] = v;
         }
         unsigned char *dst = blk == 0 ? sm + S1_QS : blk == 1 ? sm + S1_KS : blk == 2 ? sm + S1_VT0 : sm + S1_VT1;
-        for (int p = 0; p < CH; ++p) {
-            const float x = p < nv ? to_f(a.qkv[(size_t)(t0 + p) * CC + c]) : 0.0f;
-            const float u = w.x * xm[0] + w.y * xm[1] + w.z * xm[2] + w.w * x;
-            const float val = p < nv ? silu_f(u) : 0.0f;
-            xm[0] = xm[1]; xm[1] = xm[2]; xm[2] = x;
-            const uint32_t off = blk < 2 ? km<4>(p, d, DK) : km<4>(d, p, CH);
-            *reinterpret_cast<float *>(dst + off) = blk < 2 ? val : tc::tf32_rn(val);   // q, k rounded after the norm
+        for (int pb = 0; pb < CH; pb += 32) {          // 32 independent loads in flight per thread
+            float xs[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                xs[e] = (pb + e) < nv ? to_f(a.qkv[(size_t)(t0 + pb + e) * CC + c]) : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int p = pb + e;
+                const float u = w.x * xm[0] + w.y * xm[1] + w.z * xm[2] + w.w * xs[e];
+                const float val = p < nv ? silu_f(u) : 0.0f;
+                xm[0] = xm[1]; xm[1] = xm[2]; xm[2] = xs[e];
+                const uint32_t off = blk < 2 ? km<4>(p, d, DK) : km<4>(d, p, CH);
+                *reinterpret_cast<float *>(dst + off) = blk < 2 ? val : tc::tf32_rn(val);   // q, k rounded after the norm
+            }
         }
     }
     // gates of both V-heads; padded tokens get g = 0, beta = 0
@@ -319,10 +326,10 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
         float x[CH];
 #pragma unroll
         for (int t = 0; t < CH; ++t) {
-            float acc = (t == c) ? ss.B[h][t] : 0.0f;
+            float acc[4] = {(t == c) ? ss.B[h][t] : 0.0f, 0.0f, 0.0f, 0.0f};   // 4 chains for ILP
 #pragma unroll
-            for (int s = 0; s < t; ++s) acc = fmaf(-Lb[t * CH + s], x[s], acc);
-            x[t] = acc;
+            for (int s = 0; s < t; ++s) acc[s & 3] = fmaf(-Lb[t * CH + s], x[s], acc[s & 3]);
+            x[t] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
         unsigned char *Ts = sm + (h ? S1_TS1 : S1_TS0);
 #pragma unroll
@@ -388,19 +395,34 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
 
 // ------------------------------------------------------------------- carry
 constexpr int P2_THREADS = 256;
-constexpr uint32_t S2_SS = 0;          // S^T bf16 [j][i] Kd128 (A of W S0, Q S0)      32 KiB
-constexpr uint32_t S2_WQ = 32768;      // W | Q~ (bf16 [t][i] Kd128, 16 KiB each)
-constexpr uint32_t S2_PK = 65536;      // P (tf32 [t][s] Kd64) | K~^T (tf32 [i][t] Kd64)
-constexpr uint32_t S2_VN = 114688;     // Vnew^T tf32 [j][t] Kd64 (A of P Vnew, K^T Vnew) 32 KiB
-constexpr uint32_t S2_Y = 147456;      // y [t][j] fp32                                  32 KiB
-constexpr uint32_t S2_SMALL = 180224;
+constexpr uint32_t S2_SS = 0;          // S^T bf16 [j][i] Kd128 (A of W S0, Q S0)         32 KiB
+constexpr uint32_t S2_WQ0 = 32768;     // W | Q~ (bf16 [t][i] Kd128, 16 KiB each), stage 0
+constexpr uint32_t S2_WQ1 = 65536;     //                                          stage 1
+constexpr uint32_t S2_PK0 = 98304;     // P (tf32 [t][s] Kd64) | K~^T (tf32 [i][t] Kd64), stage 0
+constexpr uint32_t S2_PK1 = 147456;    //                                                  stage 1
+constexpr uint32_t S2_VN = 196608;     // Vnew^T tf32 [j][t] Kd64; after the second MMA, y [t][j] fp32
+constexpr uint32_t S2_SMALL = 229376;
 struct P2Small {
-    uint64_t bar_wq, bar_pk, bar_m1, bar_m2;
+    uint64_t bar_wq[2], bar_pk[2], bar_m1, bar_m2;
     uint32_t tmem;
     int abort;
 };
 constexpr size_t P2_SMEM = S2_SMALL + sizeof(P2Small) + 128;
 constexpr uint32_t T2_WS = 0, T2_Y = 64, T2_S = 128, T2_COLS = 256;
+
+// Caller: thread 0. Loads chunk c's W | Q~ and P | K~^T into stage c % 2.
+template <bool WQ>
+__device__ __forceinline__ void carry_issue(const unsigned char *blob, uint32_t sb, P2Small &ss, int c)
+{
+    const int st = c & 1;
+    if (WQ) {
+        mbar_arrive_expect_tx(smem_u32(&ss.bar_wq[st]), 32768);
+        bulk_g2s(sb + (st ? S2_WQ1 : S2_WQ0), blob + BLOB_W, 32768, smem_u32(&ss.bar_wq[st]));
+    } else {
+        mbar_arrive_expect_tx(smem_u32(&ss.bar_pk[st]), 49152);
+        bulk_g2s(sb + (st ? S2_PK1 : S2_PK0), blob + BLOB_P, 49152, smem_u32(&ss.bar_pk[st]));
+    }
+}
 
 template <typename TO>
 __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkArgs a)
@@ -429,24 +451,34 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
     }
     const uint32_t sb = smem_u32(sm);
     auto blob_of = [&](int c) { return a.blobs + ((size_t)(g0 + c) * HV + vh) * BLOB_BYTES; };
+    auto gamma_of = [&](int c) { return c < nc ? *reinterpret_cast<const float *>(blob_of(c) + BLOB_G) : 0.0f; };
 
     if (warp == 0) {
         tc::tmem_alloc(smem_u32(&ss.tmem), T2_COLS);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(smem_u32(&ss.bar_wq), 1);
-        mbar_init(smem_u32(&ss.bar_pk), 1);
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(smem_u32(&ss.bar_wq[st]), 1);
+            mbar_init(smem_u32(&ss.bar_pk[st]), 1);
+        }
         mbar_init(smem_u32(&ss.bar_m1), 1);
         mbar_init(smem_u32(&ss.bar_m2), 1);
         ss.abort = 0;
         fence_mbar_init();
-        const unsigned char *b0 = blob_of(0);
-        mbar_arrive_expect_tx(smem_u32(&ss.bar_wq), 32768);
-        bulk_g2s(sb + S2_WQ, b0 + BLOB_W, 32768, smem_u32(&ss.bar_wq));
-        mbar_arrive_expect_tx(smem_u32(&ss.bar_pk), 49152);
-        bulk_g2s(sb + S2_PK, b0 + BLOB_P, 49152, smem_u32(&ss.bar_pk));
+        for (int c = 0; c < 2 && c < nc; ++c) {        // both stages in flight from the start
+            carry_issue<true>(blob_of(c), sb, ss, c);
+            carry_issue<false>(blob_of(c), sb, ss, c);
+        }
     }
+    // operands of chunk 0 that go through registers: U column j, gamma_n
+    float u_cur[32], u_nxt[32];
+    {
+        const float *U = reinterpret_cast<const float *>(blob_of(0) + BLOB_U);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) u_cur[e] = U[(32 * hf + e) * DV + j];
+    }
+    float gam_c1 = gamma_of(1);                        // gamma_n of the next chunk
     tc::fence_before_sync();
     __syncthreads();
     const uint32_t tm = ss.tmem;
@@ -454,7 +486,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
 
     // initial state: bf16 copy into shared memory, gamma_n(chunk 0) * S0 into TMEM
     {
-        const float gam0 = *reinterpret_cast<const float *>(blob_of(0) + BLOB_G);
+        const float gam0 = gamma_of(0);
         for (int cb = 0; cb < 4; ++cb) {
             const int i0 = 64 * hf + 16 * cb;
             float v[16];
@@ -487,28 +519,38 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
     __syncthreads();
 
     const float scale = rsqrtf((float)DK);
-    const float *Yb = reinterpret_cast<const float *>(sm + S2_Y);
+    const float4 wn = *reinterpret_cast<const float4 *>(a.norm_w + 4 * lane);
     for (int c = 0; c < nc; ++c) {
-        const unsigned char *blob = blob_of(c);
-        const uint32_t par = (uint32_t)(c & 1);
+        const int st = c & 1;
+        const uint32_t spar = (uint32_t)((c >> 1) & 1);   // phase of this stage's barriers
+        const uint32_t par = (uint32_t)(c & 1);           // phase of the per-chunk MMA barriers
         const int nvc = max(0, min(CH, seqL - CH * c));
         // (1) W S0 and Q S0 (bf16, M=128, N=64, K=128) into TMEM
         if (tid == 0) {
             tc::fence_after_sync();
-            if (!mbar_wait_bounded(smem_u32(&ss.bar_wq), par)) ss.abort = 1;
+            if (!mbar_wait_bounded(smem_u32(&ss.bar_wq[st]), spar)) ss.abort = 1;
+            const uint32_t wq = sb + (st ? S2_WQ1 : S2_WQ0);
             const uint32_t id = tc::instr_desc(tc::FMT_BF16, 128, CH);
-            tc::mma_tile<false>(tm + T2_WS, sb + S2_SS, DK, sb + S2_WQ, DK, DK, id, false);
-            tc::mma_tile<false>(tm + T2_Y, sb + S2_SS, DK, sb + S2_WQ + 16384, DK, DK, id, false);
+            tc::mma_tile<false>(tm + T2_WS, sb + S2_SS, DK, wq, DK, DK, id, false);
+            tc::mma_tile<false>(tm + T2_Y, sb + S2_SS, DK, wq + 16384, DK, DK, id, false);
             tc::mma_commit(smem_u32(&ss.bar_m1));
         }
-        // U column j, tokens [32hf, 32hf+32), while the tensor core works
-        float u[32];
-        {
-            const float *U = reinterpret_cast<const float *>(blob + BLOB_U);
+        // loads for later, issued now so that their latency hides behind the MMAs:
+        // this chunk's z rows (warp w: tokens 8w..8w+7), next chunk's U column, gamma two ahead
+        uint2 zr[8];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = U[(32 * hf + e) * DV + j];
+        for (int r = 0; r < 8; ++r) {
+            const int t = 8 * warp + r;
+            zr[r] = t < nvc ? *reinterpret_cast<const uint2 *>(a.z + (size_t)(seq0 + CH * c + t) * DI +
+                                                              (size_t)vh * DV + 4 * lane)
+                            : make_uint2(0u, 0u);
         }
-        const float gam_next = (c + 1 < nc) ? *reinterpret_cast<const float *>(blob_of(c + 1) + BLOB_G) : 0.0f;
+        if (c + 1 < nc) {
+            const float *U = reinterpret_cast<const float *>(blob_of(c + 1) + BLOB_U);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u_nxt[e] = U[(32 * hf + e) * DV + j];
+        }
+        const float gam_c2 = gamma_of(c + 2);
         if (!mbar_wait_bounded(smem_u32(&ss.bar_m1), par)) ss.abort = 1;
         tc::fence_after_sync();
         // (2) Vnew^T = U^T - (W S0)^T -> tf32 tile
@@ -519,8 +561,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
             tc::wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4 *>(sm + S2_VN + km<4>(j, 32 * hf + e, CH)) =
-                    tc::tf32_rn(make_float4(u[e] - d[e], u[e + 1] - d[e + 1], u[e + 2] - d[e + 2], u[e + 3] - d[e + 3]));
+                *reinterpret_cast<float4 *>(sm + S2_VN + km<4>(j, 32 * hf + e, CH)) = tc::tf32_rn(
+                    make_float4(u_cur[e] - d[e], u_cur[e + 1] - d[e + 1], u_cur[e + 2] - d[e + 2], u_cur[e + 3] - d[e + 3]));
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
@@ -529,23 +571,17 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
         // (3) Y += Vnew^T P^T and S += Vnew^T K~ (tf32)
         if (tid == 0) {
             tc::fence_after_sync();
-            if (c + 1 < nc) {                          // W | Q~ of the next chunk (slot free: MMA (1) is done)
-                mbar_arrive_expect_tx(smem_u32(&ss.bar_wq), 32768);
-                bulk_g2s(sb + S2_WQ, blob_of(c + 1) + BLOB_W, 32768, smem_u32(&ss.bar_wq));
-            }
-            if (!mbar_wait_bounded(smem_u32(&ss.bar_pk), par)) ss.abort = 1;
-            tc::mma_tile<true>(tm + T2_Y, sb + S2_VN, CH, sb + S2_PK, CH, CH, tc::instr_desc(tc::FMT_TF32, 128, CH),
+            if (c + 2 < nc) carry_issue<true>(blob_of(c + 2), sb, ss, c + 2);   // stage free: MMA (1) done
+            if (!mbar_wait_bounded(smem_u32(&ss.bar_pk[st]), spar)) ss.abort = 1;
+            const uint32_t pk = sb + (st ? S2_PK1 : S2_PK0);
+            tc::mma_tile<true>(tm + T2_Y, sb + S2_VN, CH, pk, CH, CH, tc::instr_desc(tc::FMT_TF32, 128, CH), true);
+            tc::mma_tile<true>(tm + T2_S, sb + S2_VN, CH, pk + 16384, CH, CH, tc::instr_desc(tc::FMT_TF32, 128, 128),
                                true);
-            tc::mma_tile<true>(tm + T2_S, sb + S2_VN, CH, sb + S2_PK + 16384, CH, CH,
-                               tc::instr_desc(tc::FMT_TF32, 128, 128), true);
             tc::mma_commit(smem_u32(&ss.bar_m2));
         }
         if (!mbar_wait_bounded(smem_u32(&ss.bar_m2), par)) ss.abort = 1;
         tc::fence_after_sync();
-        if (tid == 0 && c + 1 < nc) {                  // P | K~^T of the next chunk
-            mbar_arrive_expect_tx(smem_u32(&ss.bar_pk), 49152);
-            bulk_g2s(sb + S2_PK, blob_of(c + 1) + BLOB_P, 49152, smem_u32(&ss.bar_pk));
-        }
+        if (tid == 0 && c + 2 < nc) carry_issue<false>(blob_of(c + 2), sb, ss, c + 2);
         // (4) state: bf16 copy for the next chunk and decay by its gamma_n, or the final state out
         for (int cb = 0; cb < 4; ++cb) {
             const int i0 = 64 * hf + 16 * cb;
@@ -562,7 +598,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
                         *reinterpret_cast<const uint4 *>(o);
                 }
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] *= gam_next;
+                for (int e = 0; e < 16; ++e) v[e] *= gam_c1;
                 tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + i0), v);
             } else if (a.S_out) {
                 float4 *dst = reinterpret_cast<float4 *>(a.S_out + sbase_g + (size_t)j * DK + i0);
@@ -570,15 +606,15 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
                 for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
             }
         }
-        // y of this chunk -> [t][j] buffer
+        // y of this chunk -> [t][j] buffer (reuses the Vnew tile: the MMAs reading it are done)
+        float *Yb = reinterpret_cast<float *>(sm + S2_VN);
         {
             float y[32];
             tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_Y + 32 * hf), *reinterpret_cast<float(*)[16]>(y));
             tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_Y + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(y + 16));
             tc::wait_ld();
-            float *Yw = reinterpret_cast<float *>(sm + S2_Y);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) Yw[(32 * hf + e) * DV + j] = y[e] * scale;
+            for (int e = 0; e < 32; ++e) Yb[(32 * hf + e) * DV + j] = y[e] * scale;
         }
         tc::wait_st();
         fence_proxy_async_smem();
@@ -586,24 +622,25 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
         __syncthreads();
         if (ss.abort) break;
         // (5) gated RMSNorm . silu(z) of the chunk's tokens (warp w: tokens 8w..8w+7)
-        {
-            const float4 wn = *reinterpret_cast<const float4 *>(a.norm_w + 4 * lane);
-            for (int r = 0; r < 8; ++r) {
-                const int t = 8 * warp + r;
-                if (t >= nvc) break;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int t = 8 * warp + r;
+            if (t < nvc) {
                 const float4 y4 = *reinterpret_cast<const float4 *>(Yb + t * DV + 4 * lane);
                 const float ms = warp_sum(y4.x * y4.x + y4.y * y4.y + y4.z * y4.z + y4.w * y4.w) * (1.0f / DV);
                 const float rr = rsqrtf(ms + a.norm_eps);
-                const size_t o = (size_t)(seq0 + CH * c + t) * DI + (size_t)vh * DV + 4 * lane;
-                const uint2 zr = *reinterpret_cast<const uint2 *>(a.z + o);
-                const bf16 *zz = reinterpret_cast<const bf16 *>(&zr);
-                TO *out = static_cast<TO *>(a.out) + o;
+                const bf16 *zz = reinterpret_cast<const bf16 *>(&zr[r]);
+                TO *out = static_cast<TO *>(a.out) + (size_t)(seq0 + CH * c + t) * DI + (size_t)vh * DV + 4 * lane;
                 out[0] = from_f<TO>(y4.x * rr * wn.x * silu_f(to_f(zz[0])));
                 out[1] = from_f<TO>(y4.y * rr * wn.y * silu_f(to_f(zz[1])));
                 out[2] = from_f<TO>(y4.z * rr * wn.z * silu_f(to_f(zz[2])));
                 out[3] = from_f<TO>(y4.w * rr * wn.w * silu_f(to_f(zz[3])));
             }
         }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) u_cur[e] = u_nxt[e];
+        gam_c1 = gam_c2;
+        __syncthreads();                                // y buffer is the next chunk's Vnew tile
     }
     tc::fence_before_sync();
     __syncthreads();
