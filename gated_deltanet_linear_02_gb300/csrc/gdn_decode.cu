@@ -14,13 +14,16 @@
 // touched by this CTA alone. No other CTA reads them, and the state shift
 // needs no cross-CTA ordering.
 //
-// The states stream through a ring of three 64 KiB shared-memory slots. Thread
-// 0 fills them with TMA bulk copies (cp.async.bulk), which complete on one
-// mbarrier per slot, and keeps two states in flight ahead of the one being
-// computed. Warp w computes rows j in [8w, 8w+8) of S^T (value index j, whose
-// 128 keys i are contiguous). Lane l holds keys [4l, 4l+4). pred_j, delta_j and
-// y_j depend on row j alone, so a row needs only warp-shuffle dot products.
-// The updated row goes straight back to global memory with a streaming store.
+// The states stream through a ring of six 32 KiB shared-memory slots, each
+// holding 64 rows of one state. Thread 0 fills them with TMA bulk copies
+// (cp.async.bulk), which complete on one mbarrier per slot, and keeps five
+// slots in flight ahead of the one being computed. Warp w computes 4 rows j of
+// each slot (rows of S^T: value index j, 128 contiguous keys i). Lane l holds
+// keys [4l, 4l+4). pred_j, delta_j and y_j depend on row j alone, so a row
+// needs only warp-shuffle dot products. The updated row goes straight back to
+// global memory with a streaming store. An item's prologue inputs (conv_state,
+// qkv, gates, z) are loaded one item ahead, so their latency hides behind the
+// previous item's sweep.
 #include "gdn_async.cuh"
 #include "gdn_common.cuh"
 
@@ -63,13 +66,15 @@ struct DecodeArgs {
 
 constexpr int DEC_THREADS = 512;
 constexpr int DEC_WARPS = DEC_THREADS / 32;
-constexpr int DEC_ROWS_PER_WARP = DV / DEC_WARPS;         // 8
-constexpr int DEC_SLOTS = 3;
-constexpr uint32_t STATE_BYTES = DV * DK * sizeof(float); // 64 KiB
-constexpr int DEC_COPIES = 4;                              // bulk copies per state
+constexpr int DEC_SLOT_ROWS = 64;                          // rows j of S^T per staging slot
+constexpr int DEC_UNITS = DV / DEC_SLOT_ROWS;              // slots per state (2)
+constexpr int DEC_ROWS_PER_WARP = DEC_SLOT_ROWS / DEC_WARPS;   // 4
+constexpr int DEC_SLOTS = 6;
+constexpr uint32_t SLOT_BYTES = DEC_SLOT_ROWS * DK * sizeof(float);   // 32 KiB
+constexpr int DEC_COPIES = 2;                              // bulk copies per slot
 
 struct DecodeSmem {
-    alignas(128) float slot[DEC_SLOTS][DV * DK];   // TMA destinations
+    alignas(128) float slot[DEC_SLOTS][DEC_SLOT_ROWS * DK];   // TMA destinations
     alignas(16) float q[DK];                        // read as float4
     alignas(16) float k[DK];
     alignas(16) float v[2][DV];
@@ -77,28 +82,75 @@ struct DecodeSmem {
     alignas(8) uint64_t full[DEC_SLOTS];
     float red[32];
     float gate[2][2];
-    int pending[DEC_SLOTS];   // state number whose load is outstanding in each slot, or -1
+    int pending[DEC_SLOTS];   // unit number whose load is outstanding in each slot, or -1
     int abort;
 };
 constexpr size_t DEC_SMEM = sizeof(DecodeSmem) + 128;   // + alignment slack
 
-// Issues the TMA load of this CTA's state number `s` (item s/2, half s%2) into
-// slot s%3. Caller: thread 0 only.
-__device__ __forceinline__ void decode_issue_load(DecodeSmem &sm, const DecodeArgs &a, int s)
+// Issues the TMA load of this CTA's unit number `u` into slot u % DEC_SLOTS.
+// Units walk item by item, V-head by V-head, then slot-sized row blocks:
+// u = (2 * m + h) * DEC_UNITS + part. Caller: thread 0 only.
+__device__ __forceinline__ void decode_issue_load(DecodeSmem &sm, const DecodeArgs &a, int u)
 {
-    const int item = blockIdx.x + (s >> 1) * gridDim.x;
+    const int item = blockIdx.x + (u / (2 * DEC_UNITS)) * gridDim.x;
     if (item >= a.n_items) return;
-    const int b = item / HK, kh = item % HK, vh = kh + HK * (s & 1);
-    const char *src = reinterpret_cast<const char *>(a.ssm_state + ((size_t)b * HV + vh) * (DV * DK));
-    const int slot = s % DEC_SLOTS;
-    sm.pending[slot] = s;
+    const int h = (u / DEC_UNITS) & 1, part = u % DEC_UNITS;
+    const int b = item / HK, kh = item % HK, vh = kh + HK * h;
+    const char *src = reinterpret_cast<const char *>(a.ssm_state + ((size_t)b * HV + vh) * (DV * DK)) +
+                      (size_t)part * SLOT_BYTES;
+    const int slot = u % DEC_SLOTS;
+    sm.pending[slot] = u;
     const uint32_t bar = smem_u32(&sm.full[slot]);
     const uint32_t dst = smem_u32(sm.slot[slot]);
-    mbar_arrive_expect_tx(bar, STATE_BYTES);
+    mbar_arrive_expect_tx(bar, SLOT_BYTES);
 #pragma unroll
     for (int c = 0; c < DEC_COPIES; ++c)
-        bulk_g2s(dst + c * (STATE_BYTES / DEC_COPIES), src + c * (STATE_BYTES / DEC_COPIES),
-                 STATE_BYTES / DEC_COPIES, bar);
+        bulk_g2s(dst + c * (SLOT_BYTES / DEC_COPIES), src + c * (SLOT_BYTES / DEC_COPIES), SLOT_BYTES / DEC_COPIES,
+                 bar);
+}
+
+// Global inputs of one item's prologue held by thread `tid`: its conv channel
+// (raw conv_state rows, current input, taps) and, for threads 0 and 1, the
+// gate inputs of V-heads kh and kh + 16.
+template <typename TA> struct PrologueIn {
+    TA s0, s1, s2, xc, al, be, zc;
+    float4 w;
+    float A_log, dt_bias;
+};
+
+// conv channel of thread tid within item (., kh): q | k of K-head kh, v of vh = kh, v of vh = kh + 16
+__device__ __forceinline__ int item_channel(int kh, int tid)
+{
+    if (tid < 128) return Q_OFF + kh * DK + tid;
+    if (tid < 256) return K_OFF + kh * DK + (tid - 128);
+    if (tid < 384) return V_OFF + kh * DV + (tid - 256);
+    return V_OFF + (kh + HK) * DV + (tid - 384);
+}
+
+template <typename TA>
+__device__ __forceinline__ PrologueIn<TA> prologue_load(const DecodeArgs &a, int item, int tid)
+{
+    PrologueIn<TA> p;
+    const size_t b = item / HK;
+    const int kh = item % HK;
+    const int c = item_channel(kh, tid);
+    const TA *x = static_cast<const TA *>(a.qkv) + b * CC;
+    const TA *cs = static_cast<const TA *>(a.conv_state) + b * (size_t)(KC - 1) * CC;
+    p.w = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + c);
+    p.s0 = cs[c]; p.s1 = cs[CC + c]; p.s2 = cs[2 * CC + c]; p.xc = x[c];
+    // threads 0..255 also hold z of output column j = tid & 127 of V-head kh + 16 * (tid >> 7)
+    p.zc = tid < 2 * DV ? static_cast<const TA *>(a.z)[b * DI + (size_t)(kh + HK * (tid >> 7)) * DV + (tid & 127)]
+                        : from_f<TA>(0.0f);
+    p.al = p.be = from_f<TA>(0.0f);
+    p.A_log = p.dt_bias = 0.0f;
+    if (tid < 2) {
+        const int vh = kh + HK * tid;
+        p.al = static_cast<const TA *>(a.alpha)[b * HV + vh];
+        p.be = static_cast<const TA *>(a.beta)[b * HV + vh];
+        p.A_log = a.A_log[vh];
+        p.dt_bias = a.dt_bias[vh];
+    }
+    return p;
 }
 
 template <typename TA, typename TO>
@@ -121,6 +173,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
         for (int s = 0; s < DEC_SLOTS; ++s) decode_issue_load(sm, a, s);
 
     const float scale = rsqrtf((float)DK);
+    PrologueIn<TA> pin;
+    if ((int)blockIdx.x < a.n_items) pin = prologue_load<TA>(a, blockIdx.x, tid);
     for (int m = 0;; ++m) {
         const int item = blockIdx.x + m * gridDim.x;
         if (item >= a.n_items) break;
@@ -128,28 +182,21 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
         const int kh = item % HK;
 
         // ---- item prologue: conv + SiLU of the item's 512 channels (q and k of
-        //      K-head kh, v of both V-heads), state shift, L2 norms, gates.
+        //      K-head kh, v of both V-heads), state shift, L2 norms, gates. Its
+        //      global inputs were loaded one item ahead (pin).
         {
-            int c;
-            if (tid < 128) c = Q_OFF + kh * DK + tid;
-            else if (tid < 256) c = K_OFF + kh * DK + (tid - 128);
-            else if (tid < 384) c = V_OFF + kh * DV + (tid - 256);
-            else c = V_OFF + (kh + HK) * DV + (tid - 384);
-            const TA *x = static_cast<const TA *>(a.qkv) + b * CC;
             TA *cs = static_cast<TA *>(a.conv_state) + b * (size_t)(KC - 1) * CC;
-            const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + c);
-            const TA s0 = cs[c], s1 = cs[CC + c], s2 = cs[2 * CC + c], xc = x[c];
-            const float xh = silu_f(w.x * to_f(s0) + w.y * to_f(s1) + w.z * to_f(s2) + w.w * to_f(xc));
-            cs[c] = s1;                       // this CTA owns channel c of sequence b
-            cs[CC + c] = s2;
-            cs[2 * CC + c] = xc;
+            const int c = item_channel(kh, tid);
+            const float xh = silu_f(pin.w.x * to_f(pin.s0) + pin.w.y * to_f(pin.s1) + pin.w.z * to_f(pin.s2) +
+                                    pin.w.w * to_f(pin.xc));
+            cs[c] = pin.s1;                   // this CTA owns channel c of sequence b
+            cs[CC + c] = pin.s2;
+            cs[2 * CC + c] = pin.xc;
             const float ss = warp_sum(xh * xh);
             if (lane == 0) sm.red[warp] = ss;
             if (tid < 2) {
-                const int vh = kh + HK * tid;
                 float ga, gb;
-                gates_f(a.A_log[vh], a.dt_bias[vh], to_f(static_cast<const TA *>(a.alpha)[b * HV + vh]),
-                        to_f(static_cast<const TA *>(a.beta)[b * HV + vh]), ga, gb);
+                gates_f(pin.A_log, pin.dt_bias, to_f(pin.al), to_f(pin.be), ga, gb);
                 sm.gate[tid][0] = ga;
                 sm.gate[tid][1] = gb;
             }
@@ -159,14 +206,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
             else sm.v[(tid - 256) >> 7][tid & 127] = xh;
             __syncthreads();
         }
+        const TA zcur = pin.zc;
+        // the next item's prologue inputs: their latency hides behind this item's sweep
+        if (item + (int)gridDim.x < a.n_items) pin = prologue_load<TA>(a, item + gridDim.x, tid);
 
         // ---- the two states of the item: recurrence (a)-(d) row by row
         const float4 k4 = reinterpret_cast<const float4 *>(sm.k)[lane];
         const float4 q4 = reinterpret_cast<const float4 *>(sm.q)[lane];
-        for (int h = 0; h < 2; ++h) {
-            const int s = 2 * m + h;
-            const int slot = s % DEC_SLOTS;
-            if (!mbar_wait_bounded(smem_u32(&sm.full[slot]), (uint32_t)((s / DEC_SLOTS) & 1))) sm.abort = 1;
+        for (int hp = 0; hp < 2 * DEC_UNITS; ++hp) {
+            const int h = hp / DEC_UNITS, part = hp % DEC_UNITS;
+            const int u = 2 * DEC_UNITS * m + hp;
+            const int slot = u % DEC_SLOTS;
+            if (!mbar_wait_bounded(smem_u32(&sm.full[slot]), (uint32_t)((u / DEC_SLOTS) & 1))) sm.abort = 1;
             __syncthreads();
             if (sm.abort) break;
             const int vh = kh + HK * h;
@@ -175,8 +226,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
             const float4 *src = reinterpret_cast<const float4 *>(sm.slot[slot]);
 #pragma unroll
             for (int r = 0; r < DEC_ROWS_PER_WARP; ++r) {
-                const int j = warp * DEC_ROWS_PER_WARP + r;
-                float4 st = src[j * (DK / 4) + lane];
+                const int jl = warp * DEC_ROWS_PER_WARP + r;     // row within the slot
+                const int j = part * DEC_SLOT_ROWS + jl;
+                float4 st = src[jl * (DK / 4) + lane];
                 st.x *= dec; st.y *= dec; st.z *= dec; st.w *= dec;                                   // (a)
                 const float pred = warp_sum(st.x * k4.x + st.y * k4.y + st.z * k4.z + st.w * k4.w);    // (b)
                 const float delta = (sm.v[h][j] - pred) * beta;
@@ -189,7 +241,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
             if (tid == 0) {
                 sm.pending[slot] = -1;
                 fence_proxy_async_smem();
-                decode_issue_load(sm, a, s + DEC_SLOTS);
+                decode_issue_load(sm, a, u + DEC_SLOTS);
             }
         }
         if (sm.abort) break;
@@ -207,7 +259,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
             const float *rr4 = sm.red + 16 + 4 * h;
             const float rr = rsqrtf((rr4[0] + rr4[1] + rr4[2] + rr4[3]) * (1.0f / DV) + a.norm_eps);
             const size_t o = b * DI + (size_t)(kh + HK * h) * DV + j;
-            const float zz = to_f(static_cast<const TA *>(a.z)[o]);
+            const float zz = to_f(zcur);
             static_cast<TO *>(a.out)[o] = from_f<TO>(sm.y[h][j] * rr * a.norm_w[j] * silu_f(zz));
         }
         // the next prologue writes q/k/v/red[0..7]/gate, none of which the lines above read
