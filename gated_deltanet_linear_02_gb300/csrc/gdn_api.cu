@@ -70,6 +70,11 @@ int resolve_chunk(int chunk_size, gdn_dtype act)
 
 }  // namespace
 
+namespace gdn {
+// Lets other translation units of the library set the gdn_last_error() text.
+void record_error(const char *msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+}  // namespace gdn
+
 extern "C" {
 
 int gdn_abi_version(void) { return GDN_ABI_VERSION; }

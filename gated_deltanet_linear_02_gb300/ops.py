@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill.restype = _int
         L.gdn_prefill.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 5 + [_int, _int] + [_vp] * 5 + \
             [_int, _int, _int, _vp, _sz, _vp]
+        L.gdn_prefill_static.restype = _int
+        L.gdn_prefill_static.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 5 + [_int, _int] + [_vp] * 5 + \
+            [_int, _int, _int, _vp]
         L.gdn_prefill_workspace_size.restype = _sz
         L.gdn_prefill_workspace_size.argtypes = [_int, _int, _int, _int]
         L.gdn_device_error.restype = _int
@@ -190,3 +193,28 @@ def device_error(stream=None) -> int:
     """Synchronises the stream, then reads and clears the library's device error
     word: GDN_OK, or GDN_ERR_TIMEOUT if a bounded device-side wait gave up."""
     return lib().gdn_device_error(_stream(stream))
+
+
+STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def prefill_static(params, qkv, z, alpha, beta, cu_seqlens, out, conv_state_in=None, conv_state_out=None,
+                   ssm_state_in=None, ssm_state_out=None, chunk_size: int = 0, stream=None,
+                   cparams: gdn_params | None = None):
+    """gdn_prefill_static: gdn_prefill without a workspace argument, for callers
+    that cannot allocate device memory. The library's fixed 64 MiB device
+    scratch is used instead, shared by every call on the device."""
+    T = qkv.shape[0]
+    N = cu_seqlens.shape[0] - 1
+    dt = qkv.dtype
+    cp = cparams if cparams is not None else make_params(params)
+    st = lib().gdn_prefill_static(ctypes.byref(cp), _ptr(qkv, "qkv", (T, CC)), _ptr(z, "z", (T, DI), dt),
+                                  _ptr(alpha, "alpha", (T, HV), dt), _ptr(beta, "beta", (T, HV), dt),
+                                  _ptr(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32), N, T,
+                                  _ptr(conv_state_in, "conv_state_in", (N, KC - 1, CC), dt),
+                                  _ptr(conv_state_out, "conv_state_out", (N, KC - 1, CC), dt),
+                                  _ptr(ssm_state_in, "ssm_state_in", (N, HV, DV, DK), torch.float32),
+                                  _ptr(ssm_state_out, "ssm_state_out", (N, HV, DV, DK), torch.float32),
+                                  _ptr(out, "out", (T, DI)), _act_dtype(qkv), _act_dtype(out), int(chunk_size),
+                                  _stream(stream))
+    _check(st, "gdn_prefill_static")

@@ -144,6 +144,45 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
                        gdn_dtype act, gdn_dtype out_dt, int chunk_size, void *workspace,
                        size_t ws_bytes, void *stream);
 
+/*
+ * gdn_prefill_static -- gdn_prefill for callers that cannot allocate device
+ * memory. It takes the same arguments minus the workspace. The paper has no
+ * counterpart to this call: it exists only for how the library is used.
+ *
+ * Who needs it: code that runs where allocation is not allowed or not
+ * possible. Examples are a plugin inside a framework that owns every device
+ * allocation and hands it only input and output buffers, or a serving loop
+ * that forbids allocation after start-up. Such a caller has no workspace to
+ * pass.
+ *
+ * Scratch: a file-scope device array of GDN_STATIC_SCRATCH_BYTES (64 MiB) in
+ * libgdn. Every GPU that loads the library holds it until the process exits.
+ * A call whose gdn_prefill_workspace_size(N, T_total, act, chunk_size) exceeds
+ * it returns GDN_ERR_WORKSPACE without launching anything, and gdn_last_error()
+ * states the size it would need. As a guide, one bf16 sequence of up to about
+ * 1,100 tokens fits with the chunked form, and about 1,300 tokens with the
+ * exact scan.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it. Make that
+ * first call before any stream capture on the device.
+ *
+ * Sharing: every call on a device uses the same scratch, and the scratch keeps
+ * the previous call's contents (the kernels need none of it cleared). Calls
+ * that overlap on the GPU (different streams, or another host thread) race on
+ * it. Order them on one stream.
+ *
+ * Allocation: none. No cudaMalloc, no cudaFree, no library allocator.
+ * Errors: as gdn_prefill, plus GDN_ERR_WORKSPACE for the size limit, and
+ * GDN_ERR_CUDA if the set-up lookup fails.
+ */
+#define GDN_STATIC_SCRATCH_BYTES (64u << 20)
+gdn_status gdn_prefill_static(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
+                              const void *beta, const int32_t *cu_seqlens, int N, int T_total,
+                              const void *conv_state_in, void *conv_state_out,
+                              const float *ssm_state_in, float *ssm_state_out, void *out,
+                              gdn_dtype act, gdn_dtype out_dt, int chunk_size, void *stream);
+
 /* Bytes of workspace gdn_prefill needs for these sizes (0 if the arguments are
  * invalid; never 0 for valid ones). Pure host arithmetic. */
 size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_size);
