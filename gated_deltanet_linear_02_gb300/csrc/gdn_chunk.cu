@@ -21,11 +21,13 @@
 //        per thread), then U and W (tf32 MMAs). It writes per (chunk, V-head)
 //        operand tiles to the workspace, already in the shared-memory layout
 //        the carry kernel feeds to its MMAs.
-//  carry (one CTA per (sequence, V-head)). This is the sequential chain over
-//        the chunks. The state lives in tensor memory (fp32) and as a bf16 copy
-//        in shared memory (the A operand of W S0 and Q S0). Per chunk: MMA (W S0,
-//        Q S0) -> Vnew = U - W S0 -> MMA (P Vnew, K^T Vnew into the state) ->
-//        state copy and decay -> gated RMSNorm . silu(z) of the chunk's output.
+//  carry (one CTA per (sequence, V-head, block of 32 value columns)). This is
+//        the sequential chain over the chunks, for the CTA's columns of S (the
+//        columns are independent). The state block lives in tensor memory
+//        (fp32) and as a bf16 copy in shared memory. Per chunk: MMA (W S0, Q S0)
+//        -> Vnew = U - W S0 -> MMA (P Vnew, K^T Vnew into the state) -> state
+//        copy and decay. y goes to a buffer, and the gated RMSNorm . silu(z)
+//        over each head's 128 columns runs as a separate kernel.
 // Operand precision: the products whose rounding reaches the tolerance budget
 // (U = T V, Q K^T, P Vnew, the state update) use tf32 operands, rounded to
 // nearest when stored. W S0 and Q S0 take bf16 operands (kind::f16). All
@@ -62,6 +64,7 @@ struct ChunkArgs {
     void *out;
     int32_t *chunk_off;       // [N+1]: first global chunk of each sequence
     unsigned char *blobs;     // [max_chunks][32] x BLOB_BYTES
+    float *ybuf;              // [T_total][4096]: y before the gated norm (scale applied)
 };
 
 __device__ __forceinline__ int cu_clamp(const int32_t *cu, int i, int lo, int hi)
@@ -394,23 +397,39 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
 }
 
 // ------------------------------------------------------------------- carry
+// One CTA per (sequence, V-head, block of 32 value columns j). Columns of S are
+// independent (pred_j and y_j read only column j), so the value dimension splits
+// exactly across the four CTAs of a V-head. Products per chunk, all written with
+// the token or key index as the MMA M dimension and the CTA's 32 columns as N:
+//   (1) Vn^(t,j) = W[t][i] S[i][j]          bf16, M=64 (t), N=32, K=128
+//       Y(t,j)   = Q~[t][i] S[i][j]         bf16, M=64,     N=32, K=128
+//   (2) Y(t,j)  += P[t][s] Vnew[s][j]       tf32, M=64,     N=32, K=64
+//       S(i,j)  += K~^T[i][t] Vnew[t][j]    tf32, M=128 (i), N=32, K=64
+// The state block S(i,j) lives in tensor memory (fp32, lane = i), plus a bf16
+// copy S^T[j][i] in shared memory as the B operand of (1). Vnew = U - W S goes to
+// shared memory as Vnew^T[j][t] (tf32), the B operand of (2). y (scale applied)
+// goes to a [T][4096] fp32 buffer, and a separate kernel applies the gated
+// RMSNorm across all 128 columns of each head.
 constexpr int P2_THREADS = 256;
-constexpr uint32_t S2_SS = 0;          // S^T bf16 [j][i] Kd128 (A of W S0, Q S0)         32 KiB
-constexpr uint32_t S2_WQ0 = 32768;     // W | Q~ (bf16 [t][i] Kd128, 16 KiB each), stage 0
-constexpr uint32_t S2_WQ1 = 65536;     //                                          stage 1
-constexpr uint32_t S2_PK0 = 98304;     // P (tf32 [t][s] Kd64) | K~^T (tf32 [i][t] Kd64), stage 0
-constexpr uint32_t S2_PK1 = 147456;    //                                                  stage 1
-constexpr uint32_t S2_VN = 196608;     // Vnew^T tf32 [j][t] Kd64; after the second MMA, y [t][j] fp32
-constexpr uint32_t S2_SMALL = 229376;
+constexpr int JB = 32;                 // value columns per CTA
+constexpr int NJB = DV / JB;           // CTAs per V-head
+constexpr uint32_t S2_SS = 0;          // S^T block bf16 [32 j][128 i] Kd128            8 KiB
+constexpr uint32_t S2_VN = 8192;       // Vnew^T block tf32 [32 j][64 t] Kd64             8 KiB
+constexpr uint32_t S2_WQ0 = 16384;     // W | Q~ (bf16 [t][i] Kd128, 16 KiB each), stage 0
+constexpr uint32_t S2_WQ1 = 49152;     //                                          stage 1
+constexpr uint32_t S2_PK0 = 81920;     // P (tf32 [t][s] Kd64) | K~^T (tf32 [i][t] Kd64), stage 0
+constexpr uint32_t S2_PK1 = 131072;    //                                                  stage 1
+constexpr uint32_t S2_SMALL = 180224;
 struct P2Small {
     uint64_t bar_wq[2], bar_pk[2], bar_m1, bar_m2;
     uint32_t tmem;
     int abort;
 };
 constexpr size_t P2_SMEM = S2_SMALL + sizeof(P2Small) + 128;
-constexpr uint32_t T2_WS = 0, T2_Y = 64, T2_S = 128, T2_COLS = 256;
+// tensor-memory columns: M=64 accumulators use lanes 0-15 of each lane quarter
+constexpr uint32_t T2_VN = 0, T2_Y = 32, T2_S = 64, T2_COLS = 128;
 
-// Caller: thread 0. Loads chunk c's W | Q~ and P | K~^T into stage c % 2.
+// Caller: thread 0. Loads chunk c's W | Q~ or P | K~^T into stage c % 2.
 template <bool WQ>
 __device__ __forceinline__ void carry_issue(const unsigned char *blob, uint32_t sb, P2Small &ss, int c)
 {
@@ -424,34 +443,41 @@ __device__ __forceinline__ void carry_issue(const unsigned char *blob, uint32_t 
     }
 }
 
-template <typename TO>
 __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
     P2Small &ss = *reinterpret_cast<P2Small *>(sm + S2_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n = blockIdx.x, vh = blockIdx.y;
-    const int q = warp & 3, hf = warp >> 2;
-    const int j = 32 * q + lane;                       // TMEM lane = value index j
+    const int n = blockIdx.x, vh = blockIdx.y, jb = blockIdx.z;
+    const int q = warp & 3, hf = warp >> 2;            // lane quarter; column half (16 of the 32)
+    const int i = 32 * q + lane;                       // key row i (M=128 accumulator lane)
+    const int t = 16 * q + lane;                       // token row t (M=64 accumulator, lanes < 16)
+    const bool trow = lane < 16;
+    const int j0 = JB * jb + 16 * hf;                  // first of this thread's 16 value columns
     const size_t sbase_g = ((size_t)n * HV + vh) * (DV * DK);
     const int g0 = __ldg(a.chunk_off + n);
     const int nc = max(0, __ldg(a.chunk_off + n + 1) - g0);
     const int seq0 = cu_clamp(a.cu, n, 0, a.T_total);
     const int seqL = cu_clamp(a.cu, n + 1, seq0, a.T_total) - seq0;
 
-    if (nc == 0) {                                     // empty sequence: the state passes through
+    if (nc == 0) {                                     // empty sequence: this block of the state passes through
         if (a.S_out)
-            for (int e = tid; e < DV * DK / 4; e += P2_THREADS) {
-                const float4 v = a.S_in ? reinterpret_cast<const float4 *>(a.S_in + sbase_g)[e]
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                reinterpret_cast<float4 *>(a.S_out + sbase_g)[e] = v;
+            for (int e = tid; e < JB * DK / 4; e += P2_THREADS) {
+                const size_t off = sbase_g / 4 + (size_t)JB * jb * (DK / 4) + e;
+                const float4 v = a.S_in ? reinterpret_cast<const float4 *>(a.S_in)[off] : make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(a.S_out)[off] = v;
             }
         return;
     }
     const uint32_t sb = smem_u32(sm);
     auto blob_of = [&](int c) { return a.blobs + ((size_t)(g0 + c) * HV + vh) * BLOB_BYTES; };
     auto gamma_of = [&](int c) { return c < nc ? *reinterpret_cast<const float *>(blob_of(c) + BLOB_G) : 0.0f; };
+    auto load_u = [&](int c, float4 (&u)[4]) {        // U[t][j0 .. j0+16) of chunk c
+        const float4 *U = reinterpret_cast<const float4 *>(blob_of(c) + BLOB_U + ((size_t)t * DV + j0) * 4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[e] = trow ? U[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
 
     if (warp == 0) {
         tc::tmem_alloc(smem_u32(&ss.tmem), T2_COLS);
@@ -471,47 +497,25 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
             carry_issue<false>(blob_of(c), sb, ss, c);
         }
     }
-    // operands of chunk 0 that go through registers: U column j, gamma_n
-    float u_cur[32], u_nxt[32];
-    {
-        const float *U = reinterpret_cast<const float *>(blob_of(0) + BLOB_U);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) u_cur[e] = U[(32 * hf + e) * DV + j];
-    }
+    float4 u_cur[4], u_nxt[4];
+    load_u(0, u_cur);
     float gam_c1 = gamma_of(1);                        // gamma_n of the next chunk
     tc::fence_before_sync();
     __syncthreads();
     const uint32_t tm = ss.tmem;
     tc::fence_after_sync();
 
-    // initial state: bf16 copy into shared memory, gamma_n(chunk 0) * S0 into TMEM
+    // initial state block: bf16 copy S^T[j][i] in shared memory, gamma_n(0) * S in TMEM
     {
         const float gam0 = gamma_of(0);
-        for (int cb = 0; cb < 4; ++cb) {
-            const int i0 = 64 * hf + 16 * cb;
-            float v[16];
-            if (a.S_in) {
-                const float4 *src = reinterpret_cast<const float4 *>(a.S_in + sbase_g + (size_t)j * DK + i0);
+        float v[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 x = src[e];
-                    v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = 0.0f;
-            }
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-                __align__(16) bf16 o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = from_f<bf16>(v[8 * h8 + e]);
-                *reinterpret_cast<uint4 *>(sm + S2_SS + km<2>(j, i0 + 8 * h8, DK)) = *reinterpret_cast<const uint4 *>(o);
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] *= gam0;
-            tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + i0), v);
+        for (int e = 0; e < 16; ++e) {
+            v[e] = a.S_in ? a.S_in[sbase_g + (size_t)(j0 + e) * DK + i] : 0.0f;
+            *reinterpret_cast<bf16 *>(sm + S2_SS + km<2>(16 * hf + e, i, DK)) = from_f<bf16>(v[e]);
+            v[e] *= gam0;
         }
+        tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), v);
         tc::wait_st();
     }
     fence_proxy_async_smem();
@@ -519,128 +523,92 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
     __syncthreads();
 
     const float scale = rsqrtf((float)DK);
-    const float4 wn = *reinterpret_cast<const float4 *>(a.norm_w + 4 * lane);
     for (int c = 0; c < nc; ++c) {
         const int st = c & 1;
-        const uint32_t spar = (uint32_t)((c >> 1) & 1);   // phase of this stage's barriers
+        const uint32_t spar = (uint32_t)((c >> 1) & 1);   // phase of this stage's load barriers
         const uint32_t par = (uint32_t)(c & 1);           // phase of the per-chunk MMA barriers
         const int nvc = max(0, min(CH, seqL - CH * c));
-        // (1) W S0 and Q S0 (bf16, M=128, N=64, K=128) into TMEM
+        // (1) Vn^ = W S and Y = Q~ S (bf16, M=64, N=32, K=128)
         if (tid == 0) {
             tc::fence_after_sync();
             if (!mbar_wait_bounded(smem_u32(&ss.bar_wq[st]), spar)) ss.abort = 1;
             const uint32_t wq = sb + (st ? S2_WQ1 : S2_WQ0);
-            const uint32_t id = tc::instr_desc(tc::FMT_BF16, 128, CH);
-            tc::mma_tile<false>(tm + T2_WS, sb + S2_SS, DK, wq, DK, DK, id, false);
-            tc::mma_tile<false>(tm + T2_Y, sb + S2_SS, DK, wq + 16384, DK, DK, id, false);
+            const uint32_t id = tc::instr_desc(tc::FMT_BF16, CH, JB);
+            tc::mma_tile<false>(tm + T2_VN, wq, DK, sb + S2_SS, DK, DK, id, false);
+            tc::mma_tile<false>(tm + T2_Y, wq + 16384, DK, sb + S2_SS, DK, DK, id, false);
             tc::mma_commit(smem_u32(&ss.bar_m1));
         }
-        // loads for later, issued now so that their latency hides behind the MMAs:
-        // this chunk's z rows (warp w: tokens 8w..8w+7), next chunk's U column, gamma two ahead
-        uint2 zr[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int t = 8 * warp + r;
-            zr[r] = t < nvc ? *reinterpret_cast<const uint2 *>(a.z + (size_t)(seq0 + CH * c + t) * DI +
-                                                              (size_t)vh * DV + 4 * lane)
-                            : make_uint2(0u, 0u);
-        }
-        if (c + 1 < nc) {
-            const float *U = reinterpret_cast<const float *>(blob_of(c + 1) + BLOB_U);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) u_nxt[e] = U[(32 * hf + e) * DV + j];
-        }
+        if (c + 1 < nc) load_u(c + 1, u_nxt);          // latency hides behind this chunk's chain
         const float gam_c2 = gamma_of(c + 2);
         if (!mbar_wait_bounded(smem_u32(&ss.bar_m1), par)) ss.abort = 1;
         tc::fence_after_sync();
-        // (2) Vnew^T = U^T - (W S0)^T -> tf32 tile
+        // Vnew = U - W S for token row t, columns j0..j0+16 -> Vnew^T tf32 tile
         {
-            float d[32];
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_WS + 32 * hf), *reinterpret_cast<float(*)[16]>(d));
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_WS + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(d + 16));
+            float d[16];
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_VN + 16 * hf), d);
             tc::wait_ld();
+            if (trow) {
+                const float *u = reinterpret_cast<const float *>(u_cur);
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4 *>(sm + S2_VN + km<4>(j, 32 * hf + e, CH)) = tc::tf32_rn(
-                    make_float4(u_cur[e] - d[e], u_cur[e + 1] - d[e + 1], u_cur[e + 2] - d[e + 2], u_cur[e + 3] - d[e + 3]));
+                for (int e = 0; e < 16; ++e)
+                    *reinterpret_cast<float *>(sm + S2_VN + km<4>(16 * hf + e, t, CH)) = tc::tf32_rn(u[e] - d[e]);
+            }
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         if (ss.abort) break;
-        // (3) Y += Vnew^T P^T and S += Vnew^T K~ (tf32)
+        // (2) Y += P Vnew and S += K~^T Vnew (tf32)
         if (tid == 0) {
             tc::fence_after_sync();
-            if (c + 2 < nc) carry_issue<true>(blob_of(c + 2), sb, ss, c + 2);   // stage free: MMA (1) done
+            if (c + 2 < nc) carry_issue<true>(blob_of(c + 2), sb, ss, c + 2);   // stage free: MMA (1) is done
             if (!mbar_wait_bounded(smem_u32(&ss.bar_pk[st]), spar)) ss.abort = 1;
             const uint32_t pk = sb + (st ? S2_PK1 : S2_PK0);
-            tc::mma_tile<true>(tm + T2_Y, sb + S2_VN, CH, pk, CH, CH, tc::instr_desc(tc::FMT_TF32, 128, CH), true);
-            tc::mma_tile<true>(tm + T2_S, sb + S2_VN, CH, pk + 16384, CH, CH, tc::instr_desc(tc::FMT_TF32, 128, 128),
+            tc::mma_tile<true>(tm + T2_Y, pk, CH, sb + S2_VN, CH, CH, tc::instr_desc(tc::FMT_TF32, CH, JB), true);
+            tc::mma_tile<true>(tm + T2_S, pk + 16384, CH, sb + S2_VN, CH, CH, tc::instr_desc(tc::FMT_TF32, 128, JB),
                                true);
             tc::mma_commit(smem_u32(&ss.bar_m2));
         }
         if (!mbar_wait_bounded(smem_u32(&ss.bar_m2), par)) ss.abort = 1;
         tc::fence_after_sync();
         if (tid == 0 && c + 2 < nc) carry_issue<false>(blob_of(c + 2), sb, ss, c + 2);
-        // (4) state: bf16 copy for the next chunk and decay by its gamma_n, or the final state out
-        for (int cb = 0; cb < 4; ++cb) {
-            const int i0 = 64 * hf + 16 * cb;
+        // state block: bf16 copy for the next chunk and decay by its gamma_n, or the final state out
+        {
             float v[16];
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_S + i0), v);
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), v);
             tc::wait_ld();
             if (c + 1 < nc) {
 #pragma unroll
-                for (int h8 = 0; h8 < 2; ++h8) {
-                    __align__(16) bf16 o[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = from_f<bf16>(v[8 * h8 + e]);
-                    *reinterpret_cast<uint4 *>(sm + S2_SS + km<2>(j, i0 + 8 * h8, DK)) =
-                        *reinterpret_cast<const uint4 *>(o);
+                for (int e = 0; e < 16; ++e) {
+                    *reinterpret_cast<bf16 *>(sm + S2_SS + km<2>(16 * hf + e, i, DK)) = from_f<bf16>(v[e]);
+                    v[e] *= gam_c1;
                 }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] *= gam_c1;
-                tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + i0), v);
+                tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), v);
             } else if (a.S_out) {
-                float4 *dst = reinterpret_cast<float4 *>(a.S_out + sbase_g + (size_t)j * DK + i0);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                for (int e = 0; e < 16; ++e) a.S_out[sbase_g + (size_t)(j0 + e) * DK + i] = v[e];
             }
         }
-        // y of this chunk -> [t][j] buffer (reuses the Vnew tile: the MMAs reading it are done)
-        float *Yb = reinterpret_cast<float *>(sm + S2_VN);
+        // y (scale applied) of token row t -> [T][4096] buffer
         {
-            float y[32];
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_Y + 32 * hf), *reinterpret_cast<float(*)[16]>(y));
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_Y + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(y + 16));
+            float y[16];
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_Y + 16 * hf), y);
             tc::wait_ld();
+            if (trow && t < nvc) {
+                float4 *dst = reinterpret_cast<float4 *>(a.ybuf + (size_t)(seq0 + CH * c + t) * DI + (size_t)vh * DV + j0);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) Yb[(32 * hf + e) * DV + j] = y[e] * scale;
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(y[4 * e] * scale, y[4 * e + 1] * scale, y[4 * e + 2] * scale, y[4 * e + 3] * scale);
+            }
         }
         tc::wait_st();
         fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
         if (ss.abort) break;
-        // (5) gated RMSNorm . silu(z) of the chunk's tokens (warp w: tokens 8w..8w+7)
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int t = 8 * warp + r;
-            if (t < nvc) {
-                const float4 y4 = *reinterpret_cast<const float4 *>(Yb + t * DV + 4 * lane);
-                const float ms = warp_sum(y4.x * y4.x + y4.y * y4.y + y4.z * y4.z + y4.w * y4.w) * (1.0f / DV);
-                const float rr = rsqrtf(ms + a.norm_eps);
-                const bf16 *zz = reinterpret_cast<const bf16 *>(&zr[r]);
-                TO *out = static_cast<TO *>(a.out) + (size_t)(seq0 + CH * c + t) * DI + (size_t)vh * DV + 4 * lane;
-                out[0] = from_f<TO>(y4.x * rr * wn.x * silu_f(to_f(zz[0])));
-                out[1] = from_f<TO>(y4.y * rr * wn.y * silu_f(to_f(zz[1])));
-                out[2] = from_f<TO>(y4.z * rr * wn.z * silu_f(to_f(zz[2])));
-                out[3] = from_f<TO>(y4.w * rr * wn.w * silu_f(to_f(zz[3])));
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) u_cur[e] = u_nxt[e];
+        for (int e = 0; e < 4; ++e) u_cur[e] = u_nxt[e];
         gam_c1 = gam_c2;
-        __syncthreads();                                // y buffer is the next chunk's Vnew tile
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -652,13 +620,19 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
 
 cudaError_t launch_conv_state_out_bf16(const int32_t *cu, int N, int T_total, const void *qkv, const void *cs_in,
                                        void *cs_out, cudaStream_t s);
+cudaError_t launch_gated_norm_bf16(const float *norm_w, float norm_eps, const void *z, const float *y, void *out,
+                                   int T_total, gdn_dtype out_dt, cudaStream_t s);
 
 static size_t off_blobs(int N) { return ((size_t)(N + 1) * sizeof(int32_t) + 255) & ~(size_t)255; }
+static size_t off_ybuf(int N, int T_total)
+{
+    return off_blobs(N) + ((size_t)T_total / CH + (size_t)N) * HV * BLOB_BYTES;
+}
 
+// Workspace of the chunked path: chunk offsets | per-(chunk, V-head) blobs | y buffer.
 size_t chunk_workspace_bytes(int N, int T_total)
 {
-    const size_t max_chunks = (size_t)T_total / CH + (size_t)N;
-    return off_blobs(N) + max_chunks * HV * BLOB_BYTES;
+    return off_ybuf(N, T_total) + (size_t)T_total * DI * sizeof(float);
 }
 
 cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
@@ -675,19 +649,18 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
     a.cs_in = (const bf16 *)cs_in; a.S_in = S_in; a.S_out = S_out; a.out = out;
     a.chunk_off = static_cast<int32_t *>(ws_body);
     a.blobs = static_cast<unsigned char *>(ws_body) + off_blobs(N);
+    a.ybuf = reinterpret_cast<float *>(static_cast<unsigned char *>(ws_body) + off_ybuf(N, T_total));
 
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P1_SMEM);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chunk_carry_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P2_SMEM);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(chunk_carry_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P2_SMEM);
+        e = cudaFuncSetAttribute(chunk_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P2_SMEM);
     if (e != cudaSuccess) return e;
 
     chunk_schedule_kernel<<<1, 1024, 0, s>>>(cu, N, T_total, a.max_chunks, a.chunk_off);
     if (a.max_chunks > 0) chunk_prep_kernel<<<dim3(a.max_chunks, HK), P1_THREADS, P1_SMEM, s>>>(a);
-    if (out_dt == GDN_F32) chunk_carry_kernel<float><<<dim3(N, HV), P2_THREADS, P2_SMEM, s>>>(a);
-    else chunk_carry_kernel<bf16><<<dim3(N, HV), P2_THREADS, P2_SMEM, s>>>(a);
+    chunk_carry_kernel<<<dim3(N, HV, NJB), P2_THREADS, P2_SMEM, s>>>(a);
     e = cudaGetLastError();
+    if (e == cudaSuccess) e = launch_gated_norm_bf16(p->norm_w, p->norm_eps, z, a.ybuf, out, T_total, out_dt, s);
     if (e == cudaSuccess && cs_out) e = launch_conv_state_out_bf16(cu, N, T_total, qkv, cs_in, cs_out, s);
     return e;
 }

@@ -292,6 +292,23 @@ cudaError_t launch_prefill_scan(const gdn_params *p, const void *qkv, const void
 
 namespace gdn {
 
+// The gated RMSNorm . silu(z) over a [T][4096] fp32 buffer of y (scale
+// applied), for the chunked path (bf16 activations).
+cudaError_t launch_gated_norm_bf16(const float *norm_w, float norm_eps, const void *z, const float *y, void *out,
+                                   int T_total, gdn_dtype out_dt, cudaStream_t s)
+{
+    if (T_total <= 0) return cudaSuccess;
+    ScanWs ws;
+    ws.x = nullptr;
+    ws.g = nullptr;
+    ws.y = const_cast<float *>(y);
+    if (out_dt == GDN_F32)
+        scan_norm_kernel<bf16, float><<<T_total, 256, 0, s>>>(norm_w, norm_eps, (const bf16 *)z, (float *)out, ws);
+    else
+        scan_norm_kernel<bf16, bf16><<<T_total, 256, 0, s>>>(norm_w, norm_eps, (const bf16 *)z, (bf16 *)out, ws);
+    return cudaGetLastError();
+}
+
 // conv_state_out for the chunked path (bf16 activations); same rule as above.
 cudaError_t launch_conv_state_out_bf16(const int32_t *cu, int N, int T_total, const void *qkv, const void *cs_in,
                                        void *cs_out, cudaStream_t s)

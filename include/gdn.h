@@ -159,8 +159,8 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
  * libgdn. Every GPU that loads the library holds it until the process exits.
  * A call whose gdn_prefill_workspace_size(N, T_total, act, chunk_size) exceeds
  * it returns GDN_ERR_WORKSPACE without launching anything, and gdn_last_error()
- * states the size it would need. As a guide, one bf16 sequence of up to about
- * 1,100 tokens fits with the chunked form, and about 1,300 tokens with the
+ * states the size it would need. As a guide, one bf16 sequence of up to 895
+ * tokens fits with the chunked form, and up to about 1,300 tokens with the
  * exact scan.
  *
  * Set-up: the first call on each device looks up the array's device address
