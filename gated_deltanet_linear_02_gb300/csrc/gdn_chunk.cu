@@ -63,6 +63,7 @@ struct ChunkArgs {
     float *S_out;
     void *out;
     int32_t *chunk_off;       // [N+1]: first global chunk of each sequence
+    int4 *chunk_info;         // [max_chunks]: {sequence, chunk in it, its first row, tokens}; -1 = unused
     unsigned char *blobs;     // [max_chunks][32] x BLOB_BYTES
     float *ybuf;              // [T_total][4096]: y before the gated norm (scale applied)
 };
@@ -75,9 +76,11 @@ __device__ __forceinline__ int cu_clamp(const int32_t *cu, int i, int lo, int hi
 // ------------------------------------------------------------------ schedule
 // chunk_off[n] = sum over m < n of ceil(L_m / 64), clamped to max_chunks.
 __global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t *__restrict__ cu, int N, int T_total,
-                                                              int max_chunks, int32_t *__restrict__ chunk_off)
+                                                              int max_chunks, int32_t *__restrict__ chunk_off,
+                                                              int4 *__restrict__ chunk_info)
 {
     __shared__ int part[1024];
+    __shared__ int total;
     const int tid = threadIdx.x;
     const int per = (N + 1023) / 1024;
     const int lo = min(tid * per, N), hi = min(lo + per, N);
@@ -96,14 +99,19 @@ __global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t *__r
             run += v;
         }
         chunk_off[N] = min(run, max_chunks);
+        total = min(run, max_chunks);
     }
     __syncthreads();
     int run = part[tid];
     for (int n = lo; n < hi; ++n) {
         chunk_off[n] = min(run, max_chunks);
         const int a = cu_clamp(cu, n, 0, T_total), b = cu_clamp(cu, n + 1, a, T_total);
-        run += (b - a + CH - 1) / CH;
+        const int nch = (b - a + CH - 1) / CH;
+        for (int c = 0; c < nch && run + c < max_chunks; ++c)   // {sequence, chunk in it, start row, tokens}
+            chunk_info[run + c] = make_int4(n, c, a, min(CH, b - a - CH * c));
+        run += nch;
     }
+    for (int g = total + tid; g < max_chunks; g += blockDim.x) chunk_info[g] = make_int4(-1, 0, 0, 0);
 }
 
 // -------------------------------------------------------------------- prep
@@ -112,16 +120,30 @@ constexpr uint32_t S1_QS = 0;          // q^ tf32 [t][i] Kd128; later (Gamma K)^
 constexpr uint32_t S1_KS = 32768;      // k^ tf32 [t][i] Kd128
 constexpr uint32_t S1_VT0 = 65536;     // v^T tf32 [j][s] Kd64, head 0
 constexpr uint32_t S1_VT1 = 98304;     //                    head 1
-constexpr uint32_t S1_LB0 = 131072;    // beta_r * L[r][s], plain fp32 [64][64], head 0
-constexpr uint32_t S1_LB1 = 147456;    //                                        head 1
+constexpr uint32_t S1_LB0 = 131072;    // beta_r * L[r][s], fp32 [64][64], 16-byte groups swizzled (lb_at), head 0
+constexpr uint32_t S1_LB1 = 147456;    //                                                                    head 1
 constexpr uint32_t S1_TS0 = 163840;    // T tf32 [t][s] Kd64, head 0
 constexpr uint32_t S1_TS1 = 180224;    //                     head 1
 constexpr uint32_t S1_GK1 = 196608;    // (Gamma K)^T tf32 [i][s] Kd64, head 1
 constexpr uint32_t S1_SMALL = 229376;
+// Float index of L[t][s] in a [64][64] tile whose 16-byte groups are XOR-swizzled
+// by the row: rows written one per lane spread over the banks, and a row still
+// reads as float4 groups of 4 consecutive s.
+__device__ __forceinline__ int lb_at(int t, int s) { return t * CH + (((s >> 2) ^ (t & 15)) << 2) + (s & 3); }
+// Raw bf16 inputs of the chunk, staged before the conv: 67 rows (positions
+// -3..63) x 512 channels, row stride padded to 1040 B. It overlays the
+// L / T / (Gamma K)^T area, which is written only after the conv.
+constexpr uint32_t S1_RAW = 131072;
+constexpr int RAW_ROWS = CH + KC - 1;
+constexpr int RAW_STRIDE = 1040;
+// conv taps of the 512 channels (4 blocks x 128 channels x 16 B), staged with the rows
+constexpr uint32_t S1_CW = 200832;
+static_assert(S1_RAW + RAW_ROWS * RAW_STRIDE <= S1_CW && S1_CW + 4 * 2048 <= S1_SMALL, "staging overlap");
 struct P1Small {
     float G[2][CH];     // chunk-local cumulative log-decay per V-head
     float B[2][CH];     // beta
     float gam[2][CH];   // exp(G)
+    float ktf[2][CH];   // exp(G_n - G_t), the row factor of K~
     uint64_t bar;
     uint32_t tmem;
     int abort;
@@ -140,20 +162,13 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x, kh = blockIdx.y;
 
-    const int n_chunks = __ldg(a.chunk_off + a.N);
-    if (g >= n_chunks) return;                         // uniform for the whole CTA
-    // sequence owning global chunk g: chunk_off[n] <= g < chunk_off[n+1]
-    int lo = 0, hi = a.N;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(a.chunk_off + mid) <= g) lo = mid; else hi = mid;
-    }
-    const int n = lo;
-    const int lc = g - __ldg(a.chunk_off + n);        // chunk index inside the sequence
-    const int seq0 = cu_clamp(a.cu, n, 0, a.T_total);
-    const int seqL = cu_clamp(a.cu, n + 1, seq0, a.T_total) - seq0;
+    const int4 ci = __ldg(a.chunk_info + g);
+    if (ci.x < 0) return;                              // no chunk here (uniform for the whole CTA)
+    const int n = ci.x;                                // sequence
+    const int lc = ci.y;                               // chunk index inside the sequence
+    const int seq0 = ci.z;                             // the sequence's first row
     const int t0 = seq0 + CH * lc;
-    const int nv = max(0, min(CH, seqL - CH * lc));   // valid tokens in this chunk
+    const int nv = ci.w;                               // valid tokens in this chunk (1..64)
 
     float *Qs = reinterpret_cast<float *>(sm + S1_QS);
     float *Ks = reinterpret_cast<float *>(sm + S1_KS);
@@ -168,41 +183,45 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
         ss.abort = 0;
         fence_mbar_init();
     }
+    __syncwarp();
 
-    // ---- B. conv + SiLU of the chunk's 512 channels; raw q, k into the tf32
-    //      tiles (normalised below), v^T of both heads straight into their tiles.
-    for (int rep = 0; rep < 2; ++rep) {
-        const int li = tid + P1_THREADS * rep;       // local channel 0..511
-        const int blk = li >> 7, d = li & 127;
-        const int c = blk == 0 ? Q_OFF + kh * DK + d
-                    : blk == 1 ? K_OFF + kh * DK + d
-                    : blk == 2 ? V_OFF + kh * DV + d
-                               : V_OFF + (kh + HK) * DV + d;
-        const float4 w = __ldg(reinterpret_cast<const float4 *>(a.conv_w) + c);
-        float xm[3];
+    // ---- B1. stage the raw q|k|v inputs of chunk positions -3..63 (the 512
+    //      channels of this K-head pair: four 256-byte segments per row) and the
+    //      conv taps of those channels in shared memory. All 256 threads issue
+    //      their 16-byte loads at once, so the whole stage costs one memory latency.
+    const int chan0[4] = {Q_OFF + kh * DK, K_OFF + kh * DK, V_OFF + kh * DV, V_OFF + (kh + HK) * DV};
+    auto raw_src = [&](int r) -> const bf16 * {
+        const int p = r - 3;
+        if (p >= nv) return nullptr;                       // padding after the chunk's last token
+        const int pos = CH * lc + p;                       // relative to the sequence start
+        if (pos >= 0) return a.qkv + (size_t)(seq0 + pos) * CC;
+        return a.cs_in ? a.cs_in + ((size_t)n * (KC - 1) + (pos + KC - 1)) * CC : nullptr;
+    };
+    {
+        constexpr int RAW_U4 = RAW_ROWS * 64;              // 16-byte pieces of row data
+        constexpr int CW_U4 = 4 * DK;                      // 16-byte pieces of conv taps
+        constexpr int ITER = (RAW_U4 + CW_U4 + P1_THREADS - 1) / P1_THREADS;
+        uint4 v[ITER];
 #pragma unroll
-        for (int m = 0; m < 3; ++m) {                  // positions -3, -2, -1 of the chunk
-            const int pos = CH * lc - 3 + m;           // relative to the sequence start
-            float v = 0.0f;
-            if (pos >= 0) v = to_f(a.qkv[(size_t)(seq0 + pos) * CC + c]);
-            else if (a.cs_in) v = to_f(a.cs_in[((size_t)n * (KC - 1) + (pos + KC - 1)) * CC + c]);
-            xm[m] = v;
-        }
-        unsigned char *dst = blk == 0 ? sm + S1_QS : blk == 1 ? sm + S1_KS : blk == 2 ? sm + S1_VT0 : sm + S1_VT1;
-        for (int pb = 0; pb < CH; pb += 32) {          // 32 independent loads in flight per thread
-            float xs[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                xs[e] = (pb + e) < nv ? to_f(a.qkv[(size_t)(t0 + pb + e) * CC + c]) : 0.0f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int p = pb + e;
-                const float u = w.x * xm[0] + w.y * xm[1] + w.z * xm[2] + w.w * xs[e];
-                const float val = p < nv ? silu_f(u) : 0.0f;
-                xm[0] = xm[1]; xm[1] = xm[2]; xm[2] = xs[e];
-                const uint32_t off = blk < 2 ? km<4>(p, d, DK) : km<4>(d, p, CH);
-                *reinterpret_cast<float *>(dst + off) = blk < 2 ? val : tc::tf32_rn(val);   // q, k rounded after the norm
+        for (int k = 0; k < ITER; ++k) {
+            const int e = tid + k * P1_THREADS;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (e < RAW_U4) {
+                const bf16 *src = raw_src(e >> 6);
+                if (src) x = __ldg(reinterpret_cast<const uint4 *>(src + chan0[(e >> 4) & 3]) + (e & 15));
+            } else if (e < RAW_U4 + CW_U4) {
+                const int f = e - RAW_U4;                  // channel block f >> 7, channel f & 127
+                x = __ldg(reinterpret_cast<const uint4 *>(a.conv_w + (size_t)chan0[f >> 7] * KC) + (f & 127));
             }
+            v[k] = x;
+        }
+#pragma unroll
+        for (int k = 0; k < ITER; ++k) {
+            const int e = tid + k * P1_THREADS;
+            if (e < RAW_U4)
+                *reinterpret_cast<uint4 *>(sm + S1_RAW + (e >> 6) * RAW_STRIDE + ((e >> 4) & 3) * 256 + (e & 15) * 16) = v[k];
+            else if (e < RAW_U4 + CW_U4)
+                *reinterpret_cast<uint4 *>(sm + S1_CW + (e - RAW_U4) * 16) = v[k];
         }
     }
     // gates of both V-heads; padded tokens get g = 0, beta = 0
@@ -220,17 +239,73 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
     }
     __syncthreads();
 
-    // ---- C. L2 norm of the 64 q rows and 64 k rows (one warp per row, 16 rows per warp)
-    for (int rr = 0; rr < 16; ++rr) {
-        const int r = warp * 16 + rr;
-        float *tile = r < CH ? Qs : Ks;
-        const int t = r & 63;
-        float4 *p4 = reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(tile) + km<4>(t, lane * 4, DK));
-        float4 v = *p4;
-        const float s2 = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+    // ---- B2. conv + SiLU from the staged rows. q and k go raw into their tf32
+    //      tiles (normalised below); v^T of both heads goes straight into its
+    //      tiles. Lanes map onto the 8 rows of a core matrix, so each 16-byte
+    //      store of a warp phase fills one contiguous 128-byte core matrix.
+    const unsigned char *raw = sm + S1_RAW;
+    for (int it = warp; it < 128; it += P1_THREADS / 32) {           // q, k: (tile, row octet, k-group)
+        const int tile = it >> 6, po = (it >> 3) & 7, kgh = it & 7;
+        const int p = po * 8 + (lane & 7);
+        const int d = 4 * (kgh * 4 + (lane >> 3));                    // 4 consecutive channels d..d+3
+        float x[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {                                 // positions p-3+m = rows p+m
+            const uint2 pr = *reinterpret_cast<const uint2 *>(raw + (p + m) * RAW_STRIDE + (tile * DK + d) * 2);
+            const bf16 *hv = reinterpret_cast<const bf16 *>(&pr);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[m][e] = to_f(hv[e]);
+        }
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 w = reinterpret_cast<const float4 *>(sm + S1_CW + tile * 2048)[d + e];
+            const float u = w.x * x[0][e] + w.y * x[1][e] + w.z * x[2][e] + w.w * x[3][e];
+            o[e] = p < nv ? silu_fast(u) : 0.0f;
+        }
+        *reinterpret_cast<float4 *>(sm + (tile ? S1_KS : S1_QS) + km<4>(p, d, DK)) = make_float4(o[0], o[1], o[2], o[3]);
+    }
+    for (int it = warp; it < 128; it += P1_THREADS / 32) {           // v^T: (head, row octet of j, token group)
+        const int hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
+        const int d = dob * 8 + (lane & 7);
+        const int p0 = 4 * (pgh * 4 + (lane >> 3));                  // tokens p0..p0+3
+        const float4 w = reinterpret_cast<const float4 *>(sm + S1_CW + (2 + hv) * 2048)[d];
+        float x[7];
+#pragma unroll
+        for (int m = 0; m < 7; ++m)                                   // positions p0-3 .. p0+3
+            x[m] = to_f(*reinterpret_cast<const bf16 *>(raw + (p0 + m) * RAW_STRIDE + ((2 + hv) * DV + d) * 2));
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float u = w.x * x[e] + w.y * x[e + 1] + w.z * x[e + 2] + w.w * x[e + 3];
+            o[e] = (p0 + e) < nv ? tc::tf32_rn(silu_fast(u)) : 0.0f;
+        }
+        *reinterpret_cast<float4 *>(sm + (hv ? S1_VT1 : S1_VT0) + km<4>(d, p0, CH)) = make_float4(o[0], o[1], o[2], o[3]);
+    }
+    __syncthreads();
+
+    // ---- C. L2 norm of the 64 q rows and 64 k rows. A warp takes 8 rows at a
+    //      time; lane (row r%8, k-group) reads 8 float4s, and the 4 lanes of a
+    //      row combine their sums with two shuffles.
+    for (int gi = warp; gi < 16; gi += P1_THREADS / 32) {
+        float *tile = gi < 8 ? Qs : Ks;
+        const int t = (gi & 7) * 8 + (lane & 7), kgl = lane >> 3;
+        float4 v[8];
+        float s2 = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            v[m] = *reinterpret_cast<const float4 *>(reinterpret_cast<unsigned char *>(tile) + km<4>(t, 4 * (4 * m + kgl), DK));
+            s2 += v[m].x * v[m].x + v[m].y * v[m].y + v[m].z * v[m].z + v[m].w * v[m].w;
+        }
+        s2 += __shfl_xor_sync(0xffffffffu, s2, 8);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, 16);
         const float inv = rsqrtf(s2 + a.l2_eps);
-        v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
-        *p4 = tc::tf32_rn(v);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            float4 x = v[m];
+            x.x *= inv; x.y *= inv; x.z *= inv; x.w *= inv;
+            *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(tile) + km<4>(t, 4 * (4 * m + kgl), DK)) = tc::tf32_rn(x);
+        }
     }
     if (lane == 0 && warp < 2) {                      // warp 0: head 0, warp 1: head 1
         float run = 0.0f;
@@ -240,7 +315,11 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
         }
     }
     __syncthreads();
-    if (tid < 2 * CH) ss.gam[tid >> 6][tid & 63] = expf(ss.G[tid >> 6][tid & 63]);
+    if (tid < 2 * CH) {
+        const int h = tid >> 6, p = tid & 63;
+        ss.gam[h][p] = expf(ss.G[h][p]);
+        ss.ktf[h][p] = __expf(ss.G[h][CH - 1] - ss.G[h][p]);   // K~ row factor, exponent <= 0
+    }
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -271,31 +350,39 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
         tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_QK + 32 * hf), *reinterpret_cast<float(*)[16]>(qk));
         tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_QK + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(qk + 16));
         tc::wait_ld();
-        if (lane < 16 && !ss.abort) {
-            const int t = 16 * q + lane;
+        // Rows live in lanes 0..15. Lanes 16..31 take over columns 16..31 of their row.
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const float a1 = __shfl_sync(0xffffffffu, kk[16 + c], lane & 15);
+            const float a2 = __shfl_sync(0xffffffffu, qk[16 + c], lane & 15);
+            if (lane >= 16) { kk[c] = a1; qk[c] = a2; }
+        }
+        if (!ss.abort) {
+            const int t = 16 * q + (lane & 15);
+            const int cbase = 32 * hf + 16 * (lane >> 4);     // this lane's 16 columns
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const float Gt = ss.G[h][t], bt = ss.B[h][t];
                 float *Lb = reinterpret_cast<float *>(sm + (h ? S1_LB1 : S1_LB0));
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
+                for (int c4 = 0; c4 < 4; ++c4) {
                     float pv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int cc = c4 * 4 + e, s = 32 * hf + cc;
-                        const float dec = s <= t ? expf(Gt - ss.G[h][s]) : 0.0f;
-                        Lb[t * CH + s] = s < t ? bt * dec * kk[cc] : 0.0f;
+                        const int cc = c4 * 4 + e, s = cbase + cc;
+                        const float dec = s <= t ? __expf(Gt - ss.G[h][s]) : 0.0f;
+                        Lb[lb_at(t, s)] = s < t ? bt * dec * kk[cc] : 0.0f;
                         pv[e] = dec * qk[cc];
                     }
-                    *reinterpret_cast<float4 *>(blob[h] + BLOB_P + km<4>(t, 32 * hf + c4 * 4, CH)) =
+                    *reinterpret_cast<float4 *>(blob[h] + BLOB_P + km<4>(t, cbase + c4 * 4, CH)) =
                         tc::tf32_rn(make_float4(pv[0], pv[1], pv[2], pv[3]));
                 }
             }
         }
     }
     // Q~ = diag(gamma) q^ -> bf16 K-major (Kd 128), 8 elements per store
-    for (int u = tid; u < 2 * CH * 16; u += P1_THREADS) {
-        const int h = u >> 10, t = (u >> 4) & 63, i8 = u & 15;
+    for (int u = tid; u < 2 * CH * 16; u += P1_THREADS) {   // lanes walk the 8 rows of a core matrix
+        const int h = u >> 10, i8 = (u >> 3) & 15, t = ((u >> 7) & 7) * 8 + (u & 7);
         const float gm = ss.gam[h][t];
         const float4 x0 = *reinterpret_cast<const float4 *>(sm + S1_QS + km<4>(t, i8 * 8, DK));
         const float4 x1 = *reinterpret_cast<const float4 *>(sm + S1_QS + km<4>(t, i8 * 8 + 4, DK));
@@ -304,15 +391,15 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
                                    from_f<bf16>(x1.z * gm), from_f<bf16>(x1.w * gm)};
         *reinterpret_cast<uint4 *>(blob[h] + BLOB_Q + km<2>(t, i8 * 8, DK)) = *reinterpret_cast<const uint4 *>(o);
     }
-    // K~^T [i][t] = exp(G_n - G_t) k^[t][i] -> tf32 K-major (Kd 64), 4 tokens per store
-    for (int u = tid; u < 2 * DK * 16; u += P1_THREADS) {
-        const int h = u >> 11, i = (u >> 4) & 127, t4 = u & 15;
-        const float Gn = ss.G[h][CH - 1];
+    // K~^T [i][t] = exp(G_n - G_t) k^[t][i] -> tf32 K-major (Kd 64), 4 tokens per
+    // store; lanes cover 4 whole core matrices, so a warp writes 512 contiguous bytes
+    for (int it = warp; it < 2 * 16 * 4; it += P1_THREADS / 32) {
+        const int h = it >> 6, i = ((it >> 2) & 15) * 8 + (lane & 7), t4 = (it & 3) * 4 + (lane >> 3);
         float v[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int t = t4 * 4 + e;
-            v[e] = expf(Gn - ss.G[h][t]) * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(t, i, DK));
+            v[e] = ss.ktf[h][t] * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(t, i, DK));
         }
         *reinterpret_cast<float4 *>(blob[h] + BLOB_KT + km<4>(i, t4 * 4, CH)) =
             tc::tf32_rn(make_float4(v[0], v[1], v[2], v[3]));
@@ -328,18 +415,26 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
         const float *Lb = reinterpret_cast<const float *>(sm + (h ? S1_LB1 : S1_LB0));
         float x[CH];
 #pragma unroll
+        for (int t = 0; t < CH; ++t) x[t] = 0.0f;     // x[s >= t] stay 0 while row t is summed
+#pragma unroll
         for (int t = 0; t < CH; ++t) {
             float acc[4] = {(t == c) ? ss.B[h][t] : 0.0f, 0.0f, 0.0f, 0.0f};   // 4 chains for ILP
 #pragma unroll
-            for (int s = 0; s < t; ++s) acc[s & 3] = fmaf(-Lb[t * CH + s], x[s], acc[s & 3]);
+            for (int s4 = 0; s4 < (t + 3) / 4; ++s4) {      // L[t][s] = 0 for s >= t
+                const float4 l4 = *reinterpret_cast<const float4 *>(Lb + lb_at(t, 4 * s4));
+                acc[0] = fmaf(-l4.x, x[4 * s4], acc[0]);
+                acc[1] = fmaf(-l4.y, x[4 * s4 + 1], acc[1]);
+                acc[2] = fmaf(-l4.z, x[4 * s4 + 2], acc[2]);
+                acc[3] = fmaf(-l4.w, x[4 * s4 + 3], acc[3]);
+            }
             x[t] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
         unsigned char *Ts = sm + (h ? S1_TS1 : S1_TS0);
 #pragma unroll
         for (int t = 0; t < CH; ++t) *reinterpret_cast<float *>(Ts + km<4>(t, c, CH)) = tc::tf32_rn(x[t]);
     } else {
-        for (int u = tid - 2 * CH; u < 2 * DK * 16; u += P1_THREADS - 2 * CH) {
-            const int h = u >> 11, i = (u >> 4) & 127, s4 = u & 15;
+        for (int it = warp - 4; it < 2 * 16 * 4; it += 4) {         // lanes cover whole core matrices
+            const int h = it >> 6, i = ((it >> 2) & 15) * 8 + (lane & 7), s4 = (it & 3) * 4 + (lane >> 3);
             float v[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -623,13 +718,17 @@ cudaError_t launch_conv_state_out_bf16(const int32_t *cu, int N, int T_total, co
 cudaError_t launch_gated_norm_bf16(const float *norm_w, float norm_eps, const void *z, const float *y, void *out,
                                    int T_total, gdn_dtype out_dt, cudaStream_t s);
 
-static size_t off_blobs(int N) { return ((size_t)(N + 1) * sizeof(int32_t) + 255) & ~(size_t)255; }
+static size_t off_info(int N) { return ((size_t)(N + 1) * sizeof(int32_t) + 255) & ~(size_t)255; }
+static size_t off_blobs(int N, int T_total)
+{
+    return off_info(N) + ((((size_t)T_total / CH + (size_t)N) * sizeof(int4) + 255) & ~(size_t)255);
+}
 static size_t off_ybuf(int N, int T_total)
 {
-    return off_blobs(N) + ((size_t)T_total / CH + (size_t)N) * HV * BLOB_BYTES;
+    return off_blobs(N, T_total) + ((size_t)T_total / CH + (size_t)N) * HV * BLOB_BYTES;
 }
 
-// Workspace of the chunked path: chunk offsets | per-(chunk, V-head) blobs | y buffer.
+// Workspace of the chunked path: chunk offsets | chunk descriptors | per-(chunk, V-head) blobs | y buffer.
 size_t chunk_workspace_bytes(int N, int T_total)
 {
     return off_ybuf(N, T_total) + (size_t)T_total * DI * sizeof(float);
@@ -648,7 +747,8 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
     a.max_chunks = T_total / CH + N;
     a.cs_in = (const bf16 *)cs_in; a.S_in = S_in; a.S_out = S_out; a.out = out;
     a.chunk_off = static_cast<int32_t *>(ws_body);
-    a.blobs = static_cast<unsigned char *>(ws_body) + off_blobs(N);
+    a.chunk_info = reinterpret_cast<int4 *>(static_cast<unsigned char *>(ws_body) + off_info(N));
+    a.blobs = static_cast<unsigned char *>(ws_body) + off_blobs(N, T_total);
     a.ybuf = reinterpret_cast<float *>(static_cast<unsigned char *>(ws_body) + off_ybuf(N, T_total));
 
     cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P1_SMEM);
@@ -656,7 +756,7 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
         e = cudaFuncSetAttribute(chunk_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P2_SMEM);
     if (e != cudaSuccess) return e;
 
-    chunk_schedule_kernel<<<1, 1024, 0, s>>>(cu, N, T_total, a.max_chunks, a.chunk_off);
+    chunk_schedule_kernel<<<1, 1024, 0, s>>>(cu, N, T_total, a.max_chunks, a.chunk_off, a.chunk_info);
     if (a.max_chunks > 0) chunk_prep_kernel<<<dim3(a.max_chunks, HK), P1_THREADS, P1_SMEM, s>>>(a);
     chunk_carry_kernel<<<dim3(N, HV, NJB), P2_THREADS, P2_SMEM, s>>>(a);
     e = cudaGetLastError();

@@ -37,6 +37,11 @@ template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __flo
 // SiLU(x) = x * sigmoid(x) (the conv activation and the output gate silu(z)).
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
+// SiLU with the fast exponential and division intrinsics (a few ulp). Used only
+// where the result becomes a tf32 tensor-core operand, whose rounding is about
+// 1e3 times coarser.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
 // softplus with a linear tail above 20, the same reading the oracle takes.
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
 
