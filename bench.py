@@ -165,12 +165,10 @@ def run_gpu(args, rank, world, dev):
             dist.barrier()
         torch.cuda.synchronize()
 
+    from gated_deltanet_linear_02_gb300.replicas import job_rate, slowest_ms
+
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return slowest_ms(x, device=dev)
 
     # ---------------- decode @ B=256 over 30 layers (headline)
     n_inputs = 8
@@ -191,7 +189,7 @@ def run_gpu(args, rank, world, dev):
     per_launch_s = dec_ms / 1e3 / launches
     bytes_per_launch = BATCH * DECODE_BYTES_PER_TOKEN_LAYER + DECODE_PARAM_BYTES_PER_LAUNCH
     achieved = bytes_per_launch / per_launch_s / 1e9
-    dec_tok_s = world * BATCH * args.steps / (dec_ms / 1e3)
+    dec_tok_s = job_rate(BATCH * args.steps, world, dec_ms)
 
     # ---------------- e2e: the same decode through the C ABI from pinned host buffers
     host_in = []
@@ -219,7 +217,7 @@ def run_gpu(args, rank, world, dev):
     ev1.record(stream)
     barrier_sync()
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1))
-    e2e_tok_s = world * BATCH * args.steps / (e2e_ms / 1e3)
+    e2e_tok_s = job_rate(BATCH * args.steps, world, e2e_ms)
     del layers, host_in, dev_in, host_out
     torch.cuda.empty_cache()
 
@@ -255,7 +253,7 @@ def run_gpu(args, rank, world, dev):
     sampler.mark(t_wall0, time.time())
     pf_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))
     assert ops.device_error() == ops.GDN_OK
-    pf_tok_s = world * PREFILL_T / (pf_ms / 1e3)
+    pf_tok_s = job_rate(PREFILL_T, world, pf_ms)
     pf_tflops = PREFILL_FLOP_PER_TOKEN * PREFILL_T / (pf_ms / 1e3) / 1e12
     clocks = sampler.stop()
 
