@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
 constexpr int P2_THREADS = 256;
 constexpr int JB = 32;                 // value columns per CTA
 constexpr int NJB = DV / JB;           // CTAs per V-head
-constexpr uint32_t S2_SS = 0;          // S^T block bf16 [32 j][128 i] Kd128            8 KiB
+constexpr uint32_t S2_SS = 0;          // S block bf16, MN-major (N = 32 j, K = 128 i)    8 KiB
 constexpr uint32_t S2_VN = 8192;       // Vnew^T block tf32 [32 j][64 t] Kd64             8 KiB
 constexpr uint32_t S2_WQ0 = 16384;     // W | Q~ (bf16 [t][i] Kd128, 16 KiB each), stage 0
 constexpr uint32_t S2_WQ1 = 49152;     //                                          stage 1
@@ -535,6 +535,21 @@ __device__ __forceinline__ void carry_issue(const unsigned char *blob, uint32_t 
     } else {
         mbar_arrive_expect_tx(smem_u32(&ss.bar_pk[st]), 49152);
         bulk_g2s(sb + (st ? S2_PK1 : S2_PK0), blob + BLOB_P, 49152, smem_u32(&ss.bar_pk[st]));
+    }
+}
+
+// Thread (key row i, column half hf) stores its 16 state values S[i][j], j in
+// [16hf, 16hf+16) of the CTA's block, as bf16 into the MN-major state tile:
+// two 16-byte stores.
+__device__ __forceinline__ void store_s_bf16(unsigned char *sm, int i, int hf, const float (&v)[16])
+{
+#pragma unroll
+    for (int g8 = 0; g8 < 2; ++g8) {
+        __align__(16) bf16 o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = from_f<bf16>(v[8 * g8 + e]);
+        *reinterpret_cast<uint4 *>(sm + S2_SS + tc::mnmajor_offset_bf16(16 * hf + 8 * g8, i, DK)) =
+            *reinterpret_cast<const uint4 *>(o);
     }
 }
 
@@ -605,11 +620,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
         const float gam0 = gamma_of(0);
         float v[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            v[e] = a.S_in ? a.S_in[sbase_g + (size_t)(j0 + e) * DK + i] : 0.0f;
-            *reinterpret_cast<bf16 *>(sm + S2_SS + km<2>(16 * hf + e, i, DK)) = from_f<bf16>(v[e]);
-            v[e] *= gam0;
-        }
+        for (int e = 0; e < 16; ++e) v[e] = a.S_in ? a.S_in[sbase_g + (size_t)(j0 + e) * DK + i] : 0.0f;
+        store_s_bf16(sm, i, hf, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] *= gam0;
         tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), v);
         tc::wait_st();
     }
@@ -628,9 +642,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
             tc::fence_after_sync();
             if (!mbar_wait_bounded(smem_u32(&ss.bar_wq[st]), spar)) ss.abort = 1;
             const uint32_t wq = sb + (st ? S2_WQ1 : S2_WQ0);
-            const uint32_t id = tc::instr_desc(tc::FMT_BF16, CH, JB);
-            tc::mma_tile<false>(tm + T2_VN, wq, DK, sb + S2_SS, DK, DK, id, false);
-            tc::mma_tile<false>(tm + T2_Y, wq + 16384, DK, sb + S2_SS, DK, DK, id, false);
+            const uint32_t id = tc::instr_desc(tc::FMT_BF16, CH, JB) | (1u << 16);   // B (the state) MN-major
+            const uint64_t bs = tc::smem_desc(sb + S2_SS, 128u, (uint32_t)DK * 16u);
+            tc::mma_steps<false>(tm + T2_VN, tc::kmajor_desc<2>(wq, 0, DK), bs, DK / 16, id, false);
+            tc::mma_steps<false>(tm + T2_Y, tc::kmajor_desc<2>(wq + 16384, 0, DK), bs, DK / 16, id, false);
             tc::mma_commit(smem_u32(&ss.bar_m1));
         }
         if (c + 1 < nc) load_u(c + 1, u_nxt);          // latency hides behind this chunk's chain
@@ -659,9 +674,11 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
             if (c + 2 < nc) carry_issue<true>(blob_of(c + 2), sb, ss, c + 2);   // stage free: MMA (1) is done
             if (!mbar_wait_bounded(smem_u32(&ss.bar_pk[st]), spar)) ss.abort = 1;
             const uint32_t pk = sb + (st ? S2_PK1 : S2_PK0);
-            tc::mma_tile<true>(tm + T2_Y, pk, CH, sb + S2_VN, CH, CH, tc::instr_desc(tc::FMT_TF32, CH, JB), true);
-            tc::mma_tile<true>(tm + T2_S, pk + 16384, CH, sb + S2_VN, CH, CH, tc::instr_desc(tc::FMT_TF32, 128, JB),
-                               true);
+            const uint64_t vn = tc::kmajor_desc<4>(sb + S2_VN, 0, CH);
+            tc::mma_steps<true>(tm + T2_Y, tc::kmajor_desc<4>(pk, 0, CH), vn, CH / 8, tc::instr_desc(tc::FMT_TF32, CH, JB),
+                                true);
+            tc::mma_steps<true>(tm + T2_S, tc::kmajor_desc<4>(pk + 16384, 0, CH), vn, CH / 8,
+                                tc::instr_desc(tc::FMT_TF32, 128, JB), true);
             tc::mma_commit(smem_u32(&ss.bar_m2));
         }
         if (!mbar_wait_bounded(smem_u32(&ss.bar_m2), par)) ss.abort = 1;
@@ -673,11 +690,9 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
             tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), v);
             tc::wait_ld();
             if (c + 1 < nc) {
+                store_s_bf16(sm, i, hf, v);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    *reinterpret_cast<bf16 *>(sm + S2_SS + km<2>(16 * hf + e, i, DK)) = from_f<bf16>(v[e]);
-                    v[e] *= gam_c1;
-                }
+                for (int e = 0; e < 16; ++e) v[e] *= gam_c1;
                 tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), v);
             } else if (a.S_out) {
 #pragma unroll

@@ -127,6 +127,29 @@ __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_base, int a
     }
 }
 
+// Same product with both descriptors given for the first K step: every MMA
+// instruction covers 32 bytes of K, i.e. two 128-byte core matrices along K, so
+// the next step's descriptors are the previous ones plus 256 B >> 4 = 16 in the
+// start-address field. This holds for K-major tiles (LBO 128) and for MN-major
+// bf16 tiles with 128-byte K-group stride.
+template <bool TF32>
+__device__ __forceinline__ void mma_steps(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, int steps, uint32_t idesc,
+                                          bool accumulate)
+{
+    for (int s = 0; s < steps; ++s) {
+        if (TF32) mma_tf32(d_tmem, a_desc + 16u * s, b_desc + 16u * s, idesc, (accumulate || s > 0) ? 1u : 0u);
+        else mma_f16(d_tmem, a_desc + 16u * s, b_desc + 16u * s, idesc, (accumulate || s > 0) ? 1u : 0u);
+    }
+}
+
+// Byte offset of element (n, k) in an MN-major, no-swizzle bf16 tile with Kd
+// columns along K: 16-byte MN groups (8 elements) are SBO = Kd * 16 bytes apart,
+// groups of 8 K rows are 128 bytes apart, and each K row is 16 bytes.
+__host__ __device__ __forceinline__ uint32_t mnmajor_offset_bf16(int n, int k, int Kd)
+{
+    return (uint32_t)((n >> 3) * (Kd * 16) + (k >> 3) * 128 + (k & 7) * 16 + (n & 7) * 2);
+}
+
 // ---- fences around thread synchronisation
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
