@@ -17,8 +17,8 @@
 // Two kernels:
 //  prep  (one CTA per (chunk, K-head); both V-heads of the GQA pair). This is
 //        the S-independent part: conv + SiLU, L2 norms, gates, K K^T and Q K^T
-//        (tf32 MMAs), the unit-lower triangular solve for T (fp32, one column
-//        per thread), then U and W (tf32 MMAs). It writes per (chunk, V-head)
+//        (tf32 MMAs), the unit-lower triangular inverse for T (fp32, two
+//        levels of 32x32 blocks), then U and W (tf32 MMAs). It writes per (chunk, V-head)
 //        operand tiles to the workspace, already in the shared-memory layout
 //        the carry kernel feeds to its MMAs.
 //  carry (one CTA per (sequence, V-head, block of 32 value columns)). This is
@@ -79,9 +79,8 @@ __global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t *__r
                                                               int max_chunks, int32_t *__restrict__ chunk_off,
                                                               int4 *__restrict__ chunk_info)
 {
-    __shared__ int part[1024];
-    __shared__ int total;
-    const int tid = threadIdx.x;
+    __shared__ int warp_part[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (N + 1023) / 1024;
     const int lo = min(tid * per, N), hi = min(lo + per, N);
     int sum = 0;
@@ -89,20 +88,30 @@ __global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t *__r
         const int a = cu_clamp(cu, n, 0, T_total), b = cu_clamp(cu, n + 1, a, T_total);
         sum += (b - a + CH - 1) / CH;
     }
-    part[tid] = sum;
+    // exclusive prefix sum of the per-thread chunk counts: inclusive scan within
+    // each warp, then a scan of the 32 warp totals by warp 0
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_part[warp] = incl;
     __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int i = 0; i < 1024; ++i) {
-            const int v = part[i];
-            part[i] = run;
-            run += v;
+    if (warp == 0) {
+        int w = warp_part[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += v;
         }
-        chunk_off[N] = min(run, max_chunks);
-        total = min(run, max_chunks);
+        warp_part[lane] = w;                            // inclusive over warps
     }
     __syncthreads();
-    int run = part[tid];
+    const int all = warp_part[31];
+    const int total = min(all, max_chunks);
+    if (tid == 0) chunk_off[N] = total;
+    int run = (warp ? warp_part[warp - 1] : 0) + incl - sum;
     for (int n = lo; n < hi; ++n) {
         chunk_off[n] = min(run, max_chunks);
         const int a = cu_clamp(cu, n, 0, T_total), b = cu_clamp(cu, n + 1, a, T_total);
@@ -408,40 +417,130 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---- F. T by forward substitution (threads 0..127: one column of one head)
-    //      while threads 128..255 build (Gamma K)^T of both heads.
-    if (tid < 2 * CH) {
-        const int h = tid >> 6, c = tid & 63;
-        const float *Lb = reinterpret_cast<const float *>(sm + (h ? S1_LB1 : S1_LB0));
-        float x[CH];
+    // ---- F. T = (I + A)^-1 diag(b), A = diag(b) L (Lb), in two 32x32 block
+    //      levels. With X_b = (I + A_bb)^-1 for the diagonal blocks b = 0, 1:
+    //        T_00 = X_0 diag(b_0),  T_11 = X_1 diag(b_1),  T_01 = 0,
+    //        T_10 = -X_1 (A_10 T_00)                     (block row 1 of (I + A) T).
+    //      Level 1 (threads 0..127: one column of one block of one head) runs
+    //      the forward substitutions while warps 4..7 build (Gamma K)^T of head 0;
+    //      level 2 spreads the two 32x32x32 products over all threads. The fp32
+    //      intermediates T_00, X_1 and M = A_10 T_00 sit in the head-1 (Gamma K)^T
+    //      area, which is built last.
+    {
+        constexpr int XS = 36;                               // X_1 row stride (floats): rows 2 apart hit other banks
+        auto t00_of = [&](int h) { return reinterpret_cast<float *>(sm + S1_GK1 + h * 12288); };
+        auto x1_of = [&](int h) { return reinterpret_cast<float *>(sm + S1_GK1 + h * 12288 + 4096); };
+        auto m_of = [&](int h) { return reinterpret_cast<float *>(sm + S1_GK1 + 24576 + h * 4096); };
+        static_assert(24576 + 2 * 4096 <= 32768 && 4096 + 32 * XS * 4 <= 12288, "solve scratch");
+        if (tid < 2 * CH) {
+            const int h = tid >> 6, b = (tid >> 5) & 1, c = tid & 31;
+            const float *Lb = reinterpret_cast<const float *>(sm + (h ? S1_LB1 : S1_LB0));
+            float x[32];
 #pragma unroll
-        for (int t = 0; t < CH; ++t) x[t] = 0.0f;     // x[s >= t] stay 0 while row t is summed
+            for (int r = 0; r < 32; ++r) x[r] = 0.0f;     // x[s >= r] stay 0 while row r is summed
 #pragma unroll
-        for (int t = 0; t < CH; ++t) {
-            float acc[4] = {(t == c) ? ss.B[h][t] : 0.0f, 0.0f, 0.0f, 0.0f};   // 4 chains for ILP
+            for (int r = 0; r < 32; ++r) {
+                float acc[4] = {(r == c) ? 1.0f : 0.0f, 0.0f, 0.0f, 0.0f};   // 4 chains for ILP
 #pragma unroll
-            for (int s4 = 0; s4 < (t + 3) / 4; ++s4) {      // L[t][s] = 0 for s >= t
-                const float4 l4 = *reinterpret_cast<const float4 *>(Lb + lb_at(t, 4 * s4));
-                acc[0] = fmaf(-l4.x, x[4 * s4], acc[0]);
-                acc[1] = fmaf(-l4.y, x[4 * s4 + 1], acc[1]);
-                acc[2] = fmaf(-l4.z, x[4 * s4 + 2], acc[2]);
-                acc[3] = fmaf(-l4.w, x[4 * s4 + 3], acc[3]);
+                for (int s4 = 0; s4 < (r + 3) / 4; ++s4) {      // A[r][s] = 0 for s >= r
+                    const float4 l4 = *reinterpret_cast<const float4 *>(Lb + lb_at(32 * b + r, 32 * b + 4 * s4));
+                    acc[0] = fmaf(-l4.x, x[4 * s4], acc[0]);
+                    acc[1] = fmaf(-l4.y, x[4 * s4 + 1], acc[1]);
+                    acc[2] = fmaf(-l4.z, x[4 * s4 + 2], acc[2]);
+                    acc[3] = fmaf(-l4.w, x[4 * s4 + 3], acc[3]);
+                }
+                x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
-            x[t] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-        }
-        unsigned char *Ts = sm + (h ? S1_TS1 : S1_TS0);
+            const float bc = ss.B[h][32 * b + c];
+            unsigned char *Ts = sm + (h ? S1_TS1 : S1_TS0);
+            float *plain = b ? x1_of(h) : t00_of(h);
 #pragma unroll
-        for (int t = 0; t < CH; ++t) *reinterpret_cast<float *>(Ts + km<4>(t, c, CH)) = tc::tf32_rn(x[t]);
-    } else {
-        for (int it = warp - 4; it < 2 * 16 * 4; it += 4) {         // lanes cover whole core matrices
-            const int h = it >> 6, i = ((it >> 2) & 15) * 8 + (lane & 7), s4 = (it & 3) * 4 + (lane >> 3);
+            for (int r = 0; r < 32; ++r) {
+                *reinterpret_cast<float *>(Ts + km<4>(32 * b + r, 32 * b + c, CH)) = tc::tf32_rn(x[r] * bc);
+                plain[r * (b ? XS : 32) + c] = b ? x[r] : x[r] * bc;
+            }
+        } else {
+            for (int it = warp - 4; it < 16 * 4; it += 4) {            // (Gamma K)^T of head 0 into QS
+                const int i = ((it >> 2) & 15) * 8 + (lane & 7), s4 = (it & 3) * 4 + (lane >> 3);
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int sx = s4 * 4 + e;
+                    v[e] = ss.gam[0][sx] * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(sx, i, DK));
+                }
+                *reinterpret_cast<float4 *>(sm + S1_QS + km<4>(i, s4 * 4, CH)) =
+                    tc::tf32_rn(make_float4(v[0], v[1], v[2], v[3]));
+            }
+        }
+        __syncthreads();
+        // level 2: thread (head, row pair, column quad) owns rows r0, r0+1 and columns c0..c0+3
+        const int h = tid >> 7, r0 = 2 * (((tid >> 5) & 3) * 4 + (lane >> 3)), c0 = 4 * (lane & 7);
+        {                                                     // M = A_10 T_00
+            const float *Lb = reinterpret_cast<const float *>(sm + (h ? S1_LB1 : S1_LB0));
+            const float *T00 = t00_of(h);
+            float acc[2][4] = {};
+#pragma unroll
+            for (int k = 0; k < 32; k += 4) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(Lb + lb_at(32 + r0, k));
+                const float4 a1 = *reinterpret_cast<const float4 *>(Lb + lb_at(33 + r0, k));
+                const float ar[2][4] = {{a0.x, a0.y, a0.z, a0.w}, {a1.x, a1.y, a1.z, a1.w}};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(T00 + (k + e) * 32 + c0);
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        acc[rr][0] = fmaf(ar[rr][e], t4.x, acc[rr][0]);
+                        acc[rr][1] = fmaf(ar[rr][e], t4.y, acc[rr][1]);
+                        acc[rr][2] = fmaf(ar[rr][e], t4.z, acc[rr][2]);
+                        acc[rr][3] = fmaf(ar[rr][e], t4.w, acc[rr][3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+                *reinterpret_cast<float4 *>(m_of(h) + (r0 + rr) * 32 + c0) =
+                    make_float4(acc[rr][0], acc[rr][1], acc[rr][2], acc[rr][3]);
+        }
+        __syncthreads();
+        {                                                     // T_10 = -X_1 M; T_01 = 0
+            const float *X1 = x1_of(h);
+            const float *M = m_of(h);
+            float acc[2][4] = {};
+#pragma unroll
+            for (int k = 0; k < 32; k += 4) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(X1 + r0 * XS + k);
+                const float4 a1 = *reinterpret_cast<const float4 *>(X1 + (r0 + 1) * XS + k);
+                const float ar[2][4] = {{a0.x, a0.y, a0.z, a0.w}, {a1.x, a1.y, a1.z, a1.w}};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(M + (k + e) * 32 + c0);
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        acc[rr][0] = fmaf(ar[rr][e], m4.x, acc[rr][0]);
+                        acc[rr][1] = fmaf(ar[rr][e], m4.y, acc[rr][1]);
+                        acc[rr][2] = fmaf(ar[rr][e], m4.z, acc[rr][2]);
+                        acc[rr][3] = fmaf(ar[rr][e], m4.w, acc[rr][3]);
+                    }
+                }
+            }
+            unsigned char *Ts = sm + (h ? S1_TS1 : S1_TS0);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                *reinterpret_cast<float4 *>(Ts + km<4>(32 + r0 + rr, c0, CH)) =
+                    tc::tf32_rn(make_float4(-acc[rr][0], -acc[rr][1], -acc[rr][2], -acc[rr][3]));
+                *reinterpret_cast<float4 *>(Ts + km<4>(r0 + rr, 32 + c0, CH)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        __syncthreads();
+        for (int it = warp; it < 16 * 4; it += P1_THREADS / 32) {      // (Gamma K)^T of head 1
+            const int i = ((it >> 2) & 15) * 8 + (lane & 7), s4 = (it & 3) * 4 + (lane >> 3);
             float v[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int s = s4 * 4 + e;
-                v[e] = ss.gam[h][s] * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(s, i, DK));
+                const int sx = s4 * 4 + e;
+                v[e] = ss.gam[1][sx] * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(sx, i, DK));
             }
-            *reinterpret_cast<float4 *>(sm + (h ? S1_GK1 : S1_QS) + km<4>(i, s4 * 4, CH)) =
+            *reinterpret_cast<float4 *>(sm + S1_GK1 + km<4>(i, s4 * 4, CH)) =
                 tc::tf32_rn(make_float4(v[0], v[1], v[2], v[3]));
         }
     }
