@@ -597,33 +597,55 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
 // the token or key index as the MMA M dimension and the CTA's 32 columns as N:
 //   (1) Vn^(t,j) = W[t][i] S[i][j]          bf16, M=64 (t), N=32, K=128
 //       Y(t,j)   = Q~[t][i] S[i][j]         bf16, M=64,     N=32, K=128
-//   (2) Y(t,j)  += P[t][s] Vnew[s][j]       tf32, M=64,     N=32, K=64
-//       S(i,j)  += K~^T[i][t] Vnew[t][j]    tf32, M=128 (i), N=32, K=64
+//   (2) S(i,j)  += K~^T[i][t] Vnew[t][j]    tf32, M=128 (i), N=32, K=64
+//       Y(t,j)  += P[t][s] Vnew[s][j]       tf32, M=64,     N=32, K=64 (issued
+//                                            with the next chunk's products)
 // The state block S(i,j) lives in tensor memory (fp32, lane = i), plus a bf16
-// copy S^T[j][i] in shared memory as the B operand of (1). Vnew = U - W S goes to
-// shared memory as Vnew^T[j][t] (tf32), the B operand of (2). y (scale applied)
-// goes to a [T][4096] fp32 buffer, and a separate kernel applies the gated
-// RMSNorm across all 128 columns of each head.
-constexpr int P2_THREADS = 256;
+// copy in shared memory as the B operand of (1). Vnew = U - W S goes to shared
+// memory as Vnew^T[j][t] (tf32), the B operand of (2). y (scale applied) goes to
+// a [T][4096] fp32 buffer, and a separate kernel applies the gated RMSNorm
+// across all 128 columns of each head.
+//
+// Issue. A tcgen05.mma instruction holds its issuing thread for a fixed time of
+// some 60 cycles however small the product, while the tensor core accepts such
+// instructions from several warps at once; small products then run at the rate
+// shared memory feeds their operands. Only Vn^ = W S and the state update are on
+// the chunk-to-chunk chain, so each is split along K between two issuer warps
+// with separate accumulators (the epilogues add the halves), and each Y product
+// is queued right behind a chain product, so that it runs while the epilogue of
+// that product does: issuer k's K half of Y = Q~ S behind its half of Vn^, and
+// its half of Y += P Vnew behind its half of the state update. Eight more warps
+// run the tensor-memory epilogues. The issuers take no part in CTA-wide
+// barriers (they would hold them up while an issue blocks): the epilogue warps
+// hand over through two mbarriers that all 256 epilogue threads arrive on,
+// "Vnew written" and "next state block written".
+constexpr int P2_EPI_WARPS = 8;
+constexpr int P2_THREADS = 32 * (P2_EPI_WARPS + 2);
 constexpr int JB = 32;                 // value columns per CTA
 constexpr int NJB = DV / JB;           // CTAs per V-head
 constexpr uint32_t S2_SS = 0;          // S block bf16, MN-major (N = 32 j, K = 128 i)    8 KiB
-constexpr uint32_t S2_VN = 8192;       // Vnew^T block tf32 [32 j][64 t] Kd64             8 KiB
-constexpr uint32_t S2_WQ0 = 16384;     // W | Q~ (bf16 [t][i] Kd128, 16 KiB each), stage 0
-constexpr uint32_t S2_WQ1 = 49152;     //                                          stage 1
-constexpr uint32_t S2_PK0 = 81920;     // P (tf32 [t][s] Kd64) | K~^T (tf32 [i][t] Kd64), stage 0
-constexpr uint32_t S2_PK1 = 131072;    //                                                  stage 1
-constexpr uint32_t S2_SMALL = 180224;
+constexpr uint32_t S2_VN = 8192;       // Vnew^T block tf32 [32 j][64 t] Kd64, chunk c at + 8 KiB (c % 2)
+constexpr uint32_t S2_WQ0 = 24576;     // W | Q~ (bf16 [t][i] Kd128, 16 KiB each), stage 0
+constexpr uint32_t S2_WQ1 = 57344;     //                                          stage 1
+constexpr uint32_t S2_PK0 = 90112;     // P (tf32 [t][s] Kd64) | K~^T (tf32 [i][t] Kd64), stage 0
+constexpr uint32_t S2_PK1 = 139264;    //                                                  stage 1
+constexpr uint32_t S2_SMALL = 188416;
 struct P2Small {
-    uint64_t bar_wq[2], bar_pk[2], bar_m1, bar_m2;
+    uint64_t bar_wq[2], bar_pk[2];     // operand loads, per stage
+    uint64_t bar_m1[2], bar_m2[2];     // chain products, per issuer
+    uint64_t bar_y[2][2];              // all of a chunk's products, per Y buffer and issuer
+    uint64_t bar_vn, bar_s;            // epilogue -> issuers: Vnew written; next state block written
     uint32_t tmem;
     int abort;
 };
 constexpr size_t P2_SMEM = S2_SMALL + sizeof(P2Small) + 128;
-// tensor-memory columns: M=64 accumulators use lanes 0-15 of each lane quarter
-constexpr uint32_t T2_VN = 0, T2_Y = 32, T2_S = 64, T2_COLS = 128;
+// tensor-memory columns (M=64 accumulators use lanes 0-15 of each lane quarter):
+// issuer k's half of Vn^ at T2_VN + 32k; the state block S and issuer 1's half
+// of its update dS; issuer k's half of Y at T2_Y + 64 (c % 2) + 32k, two
+// buffers so that chunk c's y drains while chunk c + 1's products run
+constexpr uint32_t T2_VN = 0, T2_S = 64, T2_DS = 96, T2_Y = 128, T2_COLS = 256;
 
-// Caller: thread 0. Loads chunk c's W | Q~ or P | K~^T into stage c % 2.
+// Caller: one thread. Loads chunk c's W | Q~ or P | K~^T into stage c % 2.
 template <bool WQ>
 __device__ __forceinline__ void carry_issue(const unsigned char *blob, uint32_t sb, P2Small &ss, int c)
 {
@@ -659,7 +681,9 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
     P2Small &ss = *reinterpret_cast<P2Small *>(sm + S2_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x, vh = blockIdx.y, jb = blockIdx.z;
-    const int q = warp & 3, hf = warp >> 2;            // lane quarter; column half (16 of the 32)
+    const bool issuer = warp >= P2_EPI_WARPS;          // warps 8, 9: lane 0 issues MMAs
+    const int ik = warp - P2_EPI_WARPS;                // issuer index (issuer warps only)
+    const int q = warp & 3, hf = (warp >> 2) & 1;      // lane quarter; column half (16 of the 32)
     const int i = 32 * q + lane;                       // key row i (M=128 accumulator lane)
     const int t = 16 * q + lane;                       // token row t (M=64 accumulator, lanes < 16)
     const bool trow = lane < 16;
@@ -693,12 +717,16 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        for (int st = 0; st < 2; ++st) {
-            mbar_init(smem_u32(&ss.bar_wq[st]), 1);
-            mbar_init(smem_u32(&ss.bar_pk[st]), 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(smem_u32(&ss.bar_wq[k]), 1);
+            mbar_init(smem_u32(&ss.bar_pk[k]), 1);
+            mbar_init(smem_u32(&ss.bar_m1[k]), 1);
+            mbar_init(smem_u32(&ss.bar_m2[k]), 1);
+            mbar_init(smem_u32(&ss.bar_y[0][k]), 1);
+            mbar_init(smem_u32(&ss.bar_y[1][k]), 1);
         }
-        mbar_init(smem_u32(&ss.bar_m1), 1);
-        mbar_init(smem_u32(&ss.bar_m2), 1);
+        mbar_init(smem_u32(&ss.bar_vn), 32 * P2_EPI_WARPS);
+        mbar_init(smem_u32(&ss.bar_s), 32 * P2_EPI_WARPS);
         ss.abort = 0;
         fence_mbar_init();
         for (int c = 0; c < 2 && c < nc; ++c) {        // both stages in flight from the start
@@ -707,15 +735,18 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
         }
     }
     float4 u_cur[4], u_nxt[4];
-    load_u(0, u_cur);
-    float gam_c1 = gamma_of(1);                        // gamma_n of the next chunk
+    float gam_c1 = 0.0f;                               // gamma_n of the next chunk
+    if (!issuer) {
+        load_u(0, u_cur);
+        gam_c1 = gamma_of(1);
+    }
     tc::fence_before_sync();
     __syncthreads();
     const uint32_t tm = ss.tmem;
     tc::fence_after_sync();
 
-    // initial state block: bf16 copy S^T[j][i] in shared memory, gamma_n(0) * S in TMEM
-    {
+    // initial state block: bf16 copy in shared memory, gamma_n(0) * S in TMEM
+    if (!issuer) {
         const float gam0 = gamma_of(0);
         float v[16];
 #pragma unroll
@@ -731,93 +762,135 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
     __syncthreads();
 
     const float scale = rsqrtf((float)DK);
-    for (int c = 0; c < nc; ++c) {
-        const int st = c & 1;
-        const uint32_t spar = (uint32_t)((c >> 1) & 1);   // phase of this stage's load barriers
-        const uint32_t par = (uint32_t)(c & 1);           // phase of the per-chunk MMA barriers
-        const int nvc = max(0, min(CH, seqL - CH * c));
-        // (1) Vn^ = W S and Y = Q~ S (bf16, M=64, N=32, K=128)
-        if (tid == 0) {
-            tc::fence_after_sync();
-            if (!mbar_wait_bounded(smem_u32(&ss.bar_wq[st]), spar)) ss.abort = 1;
-            const uint32_t wq = sb + (st ? S2_WQ1 : S2_WQ0);
-            const uint32_t id = tc::instr_desc(tc::FMT_BF16, CH, JB) | (1u << 16);   // B (the state) MN-major
-            const uint64_t bs = tc::smem_desc(sb + S2_SS, 128u, (uint32_t)DK * 16u);
-            tc::mma_steps<false>(tm + T2_VN, tc::kmajor_desc<2>(wq, 0, DK), bs, DK / 16, id, false);
-            tc::mma_steps<false>(tm + T2_Y, tc::kmajor_desc<2>(wq + 16384, 0, DK), bs, DK / 16, id, false);
-            tc::mma_commit(smem_u32(&ss.bar_m1));
-        }
-        if (c + 1 < nc) load_u(c + 1, u_nxt);          // latency hides behind this chunk's chain
-        const float gam_c2 = gamma_of(c + 2);
-        if (!mbar_wait_bounded(smem_u32(&ss.bar_m1), par)) ss.abort = 1;
+    // y of chunk cy (scale applied), token row t -> [T][4096] buffer, once both
+    // issuers' products of that chunk have completed. Each Y buffer has its own
+    // barriers, which complete every second chunk.
+    auto drain_y = [&](int cy) {
+        const uint32_t ph = (uint32_t)((cy >> 1) & 1);
+        if (!mbar_wait_bounded(smem_u32(&ss.bar_y[cy & 1][0]), ph) || !mbar_wait_bounded(smem_u32(&ss.bar_y[cy & 1][1]), ph))
+            ss.abort = 1;
         tc::fence_after_sync();
-        // Vnew = U - W S for token row t, columns j0..j0+16 -> Vnew^T tf32 tile
-        {
-            float d[16];
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_VN + 16 * hf), d);
-            tc::wait_ld();
-            if (trow) {
-                const float *u = reinterpret_cast<const float *>(u_cur);
+        float y[16], y1[16];
+        const uint32_t yc = T2_Y + 64 * (cy & 1) + 16 * hf;
+        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, yc), y);
+        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, yc + 32), y1);
+        tc::wait_ld();
+        const int nvy = max(0, min(CH, seqL - CH * cy));
+        if (trow && t < nvy && !ss.abort) {
+            float4 *dst = reinterpret_cast<float4 *>(a.ybuf + (size_t)(seq0 + CH * cy + t) * DI + (size_t)vh * DV + j0);
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    *reinterpret_cast<float *>(sm + S2_VN + km<4>(16 * hf + e, t, CH)) = tc::tf32_rn(u[e] - d[e]);
+            for (int e = 0; e < 4; ++e)
+                dst[e] = make_float4((y[4 * e] + y1[4 * e]) * scale, (y[4 * e + 1] + y1[4 * e + 1]) * scale,
+                                     (y[4 * e + 2] + y1[4 * e + 2]) * scale, (y[4 * e + 3] + y1[4 * e + 3]) * scale);
+        }
+    };
+    const uint32_t id1 = tc::instr_desc(tc::FMT_BF16, CH, JB) | (1u << 16);   // B (the state) MN-major
+    const uint32_t id2s = tc::instr_desc(tc::FMT_TF32, 128, JB), id2y = tc::instr_desc(tc::FMT_TF32, CH, JB);
+    const volatile int &aborted = ss.abort;
+    if (issuer) {
+        if (lane == 0) {
+            for (int c = 0; c < nc; ++c) {
+                const int st = c & 1;
+                const uint32_t spar = (uint32_t)((c >> 1) & 1);   // phase of this stage's load barriers
+                const uint32_t wq = sb + (st ? S2_WQ1 : S2_WQ0), pk = sb + (st ? S2_PK1 : S2_PK0);
+                const uint32_t vnb = sb + S2_VN + 8192u * st;     // this chunk's Vnew^T buffer
+                const uint32_t ycol = T2_Y + 64 * st + 32 * ik;
+                // (1) K half i in [64k, 64k+64) of Vn^ = W S, committed alone, then
+                //     the same half of Y = Q~ S. Chunk 0's state block was written
+                //     before the loop; later ones are announced on bar_s.
+                if (c > 0 && !mbar_wait_bounded(smem_u32(&ss.bar_s), (uint32_t)((c - 1) & 1))) ss.abort = 1;
+                if (!mbar_wait_bounded(smem_u32(&ss.bar_wq[st]), spar)) ss.abort = 1;
+                if (aborted) break;
+                tc::fence_after_sync();
+                const uint64_t bs = tc::smem_desc(sb + S2_SS + 1024u * ik, 128u, (uint32_t)DK * 16u);
+                tc::mma_steps<false>(tm + T2_VN + 32 * ik, tc::kmajor_desc<2>(wq, 64 * ik, DK), bs, 4, id1, false);
+                tc::mma_commit(smem_u32(&ss.bar_m1[ik]));
+                tc::mma_steps<false>(tm + ycol, tc::kmajor_desc<2>(wq + 16384, 64 * ik, DK), bs, 4, id1, false);
+                // (2) K half t in [32k, 32k+32) of the state update, into S (k = 0)
+                //     or dS (k = 1), committed alone, then the same half of Y += P Vnew
+                if (!mbar_wait_bounded(smem_u32(&ss.bar_vn), (uint32_t)(c & 1))) ss.abort = 1;
+                if (!mbar_wait_bounded(smem_u32(&ss.bar_pk[st]), spar)) ss.abort = 1;
+                if (aborted) break;
+                tc::fence_after_sync();
+                const uint64_t vn = tc::kmajor_desc<4>(vnb, 32 * ik, CH);
+                tc::mma_steps<true>(tm + (ik ? T2_DS : T2_S), tc::kmajor_desc<4>(pk + 16384, 32 * ik, CH), vn, 4, id2s,
+                                    ik == 0);
+                tc::mma_commit(smem_u32(&ss.bar_m2[ik]));
+                tc::mma_steps<true>(tm + ycol, tc::kmajor_desc<4>(pk, 32 * ik, CH), vn, 4, id2y, true);
+                tc::mma_commit(smem_u32(&ss.bar_y[st][ik]));
             }
         }
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (ss.abort) break;
-        // (2) Y += P Vnew and S += K~^T Vnew (tf32)
-        if (tid == 0) {
-            tc::fence_after_sync();
-            if (c + 2 < nc) carry_issue<true>(blob_of(c + 2), sb, ss, c + 2);   // stage free: MMA (1) is done
-            if (!mbar_wait_bounded(smem_u32(&ss.bar_pk[st]), spar)) ss.abort = 1;
-            const uint32_t pk = sb + (st ? S2_PK1 : S2_PK0);
-            const uint64_t vn = tc::kmajor_desc<4>(sb + S2_VN, 0, CH);
-            tc::mma_steps<true>(tm + T2_Y, tc::kmajor_desc<4>(pk, 0, CH), vn, CH / 8, tc::instr_desc(tc::FMT_TF32, CH, JB),
-                                true);
-            tc::mma_steps<true>(tm + T2_S, tc::kmajor_desc<4>(pk + 16384, 0, CH), vn, CH / 8,
-                                tc::instr_desc(tc::FMT_TF32, 128, JB), true);
-            tc::mma_commit(smem_u32(&ss.bar_m2));
-        }
-        if (!mbar_wait_bounded(smem_u32(&ss.bar_m2), par)) ss.abort = 1;
-        tc::fence_after_sync();
-        if (tid == 0 && c + 2 < nc) carry_issue<false>(blob_of(c + 2), sb, ss, c + 2);
-        // state block: bf16 copy for the next chunk and decay by its gamma_n, or the final state out
-        {
-            float v[16];
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), v);
-            tc::wait_ld();
-            if (c + 1 < nc) {
-                store_s_bf16(sm, i, hf, v);
+    } else {
+        float sdec[16];                                // state block to decay into TMEM before this chunk's update
+        float gam_dec = 0.0f;                          // its decay: gamma_n of the chunk about to update it
+        for (int c = 0; c < nc; ++c) {
+            const int st = c & 1;
+            const uint32_t par = (uint32_t)(c & 1);   // phase of the per-chunk MMA barriers
+            if (c > 0) {                               // previous state block decays for this chunk's update
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] *= gam_c1;
-                tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), v);
+                for (int e = 0; e < 16; ++e) sdec[e] *= gam_dec;
+                tc::tmem_st16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), sdec);
+            }
+            if (c + 1 < nc) load_u(c + 1, u_nxt);      // latency hides behind this chunk's chain
+            const float gam_c2 = gamma_of(c + 2);
+            if (!mbar_wait_bounded(smem_u32(&ss.bar_m1[0]), par) || !mbar_wait_bounded(smem_u32(&ss.bar_m1[1]), par))
+                ss.abort = 1;
+            if (aborted) break;
+            tc::fence_after_sync();
+            // Vnew = U - W S for token row t, columns j0..j0+16 -> Vnew^T tf32 tile
+            {
+                float d[16], d1[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_VN + 16 * hf), d);
+                tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_VN + 32 + 16 * hf), d1);
+                tc::wait_ld();
+                if (trow) {
+                    const float *u = reinterpret_cast<const float *>(u_cur);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        *reinterpret_cast<float *>(sm + S2_VN + 8192u * st + km<4>(16 * hf + e, t, CH)) =
+                            tc::tf32_rn(u[e] - (d[e] + d1[e]));
+                }
+            }
+            tc::wait_st();
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(smem_u32(&ss.bar_vn));
+            if (c > 0) {                               // y of the previous chunk, while the state update runs
+                drain_y(c - 1);
+                // that chunk's P | K~^T stage was last read by its Y += P Vnew
+                if (tid == 0 && c + 1 < nc) carry_issue<false>(blob_of(c + 1), sb, ss, c + 1);
+            }
+            if (!mbar_wait_bounded(smem_u32(&ss.bar_m2[0]), par) || !mbar_wait_bounded(smem_u32(&ss.bar_m2[1]), par))
+                ss.abort = 1;
+            if (aborted) break;
+            tc::fence_after_sync();
+            // W | Q~ of this stage were last read by Y = Q~ S, issued before each state update
+            if (tid == 0 && c + 2 < nc) carry_issue<true>(blob_of(c + 2), sb, ss, c + 2);
+            // state block S + dS: bf16 copy for the next chunk (its decay waits
+            // for the next chunk's Vnew), or the final state out
+            {
+                float ds[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_S + 16 * hf), sdec);
+                tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_DS + 16 * hf), ds);
+                tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) sdec[e] += ds[e];
+            }
+            if (c + 1 < nc) {
+                store_s_bf16(sm, i, hf, sdec);
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(smem_u32(&ss.bar_s));
             } else if (a.S_out) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) a.S_out[sbase_g + (size_t)(j0 + e) * DK + i] = v[e];
+                for (int e = 0; e < 16; ++e) a.S_out[sbase_g + (size_t)(j0 + e) * DK + i] = sdec[e];
             }
-        }
-        // y (scale applied) of token row t -> [T][4096] buffer
-        {
-            float y[16];
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T2_Y + 16 * hf), y);
-            tc::wait_ld();
-            if (trow && t < nvc) {
-                float4 *dst = reinterpret_cast<float4 *>(a.ybuf + (size_t)(seq0 + CH * c + t) * DI + (size_t)vh * DV + j0);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_float4(y[4 * e] * scale, y[4 * e + 1] * scale, y[4 * e + 2] * scale, y[4 * e + 3] * scale);
-            }
+            for (int e = 0; e < 4; ++e) u_cur[e] = u_nxt[e];
+            gam_dec = gam_c1;
+            gam_c1 = gam_c2;
         }
-        tc::wait_st();
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (ss.abort) break;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) u_cur[e] = u_nxt[e];
-        gam_c1 = gam_c2;
+        if (!aborted) drain_y(nc - 1);
     }
     tc::fence_before_sync();
     __syncthreads();
