@@ -15,15 +15,18 @@
 // needs no cross-CTA ordering.
 //
 // The states stream through a ring of six 32 KiB shared-memory slots, each
-// holding 64 rows of one state. Thread 0 fills them with TMA bulk copies
-// (cp.async.bulk), which complete on one mbarrier per slot, and keeps five
-// slots in flight ahead of the one being computed. Warp w computes 4 rows j of
-// each slot (rows of S^T: value index j, 128 contiguous keys i). Lane l holds
-// keys [4l, 4l+4). pred_j, delta_j and y_j depend on row j alone, so a row
-// needs only warp-shuffle dot products. The updated row goes straight back to
-// global memory with a streaming store. An item's prologue inputs (conv_state,
-// qkv, gates, z) are loaded one item ahead, so their latency hides behind the
-// previous item's sweep.
+// holding 64 rows of one state. A producer warp fills them with TMA bulk copies
+// (cp.async.bulk), which complete on a "full" mbarrier per slot; it refills a
+// slot as soon as all 16 compute warps have arrived on the slot's "empty"
+// mbarrier, so the ring stays as full as the slots allow and no CTA-wide
+// barrier sits between slots. Warp w computes 4 rows j of each slot (rows of
+// S^T: value index j, 128 contiguous keys i). Lane l holds keys [4l, 4l+4).
+// pred_j, delta_j and y_j depend on row j alone, so a row needs only
+// warp-shuffle dot products. The updated row goes straight back to global
+// memory with a streaming store. The compute warps synchronise among
+// themselves (a named barrier) only in an item's prologue and its output norm.
+// An item's prologue inputs (conv_state, qkv, gates, z) are loaded one item
+// ahead, so their latency hides behind the previous item's sweep.
 #include "gdn_async.cuh"
 #include "gdn_common.cuh"
 
@@ -64,8 +67,9 @@ struct DecodeArgs {
     int n_items;   // B * 16
 };
 
-constexpr int DEC_THREADS = 512;
-constexpr int DEC_WARPS = DEC_THREADS / 32;
+constexpr int DEC_WARPS = 16;                              // compute warps
+constexpr int DEC_COMPUTE = 32 * DEC_WARPS;
+constexpr int DEC_THREADS = DEC_COMPUTE + 32;              // + the producer warp
 constexpr int DEC_SLOT_ROWS = 64;                          // rows j of S^T per staging slot
 constexpr int DEC_UNITS = DV / DEC_SLOT_ROWS;              // slots per state (2)
 constexpr int DEC_ROWS_PER_WARP = DEC_SLOT_ROWS / DEC_WARPS;   // 4
@@ -80,6 +84,7 @@ struct DecodeSmem {
     alignas(16) float v[2][DV];
     alignas(16) float y[2][DV];
     alignas(8) uint64_t full[DEC_SLOTS];
+    uint64_t empty[DEC_SLOTS];
     float red[32];
     float gate[2][2];
     int pending[DEC_SLOTS];   // unit number whose load is outstanding in each slot, or -1
@@ -89,11 +94,11 @@ constexpr size_t DEC_SMEM = sizeof(DecodeSmem) + 128;   // + alignment slack
 
 // Issues the TMA load of this CTA's unit number `u` into slot u % DEC_SLOTS.
 // Units walk item by item, V-head by V-head, then slot-sized row blocks:
-// u = (2 * m + h) * DEC_UNITS + part. Caller: thread 0 only.
+// u = (2 * m + h) * DEC_UNITS + part. Caller: the producer thread; the unit's
+// item exists.
 __device__ __forceinline__ void decode_issue_load(DecodeSmem &sm, const DecodeArgs &a, int u)
 {
     const int item = blockIdx.x + (u / (2 * DEC_UNITS)) * gridDim.x;
-    if (item >= a.n_items) return;
     const int h = (u / DEC_UNITS) & 1, part = u % DEC_UNITS;
     const int b = item / HK, kh = item % HK, vh = kh + HK * h;
     const char *src = reinterpret_cast<const char *>(a.ssm_state + ((size_t)b * HV + vh) * (DV * DK)) +
@@ -153,25 +158,54 @@ __device__ __forceinline__ PrologueIn<TA> prologue_load(const DecodeArgs &a, int
     return p;
 }
 
+// Barrier among the 16 compute warps only (the producer warp never joins it).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(DEC_COMPUTE) : "memory"); }
+
 template <typename TA, typename TO>
 __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const DecodeArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
     DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const volatile int &aborted = sm.abort;
 
     if (tid == 0) {
         for (int i = 0; i < DEC_SLOTS; ++i) {
             mbar_init(smem_u32(&sm.full[i]), 1);
+            mbar_init(smem_u32(&sm.empty[i]), DEC_WARPS);
             sm.pending[i] = -1;
         }
         sm.abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0)
-        for (int s = 0; s < DEC_SLOTS; ++s) decode_issue_load(sm, a, s);
 
+    if (warp == DEC_WARPS) {
+        // ---- producer: unit u goes into slot u % DEC_SLOTS once the compute
+        //      warps have released that slot's previous unit, u - DEC_SLOTS
+        if (lane == 0) {
+            for (int u = 0;; ++u) {
+                if (blockIdx.x + (u / (2 * DEC_UNITS)) * (int)gridDim.x >= a.n_items) break;
+                const int slot = u % DEC_SLOTS;
+                if (u >= DEC_SLOTS) {
+                    if (!mbar_wait_bounded(smem_u32(&sm.empty[slot]), (uint32_t)((u / DEC_SLOTS - 1) & 1))) sm.abort = 1;
+                    sm.pending[slot] = -1;     // its previous load completed before the compute warps released it
+                }
+                if (aborted) break;
+                fence_proxy_async_smem();
+                decode_issue_load(sm, a, u);
+            }
+            // after an abort, let the copies still in flight land before the
+            // CTA's shared memory is released
+            if (aborted)
+                for (int i = 0; i < DEC_SLOTS; ++i)
+                    if (sm.pending[i] >= 0)
+                        mbar_wait_bounded(smem_u32(&sm.full[i]), (uint32_t)((sm.pending[i] / DEC_SLOTS) & 1));
+        }
+        return;
+    }
+
+    // ---- compute warps
     const float scale = rsqrtf((float)DK);
     PrologueIn<TA> pin;
     if ((int)blockIdx.x < a.n_items) pin = prologue_load<TA>(a, blockIdx.x, tid);
@@ -200,26 +234,30 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
                 sm.gate[tid][0] = ga;
                 sm.gate[tid][1] = gb;
             }
-            __syncthreads();
+            compute_sync();
             if (tid < 128) sm.q[tid] = xh * rsqrtf(sm.red[0] + sm.red[1] + sm.red[2] + sm.red[3] + a.l2_eps);
             else if (tid < 256) sm.k[tid - 128] = xh * rsqrtf(sm.red[4] + sm.red[5] + sm.red[6] + sm.red[7] + a.l2_eps);
             else sm.v[(tid - 256) >> 7][tid & 127] = xh;
-            __syncthreads();
+            compute_sync();
         }
         const TA zcur = pin.zc;
         // the next item's prologue inputs: their latency hides behind this item's sweep
         if (item + (int)gridDim.x < a.n_items) pin = prologue_load<TA>(a, item + gridDim.x, tid);
 
-        // ---- the two states of the item: recurrence (a)-(d) row by row
+        // ---- the two states of the item: recurrence (a)-(d) row by row. Each
+        //      warp takes its rows of a slot as soon as the slot has landed and
+        //      releases the slot when it is done with them.
         const float4 k4 = reinterpret_cast<const float4 *>(sm.k)[lane];
         const float4 q4 = reinterpret_cast<const float4 *>(sm.q)[lane];
         for (int hp = 0; hp < 2 * DEC_UNITS; ++hp) {
             const int h = hp / DEC_UNITS, part = hp % DEC_UNITS;
             const int u = 2 * DEC_UNITS * m + hp;
             const int slot = u % DEC_SLOTS;
-            if (!mbar_wait_bounded(smem_u32(&sm.full[slot]), (uint32_t)((u / DEC_SLOTS) & 1))) sm.abort = 1;
-            __syncthreads();
-            if (sm.abort) break;
+            if (aborted) continue;                       // skip the work, keep the barriers in step
+            if (!mbar_wait_bounded(smem_u32(&sm.full[slot]), (uint32_t)((u / DEC_SLOTS) & 1))) {
+                sm.abort = 1;
+                continue;
+            }
             const int vh = kh + HK * h;
             float *Sg = a.ssm_state + (b * HV + vh) * (size_t)(DV * DK);
             const float dec = sm.gate[h][0], beta = sm.gate[h][1];
@@ -237,14 +275,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
                 __stcs(reinterpret_cast<float4 *>(Sg + (size_t)j * DK) + lane, st);
                 if (lane == 0) sm.y[h][j] = yq * scale;
             }
-            __syncthreads();                     // every warp is done reading this slot
-            if (tid == 0) {
-                sm.pending[slot] = -1;
-                fence_proxy_async_smem();
-                decode_issue_load(sm, a, u + DEC_SLOTS);
-            }
+            __syncwarp();                                // this warp's reads of the slot are done
+            if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
         }
-        if (sm.abort) break;
+        compute_sync();                                  // all rows of y are in, and the abort flag agrees
+        if (aborted) break;
 
         // ---- gated RMSNorm of both heads, times silu(z) ("Output path")
         if (tid < 256) {
@@ -253,7 +288,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
             const float ss = warp_sum(y * y);
             if (lane == 0) sm.red[16 + warp] = ss;
         }
-        __syncthreads();
+        compute_sync();
         if (tid < 256) {
             const int h = tid >> 7, j = tid & 127;
             const float *rr4 = sm.red + 16 + 4 * h;
@@ -264,12 +299,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
         }
         // the next prologue writes q/k/v/red[0..7]/gate, none of which the lines above read
     }
-    if (sm.abort && tid == 0) {
-        atomicExch(&g_decode_error, (unsigned int)GDN_ERR_TIMEOUT);
-        // let the copies still in flight land before the CTA's shared memory is released
-        for (int i = 0; i < DEC_SLOTS; ++i)
-            if (sm.pending[i] >= 0) mbar_wait_bounded(smem_u32(&sm.full[i]), (uint32_t)((sm.pending[i] / DEC_SLOTS) & 1));
-    }
+    if (aborted && tid == 0) atomicExch(&g_decode_error, (unsigned int)GDN_ERR_TIMEOUT);
 }
 
 // ------------------------------------------------------------------ launchers
