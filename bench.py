@@ -53,7 +53,7 @@ PREFILL_FLOP_PER_TOKEN = 5_242_880
 # From the ncu capture in profiles/decode_step_kernel_B256.md: a B=128 launch
 # scaled by 2, since the traffic grows with B. Set to None whenever the kernel
 # changes without a new capture.
-DECODE_TRAFFIC_PER_LAUNCH = 2 * (278_073_600 + 214_957_568)
+DECODE_TRAFFIC_PER_LAUNCH = None
 
 
 def load_peaks():

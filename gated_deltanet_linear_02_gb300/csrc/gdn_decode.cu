@@ -20,10 +20,11 @@
 // slot as soon as all 16 compute warps have arrived on the slot's "empty"
 // mbarrier, so the ring stays as full as the slots allow and no CTA-wide
 // barrier sits between slots. Warp w computes 4 rows j of each slot (rows of
-// S^T: value index j, 128 contiguous keys i). Lane l holds keys [4l, 4l+4).
-// pred_j, delta_j and y_j depend on row j alone, so a row needs only
-// warp-shuffle dot products. The updated row goes straight back to global
-// memory with a streaming store. The compute warps synchronise among
+// S^T: value index j, 128 contiguous keys i), all four at once: lanes 8r..8r+7
+// hold row r, lane 8r+g the keys of float4 groups g, g+8, g+16, g+24. pred_j,
+// delta_j and y_j depend on row j alone, so each dot product is a sum within
+// the row's 8 lanes (3 shuffle steps, the four rows in parallel). The updated
+// row goes straight back to global memory with streaming stores. The compute warps synchronise among
 // themselves (a named barrier) only in an item's prologue and its output norm.
 // An item's prologue inputs (conv_state, qkv, gates, z) are loaded one item
 // ahead, so their latency hides behind the previous item's sweep.
@@ -73,6 +74,7 @@ constexpr int DEC_THREADS = DEC_COMPUTE + 32;              // + the producer war
 constexpr int DEC_SLOT_ROWS = 64;                          // rows j of S^T per staging slot
 constexpr int DEC_UNITS = DV / DEC_SLOT_ROWS;              // slots per state (2)
 constexpr int DEC_ROWS_PER_WARP = DEC_SLOT_ROWS / DEC_WARPS;   // 4
+static_assert(DEC_ROWS_PER_WARP == 4, "a warp computes 4 rows of a slot at once, 8 lanes per row");
 constexpr int DEC_SLOTS = 6;
 constexpr uint32_t SLOT_BYTES = DEC_SLOT_ROWS * DK * sizeof(float);   // 32 KiB
 constexpr int DEC_COPIES = 2;                              // bulk copies per slot
@@ -247,8 +249,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
         // ---- the two states of the item: recurrence (a)-(d) row by row. Each
         //      warp takes its rows of a slot as soon as the slot has landed and
         //      releases the slot when it is done with them.
-        const float4 k4 = reinterpret_cast<const float4 *>(sm.k)[lane];
-        const float4 q4 = reinterpret_cast<const float4 *>(sm.q)[lane];
+        const int rr = lane >> 3, g = lane & 7;         // row of the warp's four; float4 group within it
+        float4 k4[4], q4[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            k4[c] = reinterpret_cast<const float4 *>(sm.k)[8 * c + g];
+            q4[c] = reinterpret_cast<const float4 *>(sm.q)[8 * c + g];
+        }
         for (int hp = 0; hp < 2 * DEC_UNITS; ++hp) {
             const int h = hp / DEC_UNITS, part = hp % DEC_UNITS;
             const int u = 2 * DEC_UNITS * m + hp;
@@ -261,20 +268,35 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
             const int vh = kh + HK * h;
             float *Sg = a.ssm_state + (b * HV + vh) * (size_t)(DV * DK);
             const float dec = sm.gate[h][0], beta = sm.gate[h][1];
-            const float4 *src = reinterpret_cast<const float4 *>(sm.slot[slot]);
+            const int jl = warp * DEC_ROWS_PER_WARP + rr;     // row within the slot
+            const int j = part * DEC_SLOT_ROWS + jl;
+            const float4 *src = reinterpret_cast<const float4 *>(sm.slot[slot]) + jl * (DK / 4) + g;
+            const float vj = sm.v[h][j];
+            float4 st[4];
 #pragma unroll
-            for (int r = 0; r < DEC_ROWS_PER_WARP; ++r) {
-                const int jl = warp * DEC_ROWS_PER_WARP + r;     // row within the slot
-                const int j = part * DEC_SLOT_ROWS + jl;
-                float4 st = src[jl * (DK / 4) + lane];
-                st.x *= dec; st.y *= dec; st.z *= dec; st.w *= dec;                                   // (a)
-                const float pred = warp_sum(st.x * k4.x + st.y * k4.y + st.z * k4.z + st.w * k4.w);    // (b)
-                const float delta = (sm.v[h][j] - pred) * beta;
-                st.x += k4.x * delta; st.y += k4.y * delta; st.z += k4.z * delta; st.w += k4.w * delta; // (c)
-                const float yq = warp_sum(st.x * q4.x + st.y * q4.y + st.z * q4.z + st.w * q4.w);      // (d)
-                __stcs(reinterpret_cast<float4 *>(Sg + (size_t)j * DK) + lane, st);
-                if (lane == 0) sm.y[h][j] = yq * scale;
+            for (int c = 0; c < 4; ++c) st[c] = src[8 * c];
+            float pa = 0.0f, pb = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                st[c].x *= dec; st[c].y *= dec; st[c].z *= dec; st[c].w *= dec;                      // (a)
+                pa = fmaf(st[c].x, k4[c].x, fmaf(st[c].y, k4[c].y, pa));
+                pb = fmaf(st[c].z, k4[c].z, fmaf(st[c].w, k4[c].w, pb));
             }
+            const float pred = group_sum<8>(pa + pb);                                                  // (b)
+            const float delta = (vj - pred) * beta;
+            float ya = 0.0f, yb = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                st[c].x = fmaf(k4[c].x, delta, st[c].x); st[c].y = fmaf(k4[c].y, delta, st[c].y);      // (c)
+                st[c].z = fmaf(k4[c].z, delta, st[c].z); st[c].w = fmaf(k4[c].w, delta, st[c].w);
+                ya = fmaf(st[c].x, q4[c].x, fmaf(st[c].y, q4[c].y, ya));
+                yb = fmaf(st[c].z, q4[c].z, fmaf(st[c].w, q4[c].w, yb));
+            }
+            const float yq = group_sum<8>(ya + yb);                                                    // (d)
+            float4 *dst = reinterpret_cast<float4 *>(Sg + (size_t)j * DK) + g;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) __stcs(dst + 8 * c, st[c]);
+            if (g == 0) sm.y[h][j] = yq * scale;
             __syncwarp();                                // this warp's reads of the slot are done
             if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
         }
