@@ -49,11 +49,11 @@ DECODE_PARAM_BYTES_PER_LAUNCH = 131_840
 # (M o Q K^T) V_new and the state update K^T V_new per V-head, with C=64.
 PREFILL_FLOP_PER_TOKEN = 5_242_880
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode launch at B=256.
-# From the ncu capture in profiles/decode_step_kernel_B256.md: a B=128 launch
-# scaled by 2, since the traffic grows with B. Set to None whenever the kernel
-# changes without a new capture.
-DECODE_TRAFFIC_PER_LAUNCH = None
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode launch at B=256
+# (one layer, cold L2), from the ncu capture in
+# profiles/decode_step_kernel_B256.md. Set to None whenever the kernel changes
+# without a new capture.
+DECODE_TRAFFIC_PER_LAUNCH = 556_014_848 + 491_503_616
 
 
 def load_peaks():
