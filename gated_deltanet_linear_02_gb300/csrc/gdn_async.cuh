@@ -37,6 +37,15 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// The dynamic shared-memory block rounded up to a 128-byte boundary. It is
+// formed as an offset into the __shared__ array itself, so the compiler still
+// knows the pointer addresses shared memory. That lets it move shared loads
+// past global stores, which may not alias them.
+__device__ __forceinline__ unsigned char *smem_aligned128(unsigned char *raw)
+{
+    return raw + ((128u - (smem_u32(raw) & 127u)) & 127u);
+}
+
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA / tensor core) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem()

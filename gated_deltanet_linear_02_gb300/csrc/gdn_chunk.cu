@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t *__r
 }
 
 // -------------------------------------------------------------------- prep
-constexpr int P1_THREADS = 256;
+constexpr int P1_THREADS = 512;
+constexpr int NW1 = P1_THREADS / 32;   // 16 warps: 4 per lane quarter of the tensor memory
 constexpr uint32_t S1_QS = 0;          // q^ tf32 [t][i] Kd128; later (Gamma K)^T of head 0 [i][s] Kd64
 constexpr uint32_t S1_KS = 32768;      // k^ tf32 [t][i] Kd128
 constexpr uint32_t S1_VT0 = 65536;     // v^T tf32 [j][s] Kd64, head 0
@@ -166,7 +167,7 @@ template <int ES> __device__ __forceinline__ uint32_t km(int r, int k, int Kd) {
 __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+    unsigned char *sm = smem_aligned128(smem_raw);
     P1Small &ss = *reinterpret_cast<P1Small *>(sm + S1_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x, kh = blockIdx.y;
@@ -253,43 +254,74 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
     //      tiles. Lanes map onto the 8 rows of a core matrix, so each 16-byte
     //      store of a warp phase fills one contiguous 128-byte core matrix.
     const unsigned char *raw = sm + S1_RAW;
-    for (int it = warp; it < 128; it += P1_THREADS / 32) {           // q, k: (tile, row octet, k-group)
-        const int tile = it >> 6, po = (it >> 3) & 7, kgh = it & 7;
-        const int p = po * 8 + (lane & 7);
-        const int d = 4 * (kgh * 4 + (lane >> 3));                    // 4 consecutive channels d..d+3
-        float x[4][4];
+    // Each pass loads the inputs of four iterations before it stores anything,
+    // so the loads of later iterations need not wait behind earlier stores.
+    for (int it0 = warp; it0 < 128; it0 += 4 * NW1) {                // q, k: (tile, row octet, k-group)
+        uint2 pr[4][4];
+        float4 w4[4][4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {                                 // positions p-3+m = rows p+m
-            const uint2 pr = *reinterpret_cast<const uint2 *>(raw + (p + m) * RAW_STRIDE + (tile * DK + d) * 2);
-            const bf16 *hv = reinterpret_cast<const bf16 *>(&pr);
+        for (int k = 0; k < 4; ++k) {
+            const int it = it0 + k * NW1, tile = it >> 6, po = (it >> 3) & 7, kgh = it & 7;
+            const int p = po * 8 + (lane & 7);
+            const int d = 4 * (kgh * 4 + (lane >> 3));                // 4 consecutive channels d..d+3
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[m][e] = to_f(hv[e]);
+            for (int m = 0; m < 4; ++m)                               // positions p-3+m = rows p+m
+                pr[k][m] = *reinterpret_cast<const uint2 *>(raw + (p + m) * RAW_STRIDE + (tile * DK + d) * 2);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w4[k][e] = reinterpret_cast<const float4 *>(sm + S1_CW + tile * 2048)[d + e];
         }
-        float o[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float4 w = reinterpret_cast<const float4 *>(sm + S1_CW + tile * 2048)[d + e];
-            const float u = w.x * x[0][e] + w.y * x[1][e] + w.z * x[2][e] + w.w * x[3][e];
-            o[e] = p < nv ? silu_fast(u) : 0.0f;
+        for (int k = 0; k < 4; ++k) {
+            const int it = it0 + k * NW1, tile = it >> 6, po = (it >> 3) & 7, kgh = it & 7;
+            const int p = po * 8 + (lane & 7);
+            const int d = 4 * (kgh * 4 + (lane >> 3));
+            float x[4][4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const bf16 *hv = reinterpret_cast<const bf16 *>(&pr[k][m]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[m][e] = to_f(hv[e]);
+            }
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 w = w4[k][e];
+                const float u = w.x * x[0][e] + w.y * x[1][e] + w.z * x[2][e] + w.w * x[3][e];
+                o[e] = p < nv ? silu_fast(u) : 0.0f;
+            }
+            *reinterpret_cast<float4 *>(sm + (tile ? S1_KS : S1_QS) + km<4>(p, d, DK)) = make_float4(o[0], o[1], o[2], o[3]);
         }
-        *reinterpret_cast<float4 *>(sm + (tile ? S1_KS : S1_QS) + km<4>(p, d, DK)) = make_float4(o[0], o[1], o[2], o[3]);
     }
-    for (int it = warp; it < 128; it += P1_THREADS / 32) {           // v^T: (head, row octet of j, token group)
-        const int hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
-        const int d = dob * 8 + (lane & 7);
-        const int p0 = 4 * (pgh * 4 + (lane >> 3));                  // tokens p0..p0+3
-        const float4 w = reinterpret_cast<const float4 *>(sm + S1_CW + (2 + hv) * 2048)[d];
-        float x[7];
+    for (int it0 = warp; it0 < 128; it0 += 4 * NW1) {                // v^T: (head, row octet of j, token group)
+        bf16 xr[4][7];
+        float4 w4[4];
 #pragma unroll
-        for (int m = 0; m < 7; ++m)                                   // positions p0-3 .. p0+3
-            x[m] = to_f(*reinterpret_cast<const bf16 *>(raw + (p0 + m) * RAW_STRIDE + ((2 + hv) * DV + d) * 2));
-        float o[4];
+        for (int k = 0; k < 4; ++k) {
+            const int it = it0 + k * NW1, hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
+            const int d = dob * 8 + (lane & 7);
+            const int p0 = 4 * (pgh * 4 + (lane >> 3));              // tokens p0..p0+3
+            w4[k] = reinterpret_cast<const float4 *>(sm + S1_CW + (2 + hv) * 2048)[d];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float u = w.x * x[e] + w.y * x[e + 1] + w.z * x[e + 2] + w.w * x[e + 3];
-            o[e] = (p0 + e) < nv ? tc::tf32_rn(silu_fast(u)) : 0.0f;
+            for (int m = 0; m < 7; ++m)                               // positions p0-3 .. p0+3
+                xr[k][m] = *reinterpret_cast<const bf16 *>(raw + (p0 + m) * RAW_STRIDE + ((2 + hv) * DV + d) * 2);
         }
-        *reinterpret_cast<float4 *>(sm + (hv ? S1_VT1 : S1_VT0) + km<4>(d, p0, CH)) = make_float4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int it = it0 + k * NW1, hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
+            const int d = dob * 8 + (lane & 7);
+            const int p0 = 4 * (pgh * 4 + (lane >> 3));
+            const float4 w = w4[k];
+            float x[7];
+#pragma unroll
+            for (int m = 0; m < 7; ++m) x[m] = to_f(xr[k][m]);
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float u = w.x * x[e] + w.y * x[e + 1] + w.z * x[e + 2] + w.w * x[e + 3];
+                o[e] = (p0 + e) < nv ? tc::tf32_rn(silu_fast(u)) : 0.0f;
+            }
+            *reinterpret_cast<float4 *>(sm + (hv ? S1_VT1 : S1_VT0) + km<4>(d, p0, CH)) = make_float4(o[0], o[1], o[2], o[3]);
+        }
     }
     __syncthreads();
 
@@ -350,31 +382,30 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
     blob[1] = a.blobs + ((size_t)g * HV + kh + HK) * BLOB_BYTES;
 
     // ---- E. P = Mask o QK^T and beta * L from the M=64 accumulators (row t in
-    //      TMEM lane 32*(t/16) + t%16), then Q~, K~^T and gamma_n.
+    //      TMEM lane 32*(t/16) + t%16), then Q~, K~^T and gamma_n. Warp w reads
+    //      columns [16 (w / 4), +16) of its lane quarter w % 4.
     {
         const int q = warp & 3, hf = warp >> 2;
-        float kk[32], qk[32];
-        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_KK + 32 * hf), *reinterpret_cast<float(*)[16]>(kk));
-        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_KK + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(kk + 16));
-        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_QK + 32 * hf), *reinterpret_cast<float(*)[16]>(qk));
-        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_QK + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(qk + 16));
+        float kk[16], qk[16];
+        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_KK + 16 * hf), kk);
+        tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_QK + 16 * hf), qk);
         tc::wait_ld();
-        // Rows live in lanes 0..15. Lanes 16..31 take over columns 16..31 of their row.
+        // Rows live in lanes 0..15. Lanes 16..31 take over columns 8..15 of their row.
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const float a1 = __shfl_sync(0xffffffffu, kk[16 + c], lane & 15);
-            const float a2 = __shfl_sync(0xffffffffu, qk[16 + c], lane & 15);
+        for (int c = 0; c < 8; ++c) {
+            const float a1 = __shfl_sync(0xffffffffu, kk[8 + c], lane & 15);
+            const float a2 = __shfl_sync(0xffffffffu, qk[8 + c], lane & 15);
             if (lane >= 16) { kk[c] = a1; qk[c] = a2; }
         }
         if (!ss.abort) {
             const int t = 16 * q + (lane & 15);
-            const int cbase = 32 * hf + 16 * (lane >> 4);     // this lane's 16 columns
+            const int cbase = 16 * hf + 8 * (lane >> 4);      // this lane's 8 columns
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const float Gt = ss.G[h][t], bt = ss.B[h][t];
                 float *Lb = reinterpret_cast<float *>(sm + (h ? S1_LB1 : S1_LB0));
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
+                for (int c4 = 0; c4 < 2; ++c4) {
                     float pv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -460,7 +491,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
                 plain[r * (b ? XS : 32) + c] = b ? x[r] : x[r] * bc;
             }
         } else {
-            for (int it = warp - 4; it < 16 * 4; it += 4) {            // (Gamma K)^T of head 0 into QS
+            for (int it = warp - 4; it < 16 * 4; it += NW1 - 4) {      // (Gamma K)^T of head 0 into QS
                 const int i = ((it >> 2) & 15) * 8 + (lane & 7), s4 = (it & 3) * 4 + (lane >> 3);
                 float v[4];
 #pragma unroll
@@ -473,63 +504,49 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
             }
         }
         __syncthreads();
-        // level 2: thread (head, row pair, column quad) owns rows r0, r0+1 and columns c0..c0+3
-        const int h = tid >> 7, r0 = 2 * (((tid >> 5) & 3) * 4 + (lane >> 3)), c0 = 4 * (lane & 7);
+        // level 2: thread (head, row, column quad) owns row r and columns c0..c0+3
+        const int h = tid >> 8, r = ((tid >> 5) & 7) * 4 + (lane >> 3), c0 = 4 * (lane & 7);
         {                                                     // M = A_10 T_00
             const float *Lb = reinterpret_cast<const float *>(sm + (h ? S1_LB1 : S1_LB0));
             const float *T00 = t00_of(h);
-            float acc[2][4] = {};
+            float acc[4] = {};
 #pragma unroll
             for (int k = 0; k < 32; k += 4) {
-                const float4 a0 = *reinterpret_cast<const float4 *>(Lb + lb_at(32 + r0, k));
-                const float4 a1 = *reinterpret_cast<const float4 *>(Lb + lb_at(33 + r0, k));
-                const float ar[2][4] = {{a0.x, a0.y, a0.z, a0.w}, {a1.x, a1.y, a1.z, a1.w}};
+                const float4 a4 = *reinterpret_cast<const float4 *>(Lb + lb_at(32 + r, k));
+                const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float4 t4 = *reinterpret_cast<const float4 *>(T00 + (k + e) * 32 + c0);
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        acc[rr][0] = fmaf(ar[rr][e], t4.x, acc[rr][0]);
-                        acc[rr][1] = fmaf(ar[rr][e], t4.y, acc[rr][1]);
-                        acc[rr][2] = fmaf(ar[rr][e], t4.z, acc[rr][2]);
-                        acc[rr][3] = fmaf(ar[rr][e], t4.w, acc[rr][3]);
-                    }
+                    acc[0] = fmaf(ar[e], t4.x, acc[0]);
+                    acc[1] = fmaf(ar[e], t4.y, acc[1]);
+                    acc[2] = fmaf(ar[e], t4.z, acc[2]);
+                    acc[3] = fmaf(ar[e], t4.w, acc[3]);
                 }
             }
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr)
-                *reinterpret_cast<float4 *>(m_of(h) + (r0 + rr) * 32 + c0) =
-                    make_float4(acc[rr][0], acc[rr][1], acc[rr][2], acc[rr][3]);
+            *reinterpret_cast<float4 *>(m_of(h) + r * 32 + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
         __syncthreads();
         {                                                     // T_10 = -X_1 M; T_01 = 0
             const float *X1 = x1_of(h);
             const float *M = m_of(h);
-            float acc[2][4] = {};
+            float acc[4] = {};
 #pragma unroll
             for (int k = 0; k < 32; k += 4) {
-                const float4 a0 = *reinterpret_cast<const float4 *>(X1 + r0 * XS + k);
-                const float4 a1 = *reinterpret_cast<const float4 *>(X1 + (r0 + 1) * XS + k);
-                const float ar[2][4] = {{a0.x, a0.y, a0.z, a0.w}, {a1.x, a1.y, a1.z, a1.w}};
+                const float4 a4 = *reinterpret_cast<const float4 *>(X1 + r * XS + k);
+                const float ar[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float4 m4 = *reinterpret_cast<const float4 *>(M + (k + e) * 32 + c0);
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        acc[rr][0] = fmaf(ar[rr][e], m4.x, acc[rr][0]);
-                        acc[rr][1] = fmaf(ar[rr][e], m4.y, acc[rr][1]);
-                        acc[rr][2] = fmaf(ar[rr][e], m4.z, acc[rr][2]);
-                        acc[rr][3] = fmaf(ar[rr][e], m4.w, acc[rr][3]);
-                    }
+                    acc[0] = fmaf(ar[e], m4.x, acc[0]);
+                    acc[1] = fmaf(ar[e], m4.y, acc[1]);
+                    acc[2] = fmaf(ar[e], m4.z, acc[2]);
+                    acc[3] = fmaf(ar[e], m4.w, acc[3]);
                 }
             }
             unsigned char *Ts = sm + (h ? S1_TS1 : S1_TS0);
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                *reinterpret_cast<float4 *>(Ts + km<4>(32 + r0 + rr, c0, CH)) =
-                    tc::tf32_rn(make_float4(-acc[rr][0], -acc[rr][1], -acc[rr][2], -acc[rr][3]));
-                *reinterpret_cast<float4 *>(Ts + km<4>(r0 + rr, 32 + c0, CH)) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            *reinterpret_cast<float4 *>(Ts + km<4>(32 + r, c0, CH)) =
+                tc::tf32_rn(make_float4(-acc[0], -acc[1], -acc[2], -acc[3]));
+            *reinterpret_cast<float4 *>(Ts + km<4>(r, 32 + c0, CH)) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncthreads();
         for (int it = warp; it < 16 * 4; it += P1_THREADS / 32) {      // (Gamma K)^T of head 1
@@ -562,22 +579,21 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
     if (!ss.abort && !mbar_wait_bounded(smem_u32(&ss.bar), 1)) ss.abort = 1;
     tc::fence_after_sync();
 
-    // ---- H. U -> blob as [t][j] fp32; W -> blob as bf16 K-major [t][i]
+    // ---- H. U -> blob as [t][j] fp32; W -> blob as bf16 K-major [t][i]. Warp w
+    //      reads token columns [16 (w / 4), +16) of its lane quarter w % 4.
     {
         const int q = warp & 3, hf = warp >> 2;
         const int j = 32 * q + lane;
         for (int h = 0; h < 2; ++h) {
-            float u[32], wv[32];
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_U + 64 * h + 32 * hf), *reinterpret_cast<float(*)[16]>(u));
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_U + 64 * h + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(u + 16));
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_W + 64 * h + 32 * hf), *reinterpret_cast<float(*)[16]>(wv));
-            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_W + 64 * h + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(wv + 16));
+            float u[16], wv[16];
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_U + 64 * h + 16 * hf), u);
+            tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_W + 64 * h + 16 * hf), wv);
             tc::wait_ld();
             if (!ss.abort) {
                 float *U = reinterpret_cast<float *>(blob[h] + BLOB_U);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int t = 32 * hf + e;
+                for (int e = 0; e < 16; ++e) {
+                    const int t = 16 * hf + e;
                     U[t * DV + j] = u[e];
                     *reinterpret_cast<bf16 *>(blob[h] + BLOB_W + km<2>(t, j, DK)) = from_f<bf16>(wv[e]);
                 }
@@ -677,7 +693,7 @@ __device__ __forceinline__ void store_s_bf16(unsigned char *sm, int i, int hf, c
 __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
+    unsigned char *sm = smem_aligned128(smem_raw);
     P2Small &ss = *reinterpret_cast<P2Small *>(sm + S2_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x, vh = blockIdx.y, jb = blockIdx.z;

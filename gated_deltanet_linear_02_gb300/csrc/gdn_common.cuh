@@ -28,7 +28,9 @@ static_assert(V_OFF + HV * DV == CC, "conv channel split");
 typedef __nv_bfloat16 bf16;
 
 __device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+// bf16 -> fp32 is exact: a bf16 is the top half of the fp32 bit pattern, so
+// the widening is a 16-bit shift on the integer pipe.
+__device__ __forceinline__ float to_f(bf16 x) { return __uint_as_float((uint32_t)__bfloat16_as_ushort(x) << 16); }
 
 template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
