@@ -311,11 +311,12 @@ def cpu_baseline(n_seq=None):
     from oracle import oracle
     oracle.build()
     threads = host_threads()
-    n_seq = n_seq or max(16, 8 * threads)
+    n_seq = n_seq or BATCH                # one whole decode step: ~1 s wall on 16 cores
     secs, toks = oracle_decode_sample(n_seq, threads)
     return {"value": toks / secs, "unit": "tok/s", "cores": threads, "kind": "oracle",
-            "sample": f"one decode token through all 30 layers for {n_seq} of the 256 sequences "
-                      f"(fp64 oracle, {threads} threads over sequences), {secs:.1f} s wall"}
+            "sample": f"one decode token through all 30 layers for {n_seq} of the {BATCH} sequences "
+                      f"(fp64 oracle, {threads} threads over sequences), {secs:.1f} s wall, "
+                      f"{secs * threads:.0f} core-seconds"}
 
 
 # ------------------------------------------------------------------- main
