@@ -42,8 +42,14 @@ NOMINAL_HBM_GBS = 8000.0
 # inputs qkv, z, alpha and beta are read and out written once (16384 + 8192 +
 # 128 + 8192). The layer's parameters (conv_w 131072, A_log, dt_bias and norm_w
 # 768) are read once per launch.
-DECODE_BYTES_PER_TOKEN_LAYER = 4_194_304 + 98_304 + 32_896
+DECODE_STATE_CONV_BYTES = 4_194_304 + 98_304
+DECODE_IO_BYTES_PER_TOKEN = 32_896
+DECODE_BYTES_PER_TOKEN_LAYER = DECODE_STATE_CONV_BYTES + DECODE_IO_BYTES_PER_TOKEN
 DECODE_PARAM_BYTES_PER_LAUNCH = 131_840
+# Multi-token decode (gdn_decode_multi): MULTI_T tokens per sequence per call,
+# e.g. a speculative step. The state and conv_state cross HBM once per call, the
+# per-token inputs and outputs once per token.
+MULTI_T = 4
 # Algorithmic FLOPs of the chunked prefill per token: the dense contractions
 # K K^T and Q K^T once per K-head; T V, T (Gamma K), W S, Q S, the intra-chunk
 # (M o Q K^T) V_new and the state update K^T V_new per V-head, with C=64.
@@ -191,6 +197,34 @@ def run_gpu(args, rank, world, dev):
     achieved = bytes_per_launch / per_launch_s / 1e9
     dec_tok_s = job_rate(BATCH * args.steps, world, dec_ms)
 
+    # ---------------- multi-token decode: MULTI_T consecutive tokens per sequence
+    #                  (gdn_decode_multi) through the same 30 layers and states
+    m_streams = [I.streams(I.seed_of(3, 100 + layer), MULTI_T, torch.bfloat16, device=dev, lead=(BATCH,))
+                 for layer in range(LAYERS)]
+    m_out = [torch.empty(BATCH, MULTI_T, I.D_INNER, dtype=torch.bfloat16, device=dev) for _ in range(LAYERS)]
+
+    def multi_step():
+        for L, ms, mo in zip(layers, m_streams, m_out):
+            ops.decode_multi(None, ms.qkv, ms.z, ms.alpha, ms.beta, L["conv"], L["S"], mo, cparams=L["cp"])
+
+    for _ in range(args.warmup):
+        multi_step()
+    barrier_sync()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        multi_step()
+    ev1.record(stream)
+    barrier_sync()
+    sampler.mark(t_wall0, time.time())
+    mt_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    mt_launch_s = mt_ms / 1e3 / (LAYERS * args.steps)
+    mt_bytes = BATCH * (DECODE_STATE_CONV_BYTES + MULTI_T * DECODE_IO_BYTES_PER_TOKEN) + DECODE_PARAM_BYTES_PER_LAUNCH
+    mt = dict(tok_s=job_rate(BATCH * MULTI_T * args.steps, world, mt_ms), launch_s=mt_launch_s, bytes=mt_bytes,
+              achieved=mt_bytes / mt_launch_s / 1e9)
+    assert ops.device_error() == ops.GDN_OK
+    del m_streams, m_out
+
     # ---------------- e2e: the same decode through the C ABI from pinned host buffers
     host_in = []
     for L in layers:
@@ -257,7 +291,7 @@ def run_gpu(args, rank, world, dev):
     pf_tflops = PREFILL_FLOP_PER_TOKEN * PREFILL_T / (pf_ms / 1e3) / 1e12
     clocks = sampler.stop()
 
-    return dict(dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
+    return dict(mt=mt, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
                 bytes_per_launch=bytes_per_launch, launches=launches, e2e_tok_s=e2e_tok_s, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, pf_ms=pf_ms, pf_tok_s=pf_tok_s, pf_tflops=pf_tflops, hbm_peak=hbm_peak,
                 tc_peak=tc_peak, peak_src=peak_src, clocks=clocks)
@@ -458,6 +492,12 @@ def main():
                     "roofline": {"bound": "tensor", "achieved": r["pf_tflops"], "peak": r["tc_peak"],
                                  "unit": "TFLOP/s", "frac": r["pf_tflops"] / r["tc_peak"],
                                  "algorithmic_flop_per_call": PREFILL_FLOP_PER_TOKEN * PREFILL_T}},
+        "decode_multi": {"workload": f"decode_multi_30L_B{BATCH}_T{MULTI_T}_bf16", "value": r["mt"]["tok_s"],
+                         "unit": "tok/s", "tokens_per_sequence_per_call": MULTI_T,
+                         "launch_us": r["mt"]["launch_s"] * 1e6,
+                         "roofline": {"bound": "hbm", "achieved": r["mt"]["achieved"], "peak": r["hbm_peak"],
+                                      "unit": "GB/s", "frac": r["mt"]["achieved"] / r["hbm_peak"],
+                                      "algorithmic_bytes_per_launch": r["mt"]["bytes"]}},
     }
     print(json.dumps(line))
 

@@ -11,6 +11,9 @@ cudaError_t take_decode_error(unsigned int *word, cudaStream_t s);
 cudaError_t launch_conv_step(const float *, const void *, void *, void *, int, gdn_dtype, cudaStream_t);
 cudaError_t launch_decode_step(const gdn_params *, const void *, const void *, const void *, const void *,
                                void *, float *, void *, int, gdn_dtype, gdn_dtype, cudaStream_t);
+cudaError_t launch_decode_multi(const gdn_params *, const void *, const void *, const void *, const void *,
+                                void *, float *, void *, int, int, gdn_dtype, gdn_dtype, cudaStream_t);
+cudaError_t take_multi_error(unsigned int *word, cudaStream_t s);
 size_t scan_workspace_bytes(int T_total);
 cudaError_t launch_prefill_scan(const gdn_params *, const void *, const void *, const void *, const void *,
                                 const int32_t *, int, int, const void *, void *, const float *, float *,
@@ -124,6 +127,24 @@ gdn_status gdn_decode_step(const gdn_params *p, const void *qkv, const void *z, 
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_decode_step");
 }
 
+gdn_status gdn_decode_multi(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
+                            const void *beta, void *conv_state, float *ssm_state, void *out, int B, int T,
+                            gdn_dtype act, gdn_dtype out_dt, void *stream)
+{
+    if (!ok_dtype(act) || !ok_dtype(out_dt)) return fail(GDN_ERR_INVALID_ARG, "unknown dtype");
+    if (B < 0 || B > MAX_B) return fail(GDN_ERR_INVALID_ARG, "B out of range [0, 65535]");
+    if (T < 1 || T > GDN_DECODE_MAX_T) return fail(GDN_ERR_INVALID_ARG, "T out of range [1, GDN_DECODE_MAX_T]");
+    if (B == 0) return GDN_OK;
+    gdn_status st = check_params(p);
+    if (st != GDN_OK) return st;
+    if (!ok_ptr(qkv) || !ok_ptr(z) || !ok_ptr(alpha) || !ok_ptr(beta) || !ok_ptr(conv_state) ||
+        !ok_ptr(ssm_state) || !ok_ptr(out))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    cudaError_t e = launch_decode_multi(p, qkv, z, alpha, beta, conv_state, ssm_state, out, B, T, act, out_dt,
+                                        (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_decode_multi");
+}
+
 size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_size)
 {
     if (N < 0 || N > MAX_N || T_total < 0 || T_total > MAX_T || !ok_dtype(act)) return 0;
@@ -180,10 +201,12 @@ gdn_status gdn_device_error(void *stream)
     cudaStream_t s = (cudaStream_t)stream;
     unsigned int word = 0;
     unsigned int word2 = 0;
+    unsigned int word3 = 0;
     cudaError_t e = take_decode_error(&word, s);
     if (e == cudaSuccess) e = take_chunk_error(&word2, s);
+    if (e == cudaSuccess) e = take_multi_error(&word3, s);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_error");
-    return (word | word2) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
+    return (word | word2 | word3) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_conv_step.argtypes = [_vp, _vp, _vp, _vp, _int, _int, _vp]
         L.gdn_decode_step.restype = _int
         L.gdn_decode_step.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 7 + [_int, _int, _int, _vp]
+        L.gdn_decode_multi.restype = _int
+        L.gdn_decode_multi.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 7 + [_int, _int, _int, _int, _vp]
         L.gdn_prefill.restype = _int
         L.gdn_prefill.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 5 + [_int, _int] + [_vp] * 5 + \
             [_int, _int, _int, _vp, _sz, _vp]
@@ -116,12 +118,18 @@ def _ptr(t: torch.Tensor | None, name: str, shape=None, dtype=None, device=None)
 
 def make_params(p) -> gdn_params:
     """gdn_params from anything with conv_w, A_log, dt_bias, norm_w fp32 CUDA
-    tensors and norm_eps, l2_eps floats (e.g. inputs.LayerParams)."""
-    return gdn_params(_ptr(p.conv_w, "conv_w", (CC, KC), torch.float32),
-                      _ptr(p.A_log, "A_log", (HV,), torch.float32),
-                      _ptr(p.dt_bias, "dt_bias", (HV,), torch.float32),
-                      _ptr(p.norm_w, "norm_w", (DV,), torch.float32),
-                      float(p.norm_eps), float(p.l2_eps))
+    tensors and norm_eps, l2_eps floats (e.g. inputs.LayerParams).
+
+    The struct holds raw device pointers, so it also keeps references to the
+    four tensors: they stay alive as long as the struct does, even when the
+    caller passed a temporary such as ``make_params(lp.to("cuda"))``."""
+    cp = gdn_params(_ptr(p.conv_w, "conv_w", (CC, KC), torch.float32),
+                    _ptr(p.A_log, "A_log", (HV,), torch.float32),
+                    _ptr(p.dt_bias, "dt_bias", (HV,), torch.float32),
+                    _ptr(p.norm_w, "norm_w", (DV,), torch.float32),
+                    float(p.norm_eps), float(p.l2_eps))
+    cp._keep_alive = (p.conv_w, p.A_log, p.dt_bias, p.norm_w)
+    return cp
 
 
 def _act_dtype(t: torch.Tensor) -> int:
@@ -155,6 +163,23 @@ def decode_step(params, qkv, z, alpha, beta, conv_state, ssm_state, out, stream=
                                _ptr(ssm_state, "ssm_state", (B, HV, DV, DK), torch.float32),
                                _ptr(out, "out", (B, DI)), B, act, od, _stream(stream))
     _check(st, "gdn_decode_step")
+
+
+def decode_multi(params, qkv, z, alpha, beta, conv_state, ssm_state, out, stream=None,
+                 cparams: gdn_params | None = None):
+    """gdn_decode_multi: T consecutive tokens for each of B sequences (qkv
+    [B][T][8192]), states updated in place."""
+    B, T = qkv.shape[0], qkv.shape[1]
+    dt = qkv.dtype
+    act = _act_dtype(qkv)
+    od = _act_dtype(out)
+    cp = cparams if cparams is not None else make_params(params)
+    st = lib().gdn_decode_multi(ctypes.byref(cp), _ptr(qkv, "qkv", (B, T, CC)), _ptr(z, "z", (B, T, DI), dt),
+                                _ptr(alpha, "alpha", (B, T, HV), dt), _ptr(beta, "beta", (B, T, HV), dt),
+                                _ptr(conv_state, "conv_state", (B, KC - 1, CC), dt),
+                                _ptr(ssm_state, "ssm_state", (B, HV, DV, DK), torch.float32),
+                                _ptr(out, "out", (B, T, DI)), B, T, act, od, _stream(stream))
+    _check(st, "gdn_decode_multi")
 
 
 def prefill_workspace_size(N: int, T_total: int, act=torch.bfloat16, chunk_size: int = 0) -> int:
@@ -196,6 +221,7 @@ def device_error(stream=None) -> int:
 
 
 STATIC_SCRATCH_BYTES = 64 << 20
+DECODE_MAX_T = 8   # GDN_DECODE_MAX_T: tokens per sequence of gdn_decode_multi, at most
 
 
 def prefill_static(params, qkv, z, alpha, beta, cu_seqlens, out, conv_state_in=None, conv_state_out=None,

@@ -53,6 +53,7 @@ extern "C" {
 #define GDN_CONV_K 4
 #define GDN_CONV_CHANNELS 8192
 #define GDN_D_INNER 4096
+#define GDN_DECODE_MAX_T 8   /* tokens per sequence of gdn_decode_multi, at most */
 
 typedef enum {
     GDN_OK = 0,
@@ -108,6 +109,30 @@ gdn_status gdn_decode_step(const gdn_params *p, const void *qkv, const void *z,
                            const void *alpha, const void *beta, void *conv_state,
                            float *ssm_state, void *out, int B, gdn_dtype act,
                            gdn_dtype out_dt, void *stream);
+
+/*
+ * gdn_decode_multi -- T consecutive tokens (1 <= T <= GDN_DECODE_MAX_T) for each
+ * of B independent sequences, for example a speculative step's draft tokens. It
+ * is the same mixer as gdn_decode_step, applied to the T tokens in order: the
+ * conv window is the conv_state followed by the T inputs, and the recurrence
+ * (a)-(d) of section "Per-token recurrence" runs token after token with
+ * read-after-write. The result equals T successive gdn_decode_step calls up to
+ * rounding order. Each state is read once and written once for all T tokens.
+ *   p           layer parameters
+ *   qkv         [B][T][8192] act          z          [B][T][4096] act
+ *   alpha, beta [B][T][32] act (raw logits)
+ *   conv_state  [B][3][8192] act, updated in place (it ends with the last three
+ *               raw inputs of the window)
+ *   ssm_state   [B][32][128 j][128 i] fp32, updated in place
+ *   out         [B][T][4096] out_dt
+ * 1 <= B <= 65535 (B == 0 is a no-op). Errors: GDN_ERR_INVALID_ARG (also for T
+ * out of range), GDN_ERR_CUDA. A bounded device wait that gives up is reported
+ * afterwards by gdn_device_error.
+ */
+gdn_status gdn_decode_multi(const gdn_params *p, const void *qkv, const void *z,
+                            const void *alpha, const void *beta, void *conv_state,
+                            float *ssm_state, void *out, int B, int T, gdn_dtype act,
+                            gdn_dtype out_dt, void *stream);
 
 /*
  * gdn_prefill -- N packed sequences of total length T_total, each run through

@@ -30,7 +30,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("gdn_conv_step", "gdn_decode_step", "gdn_prefill", "gdn_prefill_workspace_size",
+    for n in ("gdn_conv_step", "gdn_decode_step", "gdn_decode_multi", "gdn_prefill", "gdn_prefill_workspace_size",
               "gdn_device_error", "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
         assert n in names
 
@@ -102,6 +102,29 @@ def test_decode_argument_checks(ops):
     assert call(_params(ops, conv_w=MIS), ok_args, 4) == ops.GDN_ERR_INVALID_ARG
     assert call(_params(ops, norm_eps=-1.0), ok_args, 4) == ops.GDN_ERR_INVALID_ARG
     assert call(_params(ops, l2_eps=float("nan")), ok_args, 4) == ops.GDN_ERR_INVALID_ARG
+
+
+def test_decode_multi_argument_checks(ops):
+    L = ops.lib()
+    p = _params(ops)
+    ok_args = [FAKE] * 7
+    call = lambda pp, args, B, T, act=ops.GDN_BF16, od=ops.GDN_F32: L.gdn_decode_multi(
+        ctypes.byref(pp) if pp is not None else None, *args, B, T, act, od, None)
+    assert call(p, ok_args, 0, 4) == ops.GDN_OK                             # empty batch: no-op
+    assert call(p, ok_args, 0, 0) == ops.GDN_ERR_INVALID_ARG                # T checked even then
+    assert call(p, ok_args, 4, 0) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, ok_args, 4, ops.DECODE_MAX_T + 1) == ops.GDN_ERR_INVALID_ARG
+    assert "T out of range" in ops.last_error()
+    assert call(p, ok_args, -1, 2) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, ok_args, 65536, 2) == ops.GDN_ERR_INVALID_ARG
+    assert call(None, ok_args, 4, 2) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, ok_args, 4, 2, od=7) == ops.GDN_ERR_INVALID_ARG
+    for i in range(7):
+        bad = list(ok_args)
+        bad[i] = 0
+        assert call(p, bad, 4, 2) == ops.GDN_ERR_INVALID_ARG
+        bad[i] = MIS
+        assert call(p, bad, 4, 2) == ops.GDN_ERR_INVALID_ARG
 
 
 def test_conv_step_argument_checks(ops):
