@@ -14,6 +14,8 @@ cudaError_t launch_decode_step(const gdn_params *, const void *, const void *, c
 cudaError_t launch_decode_multi(const gdn_params *, const void *, const void *, const void *, const void *,
                                 void *, float *, void *, int, int, gdn_dtype, gdn_dtype, cudaStream_t);
 cudaError_t take_multi_error(unsigned int *word, cudaStream_t s);
+cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s);
+cudaError_t take_gemm_error(unsigned int *word, cudaStream_t s);
 size_t scan_workspace_bytes(int T_total);
 cudaError_t launch_prefill_scan(const gdn_params *, const void *, const void *, const void *, const void *,
                                 const int32_t *, int, int, const void *, void *, const float *, float *,
@@ -145,6 +147,17 @@ gdn_status gdn_decode_multi(const gdn_params *p, const void *qkv, const void *z,
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_decode_multi");
 }
 
+gdn_status gdn_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, void *stream)
+{
+    if (!ok_dtype(out_dt)) return fail(GDN_ERR_INVALID_ARG, "unknown output dtype");
+    if (M < 0 || M > (1 << 24)) return fail(GDN_ERR_INVALID_ARG, "M out of range [0, 2^24]");
+    if (M == 0) return GDN_OK;
+    if (!ok_ptr(x) || !ok_ptr(w) || !ok_ptr(y))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    cudaError_t e = launch_out_proj(x, w, y, M, out_dt, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_out_proj");
+}
+
 size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_size)
 {
     if (N < 0 || N > MAX_N || T_total < 0 || T_total > MAX_T || !ok_dtype(act)) return 0;
@@ -202,11 +215,13 @@ gdn_status gdn_device_error(void *stream)
     unsigned int word = 0;
     unsigned int word2 = 0;
     unsigned int word3 = 0;
+    unsigned int word4 = 0;
     cudaError_t e = take_decode_error(&word, s);
     if (e == cudaSuccess) e = take_chunk_error(&word2, s);
     if (e == cudaSuccess) e = take_multi_error(&word3, s);
+    if (e == cudaSuccess) e = take_gemm_error(&word4, s);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_error");
-    return (word | word2 | word3) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
+    return (word | word2 | word3 | word4) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -1,0 +1,262 @@
+// gdn_gemm.cu -- the ssm_out projection on 5th-generation tensor cores:
+// y[m][n] = sum_k x[m][k] w[n][k], with x the gated mixer output [M][4096] and w
+// the layer's ssm_out.weight [2048][4096], both bf16, accumulated in fp32.
+// The step is "cur = ssm_out . gated" of "qwen35moe -- Forward-Pass Design
+// (Pantheon port)", section "Output path" (projection 4096 -> n_embd 2048).
+//
+// Design. A persistent grid walks output tiles of 128 rows x 256 columns. Per
+// CTA:
+//  - warp 0, lane 0: the TMA producer. 2-D tensor-map copies bring 64-wide K
+//    slices of x (128 x 64) and w (256 x 64) into a ring of four shared-memory
+//    stages in the 128-byte-swizzle layout the tensor core reads directly.
+//  - warp 1, lane 0: the MMA issuer. Per K slice, four tcgen05.mma (kind::f16,
+//    M=128, N=256, K=16) accumulate into one of two 256-column fp32
+//    accumulators in tensor memory; commits release the stage, and after the
+//    last slice, the accumulator.
+//  - warps 2..5: the epilogue. Each thread owns one accumulator row (its TMEM
+//    lane) and writes its 256 outputs, while the MMA warp already fills the
+//    other accumulator with the next tile.
+// All waits are bounded; a wait that gives up records GDN_ERR_TIMEOUT.
+#include <cuda.h>
+
+#include "gdn_async.cuh"
+#include "gdn_common.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+__device__ unsigned int g_gemm_error;   // GDN_ERR_TIMEOUT if a bounded wait gave up
+
+constexpr int GM_BM = 128, GM_BN = 256, GM_BK = 64, GM_STAGES = 4;
+constexpr int GM_K = DI;                          // 4096
+constexpr int GM_N = GDN_HIDDEN;                  // 2048
+constexpr int GM_KB = GM_K / GM_BK;               // K slices per tile
+constexpr uint32_t GM_A_BYTES = GM_BM * GM_BK * 2;        // 16 KiB
+constexpr uint32_t GM_B_BYTES = GM_BN * GM_BK * 2;        // 32 KiB
+constexpr uint32_t GM_STAGE_BYTES = GM_A_BYTES + GM_B_BYTES;
+constexpr int GM_THREADS = 192;                   // TMA warp, MMA warp, 4 epilogue warps
+constexpr uint32_t GM_TMEM_COLS = 2 * GM_BN;      // two accumulators
+static_assert(GM_N % GM_BN == 0 && GM_K % GM_BK == 0, "tile shape");
+
+struct GemmSmem {
+    alignas(1024) unsigned char stage[GM_STAGES][GM_STAGE_BYTES];   // A tile | B tile, 1024-byte aligned
+    alignas(8) uint64_t full[GM_STAGES], empty[GM_STAGES];
+    uint64_t acc_full[2], acc_empty[2];
+    int last_it[GM_STAGES];                       // last K slice loaded into each stage (for an abort)
+    uint32_t tmem;
+    int abort;
+};
+constexpr size_t GM_SMEM = sizeof(GemmSmem) + 1024;   // + slack to align the block to 1024 bytes
+
+// 2-D tiled TMA load of the box at element coordinates (x = K, y = row).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+                 "[%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(GM_THREADS, 1) out_proj_kernel(const __grid_constant__ CUtensorMap mx,
+                                                                 const __grid_constant__ CUtensorMap mw,
+                                                                 TO *__restrict__ y, int M)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *blk = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    GemmSmem &sm = *reinterpret_cast<GemmSmem *>(blk);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_tiles = GM_N / GM_BN;
+    const int n_work = ((M + GM_BM - 1) / GM_BM) * n_tiles;
+    const volatile int &aborted = sm.abort;
+
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(&sm.tmem), GM_TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int s = 0; s < GM_STAGES; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
+            sm.last_it[s] = -1;
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&sm.acc_full[b]), 1);
+            mbar_init(smem_u32(&sm.acc_empty[b]), 128);
+        }
+        sm.abort = 0;
+        fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = sm.tmem;
+
+    if (warp == 0) {
+        // ---- TMA producer
+        if (lane == 0) {
+            int it = 0;                                // K slices issued so far, over all tiles
+            for (int w = blockIdx.x; w < n_work && !aborted; w += gridDim.x) {
+                const int mt = w / n_tiles, nt = w % n_tiles;
+                for (int kb = 0; kb < GM_KB; ++kb, ++it) {
+                    const int s = it % GM_STAGES;
+                    if (it >= GM_STAGES &&
+                        !mbar_wait_bounded(smem_u32(&sm.empty[s]), (uint32_t)((it / GM_STAGES - 1) & 1)))
+                        sm.abort = 1;
+                    if (aborted) break;
+                    const uint32_t dst = smem_u32(sm.stage[s]);
+                    mbar_arrive_expect_tx(smem_u32(&sm.full[s]), GM_STAGE_BYTES);
+                    tma_load_2d(dst, &mx, kb * GM_BK, mt * GM_BM, smem_u32(&sm.full[s]));
+                    tma_load_2d(dst + GM_A_BYTES, &mw, kb * GM_BK, nt * GM_BN, smem_u32(&sm.full[s]));
+                    sm.last_it[s] = it;
+                }
+            }
+            if (aborted)                               // let the copies in flight land before the CTA exits
+                for (int s = 0; s < GM_STAGES; ++s)
+                    if (sm.last_it[s] >= 0)
+                        mbar_wait_bounded(smem_u32(&sm.full[s]), (uint32_t)((sm.last_it[s] / GM_STAGES) & 1));
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc::instr_desc(tc::FMT_BF16, GM_BM, GM_BN);
+            int it = 0, ti = 0;
+            for (int w = blockIdx.x; w < n_work && !aborted; w += gridDim.x, ++ti) {
+                const int ab = ti & 1;
+                if (ti >= 2 && !mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), (uint32_t)(((ti >> 1) - 1) & 1)))
+                    sm.abort = 1;
+                tc::fence_after_sync();
+                const uint32_t d = tm + (uint32_t)(GM_BN * ab);
+                for (int kb = 0; kb < GM_KB; ++kb, ++it) {
+                    const int s = it % GM_STAGES;
+                    if (!mbar_wait_bounded(smem_u32(&sm.full[s]), (uint32_t)((it / GM_STAGES) & 1))) sm.abort = 1;
+                    if (aborted) break;
+                    tc::fence_after_sync();
+                    const uint32_t a0 = smem_u32(sm.stage[s]);
+                    const uint64_t ad = tc::sw128_desc(a0), bd = tc::sw128_desc(a0 + GM_A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < GM_BK / 16; ++k)      // K step of 16 bf16 = 32 bytes = 2 descriptor units
+                        tc::mma_f16(d, ad + 2u * k, bd + 2u * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    tc::mma_commit(smem_u32(&sm.empty[s]));   // the stage is free once these have read it
+                }
+                if (aborted) break;
+                tc::mma_commit(smem_u32(&sm.acc_full[ab]));
+            }
+        }
+    } else {
+        // ---- epilogue: thread (lane quarter warp % 4, lane) owns accumulator row 32 q + lane
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        int ti = 0;
+        for (int w = blockIdx.x; w < n_work; w += gridDim.x, ++ti) {
+            const int ab = ti & 1;
+            const int mt = w / n_tiles, nt = w % n_tiles;
+            if (!mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (uint32_t)((ti >> 1) & 1))) sm.abort = 1;
+            if (aborted) break;
+            tc::fence_after_sync();
+            const int m = mt * GM_BM + row;
+            TO *dst = y + (size_t)m * GM_N + (size_t)nt * GM_BN;
+#pragma unroll 2
+            for (int c = 0; c < GM_BN; c += 32) {
+                float v[32];
+                tc::tmem_ld16(tc::tmem_addr(tm + (uint32_t)(GM_BN * ab), 32 * q, c), *reinterpret_cast<float(*)[16]>(v));
+                tc::tmem_ld16(tc::tmem_addr(tm + (uint32_t)(GM_BN * ab), 32 * q, c + 16),
+                              *reinterpret_cast<float(*)[16]>(v + 16));
+                tc::wait_ld();
+                if (m < M) {
+                    if (sizeof(TO) == 4) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst + c);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                    } else {
+                        __align__(16) bf16 o[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = from_f<bf16>(v[e]);
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) d4[e] = reinterpret_cast<const uint4 *>(o)[e];
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            mbar_arrive(smem_u32(&sm.acc_empty[ab]));  // the MMA warp may refill this accumulator
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tc::tmem_dealloc(tm, GM_TMEM_COLS);
+    if (tid == 0 && sm.abort) atomicExch(&g_gemm_error, (unsigned int)GDN_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ launcher
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// Row-major bf16 matrix [rows][4096] read in boxes of 64 columns x box_rows rows,
+// 128-byte swizzle; rows past the end read as zero.
+static bool make_map(CUtensorMap *map, const void *base, int rows, int box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)GM_K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)GM_K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)GM_BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count();
+
+cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s)
+{
+    if (M <= 0) return cudaSuccess;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, x, M, GM_BM) || !make_map(&mw, w, GM_N, GM_BN)) return cudaErrorInvalidValue;
+    const int n_work = ((M + GM_BM - 1) / GM_BM) * (GM_N / GM_BN);
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return cudaErrorInvalidDevice;
+    const int grid = n_work < n_sm ? n_work : n_sm;
+    cudaError_t e;
+    if (out_dt == GDN_F32) {
+        e = cudaFuncSetAttribute(out_proj_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+        if (e == cudaSuccess) out_proj_kernel<float><<<grid, GM_THREADS, GM_SMEM, s>>>(mx, mw, (float *)y, M);
+    } else {
+        e = cudaFuncSetAttribute(out_proj_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+        if (e == cudaSuccess) out_proj_kernel<bf16><<<grid, GM_THREADS, GM_SMEM, s>>>(mx, mw, (bf16 *)y, M);
+    }
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+// Reads and clears this file's device error word (synchronous on `s`).
+cudaError_t take_gemm_error(unsigned int *word, cudaStream_t s)
+{
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_gemm_error, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && *word != 0)
+        e = cudaMemcpyToSymbolAsync(g_gemm_error, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e;
+}
+
+}  // namespace gdn

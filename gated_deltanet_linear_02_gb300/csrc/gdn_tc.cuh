@@ -48,6 +48,18 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int k0, int Kd)
     return smem_desc(base + (uint32_t)((k0 / (16 / ES)) * 128), 128u, (uint32_t)(Kd * ES * 8));
 }
 
+// Descriptor of a K-major tile in the 128-byte-swizzle layout that a TMA copy
+// with CU_TENSOR_MAP_SWIZZLE_128B writes for a box 128 bytes wide: rows of 128
+// bytes (64 bf16), the 16-byte chunks of row r permuted by XOR with r % 8, and
+// 8-row groups 1024 bytes apart (SBO). Layout type 2 (bits 61-63) selects the
+// 128-byte swizzle; the leading-dimension offset is unused for this layout. The
+// tile base must be 1024-byte aligned. A K offset of b bytes inside the row is
+// added to the start address (b >> 4 in the descriptor's low field).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    return smem_desc(saddr, 16u, 1024u) | ((uint64_t)2 << 61);
+}
+
 enum : uint32_t { FMT_F16 = 0, FMT_BF16 = 1, FMT_TF32 = 2 };
 
 // An fp32 value rounded to the nearest tf32 (10-bit mantissa). The tensor core

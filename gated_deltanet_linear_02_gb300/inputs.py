@@ -105,6 +105,16 @@ def initial_states(seed: int, N: int, act_dtype=torch.bfloat16, device="cpu", ze
     return conv, ssm
 
 
+N_EMBD = 2048                        # output width of the ssm_out projection
+
+
+def out_proj_weight(seed: int, act_dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
+    """ssm_out.weight [2048][4096] ~ N(0, 1/64) (std), so outputs keep the input
+    scale; rounded once to the activation dtype."""
+    g = _gen(seed + 800_000, device)
+    return (torch.randn(N_EMBD, D_INNER, generator=g, device=device) / 64.0).to(act_dtype)
+
+
 def varlen_lengths(seed: int, n: int = 8, lo: int = 256, hi: int = 32768) -> list[int]:
     """Sequence lengths drawn log-uniformly in [lo, hi] and rounded."""
     g = _gen(seed + 700_000, "cpu")

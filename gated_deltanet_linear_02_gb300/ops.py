@@ -23,6 +23,7 @@ GDN_F32, GDN_BF16 = 0, 1
 _DT = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
 
 HV, HK, DK, DV, KC, CC, DI = _inp.HV, _inp.HK, _inp.DK, _inp.DV, _inp.KCONV, _inp.C_CONV, _inp.D_INNER
+N_EMBD = _inp.N_EMBD
 
 
 class GdnError(RuntimeError):
@@ -55,6 +56,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_decode_step.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 7 + [_int, _int, _int, _vp]
         L.gdn_decode_multi.restype = _int
         L.gdn_decode_multi.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 7 + [_int, _int, _int, _int, _vp]
+        L.gdn_out_proj.restype = _int
+        L.gdn_out_proj.argtypes = [_vp, _vp, _vp, _int, _int, _vp]
         L.gdn_prefill.restype = _int
         L.gdn_prefill.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 5 + [_int, _int] + [_vp] * 5 + \
             [_int, _int, _int, _vp, _sz, _vp]
@@ -180,6 +183,16 @@ def decode_multi(params, qkv, z, alpha, beta, conv_state, ssm_state, out, stream
                                 _ptr(ssm_state, "ssm_state", (B, HV, DV, DK), torch.float32),
                                 _ptr(out, "out", (B, T, DI)), B, T, act, od, _stream(stream))
     _check(st, "gdn_decode_multi")
+
+
+def out_proj(x, w, y, stream=None):
+    """gdn_out_proj: y = x w^T on the tensor cores (x [M][4096] bf16, w
+    [2048][4096] bf16, y [M][2048] fp32 or bf16)."""
+    M = x.shape[0]
+    od = _act_dtype(y)
+    st = lib().gdn_out_proj(_ptr(x, "x", (M, DI), torch.bfloat16), _ptr(w, "w", (N_EMBD, DI), torch.bfloat16),
+                            _ptr(y, "y", (M, N_EMBD)), M, od, _stream(stream))
+    _check(st, "gdn_out_proj")
 
 
 def prefill_workspace_size(N: int, T_total: int, act=torch.bfloat16, chunk_size: int = 0) -> int:

@@ -54,6 +54,7 @@ extern "C" {
 #define GDN_CONV_CHANNELS 8192
 #define GDN_D_INNER 4096
 #define GDN_DECODE_MAX_T 8   /* tokens per sequence of gdn_decode_multi, at most */
+#define GDN_HIDDEN 2048      /* n_embd: the output width of the ssm_out projection */
 
 typedef enum {
     GDN_OK = 0,
@@ -207,6 +208,23 @@ gdn_status gdn_prefill_static(const gdn_params *p, const void *qkv, const void *
                               const void *conv_state_in, void *conv_state_out,
                               const float *ssm_state_in, float *ssm_state_out, void *out,
                               gdn_dtype act, gdn_dtype out_dt, int chunk_size, void *stream);
+
+/*
+ * gdn_out_proj -- the projection right after the mixer, section "Output path":
+ * cur = ssm_out . gated, 4096 -> GDN_HIDDEN (2048). It computes
+ *   y[m][n] = sum_k x[m][k] * w[n][k]
+ * with bf16 operands and fp32 accumulation on the tensor cores.
+ *   x   [M][4096] bf16: the gated output of gdn_decode_step / gdn_prefill
+ *       (out_dt = GDN_BF16), row-major
+ *   w   [2048][4096] bf16: the layer's ssm_out.weight, row-major (one row per
+ *       output feature)
+ *   y   [M][2048] out_dt
+ * 0 <= M <= 2^24 (M == 0 is a no-op). x and w must be 16-byte aligned (their row
+ * stride, 8192 bytes, is fixed). Errors: GDN_ERR_INVALID_ARG, GDN_ERR_CUDA (also
+ * when the driver's tensor-map encoder is unavailable). A bounded device wait
+ * that gives up is reported afterwards by gdn_device_error.
+ */
+gdn_status gdn_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, void *stream);
 
 /* Bytes of workspace gdn_prefill needs for these sizes (0 if the arguments are
  * invalid; never 0 for valid ones). Pure host arithmetic. */

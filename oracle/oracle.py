@@ -177,6 +177,17 @@ def delta_rule_chunked(q, k, v, g, b, S0, scale, chunk):
 
 # --------------------------------------------------------------- whole mixer
 
+def out_proj(x, w):
+    """The projection after the mixer, section "Output path": cur = ssm_out .
+    gated, 4096 -> n_embd. With x [M][K] (the gated output rows) and w [N][K]
+    (ssm_out.weight, one row per output feature):
+    y[m][n] = sum_k x[m][k] w[n][k]. fp64 over exact copies of the inputs;
+    the library matrix product is the step."""
+    x, w = _f64(x), _f64(w)
+    assert x.ndim == 2 and w.ndim == 2 and x.shape[1] == w.shape[1]
+    return x @ w.T
+
+
 @dataclass
 class Params:
     """One layer's parameters as fp64 arrays (the page's tensor roles:

@@ -127,6 +127,20 @@ def test_decode_multi_argument_checks(ops):
         assert call(p, bad, 4, 2) == ops.GDN_ERR_INVALID_ARG
 
 
+def test_out_proj_argument_checks(ops):
+    L = ops.lib()
+    assert L.gdn_out_proj(FAKE, FAKE, FAKE, 0, ops.GDN_BF16, None) == ops.GDN_OK      # empty: no-op
+    assert L.gdn_out_proj(FAKE, FAKE, FAKE, -1, ops.GDN_BF16, None) == ops.GDN_ERR_INVALID_ARG
+    assert L.gdn_out_proj(FAKE, FAKE, FAKE, (1 << 24) + 1, ops.GDN_BF16, None) == ops.GDN_ERR_INVALID_ARG
+    assert L.gdn_out_proj(FAKE, FAKE, FAKE, 4, 9, None) == ops.GDN_ERR_INVALID_ARG
+    for i in range(3):
+        args = [FAKE, FAKE, FAKE]
+        args[i] = 0
+        assert L.gdn_out_proj(*args, 4, ops.GDN_F32, None) == ops.GDN_ERR_INVALID_ARG
+        args[i] = MIS
+        assert L.gdn_out_proj(*args, 4, ops.GDN_F32, None) == ops.GDN_ERR_INVALID_ARG
+
+
 def test_conv_step_argument_checks(ops):
     L = ops.lib()
     assert L.gdn_conv_step(FAKE, FAKE, FAKE + 16, FAKE + 32, 0, ops.GDN_BF16, None) == ops.GDN_OK

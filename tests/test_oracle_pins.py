@@ -376,3 +376,40 @@ def test_layer_matches_chunked_form_composition(orc):
     o = np.stack([orc.gated_rmsnorm(y[t], z[t, vh * dv:(vh + 1) * dv], p.norm_w) for t in range(T)])
     np.testing.assert_allclose(out[:, vh * dv:(vh + 1) * dv], o, rtol=1e-9, atol=1e-12)
     np.testing.assert_allclose(Sf[vh], S2, rtol=1e-10, atol=1e-13)
+
+
+# ---------------------------------------------------------------- out_proj
+
+def test_out_proj_identity_block(orc):
+    """w = [I | 0] (n_embd x 4096) selects the first n_embd columns of x:
+    pins the orientation y = x w^T (one weight row per output feature)."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((5, 4096))
+    w = np.zeros((2048, 4096))
+    w[:, :2048] = np.eye(2048)
+    np.testing.assert_array_equal(orc.out_proj(x, w), x[:, :2048])
+
+
+def test_out_proj_brute_force(orc):
+    """Each output is the plain sum over k, written out as a loop on a slice."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((3, 64))
+    w = rng.standard_normal((5, 64))
+    y = orc.out_proj(x, w)
+    for m in range(3):
+        for n in range(5):
+            ref = 0.0
+            for k in range(64):
+                ref += x[m, k] * w[n, k]
+            assert abs(y[m, n] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def test_out_proj_rows_independent_and_linear(orc):
+    """Row m of y depends on row m of x only, linearly."""
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((4, 256))
+    w = rng.standard_normal((16, 256))
+    y = orc.out_proj(x, w)
+    y2 = orc.out_proj(2.0 * x[2:3], w)
+    np.testing.assert_allclose(y2[0], 2.0 * y[2], rtol=1e-12, atol=1e-12)
+
