@@ -289,9 +289,56 @@ def run_gpu(args, rank, world, dev):
     assert ops.device_error() == ops.GDN_OK
     pf_tok_s = job_rate(PREFILL_T, world, pf_ms)
     pf_tflops = PREFILL_FLOP_PER_TOKEN * PREFILL_T / (pf_ms / 1e3) / 1e12
+    # ---------------- ssm_out projection (gdn_out_proj, tcgen05 GEMM) at the prefill
+    #                  size and the decode batch, L2 flushed between timed calls
+    w_out = I.out_proj_weight(I.seed_of(2), device=dev)
+    op = {}
+    for M in (PREFILL_T, BATCH):
+        xo = torch.randn(M, I.D_INNER, device=dev).to(torch.bfloat16)
+        yo = torch.empty(M, I.N_EMBD, dtype=torch.bfloat16, device=dev)
+        for _ in range(args.warmup):
+            ops.out_proj(xo, w_out, yo)
+        barrier_sync()
+        times = []
+        t_wall0 = time.time()
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ops.out_proj(xo, w_out, yo)
+            b.record(stream)
+            times.append((a, b))
+        barrier_sync()
+        sampler.mark(t_wall0, time.time())
+        ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))
+        op[M] = dict(us=ms * 1e3, tflops=2.0 * M * I.D_INNER * I.N_EMBD / (ms / 1e3) / 1e12,
+                     gbs=(I.N_EMBD * I.D_INNER * 2 + M * I.D_INNER * 2 + M * I.N_EMBD * 2) / (ms / 1e3) / 1e9)
+        del xo, yo
+    # ---------------- input projections (gdn_in_proj) at the prefill size
+    w_in = torch.cat(I.in_proj_weights(I.seed_of(2), device=dev), dim=0)
+    h_in = torch.randn(PREFILL_T, I.N_EMBD, device=dev).to(torch.bfloat16)
+    outs_in = [torch.empty(PREFILL_T, n, dtype=torch.bfloat16, device=dev) for n in (I.C_CONV, I.D_INNER, I.HV, I.HV)]
+    for _ in range(args.warmup):
+        ops.in_proj(h_in, w_in, *outs_in)
+    barrier_sync()
+    times = []
+    t_wall0 = time.time()
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ops.in_proj(h_in, w_in, *outs_in)
+        b.record(stream)
+        times.append((a, b))
+    barrier_sync()
+    sampler.mark(t_wall0, time.time())
+    ip_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))
+    ip = dict(us=ip_ms * 1e3, tflops=2.0 * PREFILL_T * w_in.shape[0] * I.N_EMBD / (ip_ms / 1e3) / 1e12)
+    del w_in, h_in, outs_in
+    assert ops.device_error() == ops.GDN_OK
     clocks = sampler.stop()
 
-    return dict(mt=mt, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
+    return dict(ip=ip, op=op, mt=mt, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
                 bytes_per_launch=bytes_per_launch, launches=launches, e2e_tok_s=e2e_tok_s, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, pf_ms=pf_ms, pf_tok_s=pf_tok_s, pf_tflops=pf_tflops, hbm_peak=hbm_peak,
                 tc_peak=tc_peak, peak_src=peak_src, clocks=clocks)
@@ -492,6 +539,18 @@ def main():
                     "roofline": {"bound": "tensor", "achieved": r["pf_tflops"], "peak": r["tc_peak"],
                                  "unit": "TFLOP/s", "frac": r["pf_tflops"] / r["tc_peak"],
                                  "algorithmic_flop_per_call": PREFILL_FLOP_PER_TOKEN * PREFILL_T}},
+        "in_proj": {"workload": f"input_projections_M{PREFILL_T}_bf16", "op": "qkv|z|alpha|beta = h w_in^T, 2048 -> 12352",
+                    "us_per_call": r["ip"]["us"], "l2": "flushed between timed calls",
+                    "roofline": {"bound": "tensor", "achieved": r["ip"]["tflops"], "peak": r["tc_peak"],
+                                 "unit": "TFLOP/s", "frac": r["ip"]["tflops"] / r["tc_peak"]}},
+        "out_proj": {"workload": f"ssm_out_projection_M{PREFILL_T}_bf16", "op": "y = x w^T, 4096 -> 2048",
+                     "us_per_call": r["op"][PREFILL_T]["us"], "l2": "flushed between timed calls",
+                     "roofline": {"bound": "tensor", "achieved": r["op"][PREFILL_T]["tflops"], "peak": r["tc_peak"],
+                                  "unit": "TFLOP/s", "frac": r["op"][PREFILL_T]["tflops"] / r["tc_peak"]},
+                     "decode_batch": {"M": BATCH, "us_per_call": r["op"][BATCH]["us"],
+                                      "roofline": {"bound": "hbm", "achieved": r["op"][BATCH]["gbs"],
+                                                   "peak": r["hbm_peak"], "unit": "GB/s",
+                                                   "frac": r["op"][BATCH]["gbs"] / r["hbm_peak"]}}},
         "decode_multi": {"workload": f"decode_multi_30L_B{BATCH}_T{MULTI_T}_bf16", "value": r["mt"]["tok_s"],
                          "unit": "tok/s", "tokens_per_sequence_per_call": MULTI_T,
                          "launch_us": r["mt"]["launch_s"] * 1e6,

@@ -16,6 +16,8 @@ cudaError_t launch_decode_multi(const gdn_params *, const void *, const void *, 
 cudaError_t take_multi_error(unsigned int *word, cudaStream_t s);
 cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s);
 cudaError_t take_gemm_error(unsigned int *word, cudaStream_t s);
+cudaError_t launch_in_proj(const void *h, const void *w_in, void *qkv, void *z, void *alpha, void *beta, int M,
+                           gdn_dtype act, cudaStream_t s);
 size_t scan_workspace_bytes(int T_total);
 cudaError_t launch_prefill_scan(const gdn_params *, const void *, const void *, const void *, const void *,
                                 const int32_t *, int, int, const void *, void *, const float *, float *,
@@ -145,6 +147,18 @@ gdn_status gdn_decode_multi(const gdn_params *p, const void *qkv, const void *z,
     cudaError_t e = launch_decode_multi(p, qkv, z, alpha, beta, conv_state, ssm_state, out, B, T, act, out_dt,
                                         (cudaStream_t)stream);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_decode_multi");
+}
+
+gdn_status gdn_in_proj(const void *h, const void *w_in, void *qkv, void *z, void *alpha, void *beta, int M,
+                       gdn_dtype act, void *stream)
+{
+    if (!ok_dtype(act)) return fail(GDN_ERR_INVALID_ARG, "unknown activation dtype");
+    if (M < 0 || M > (1 << 24)) return fail(GDN_ERR_INVALID_ARG, "M out of range [0, 2^24]");
+    if (M == 0) return GDN_OK;
+    if (!ok_ptr(h) || !ok_ptr(w_in) || !ok_ptr(qkv) || !ok_ptr(z) || !ok_ptr(alpha) || !ok_ptr(beta))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    cudaError_t e = launch_in_proj(h, w_in, qkv, z, alpha, beta, M, act, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_in_proj");
 }
 
 gdn_status gdn_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, void *stream)

@@ -1,11 +1,17 @@
-// gdn_gemm.cu -- the ssm_out projection on 5th-generation tensor cores:
-// y[m][n] = sum_k x[m][k] w[n][k], with x the gated mixer output [M][4096] and w
-// the layer's ssm_out.weight [2048][4096], both bf16, accumulated in fp32.
-// The step is "cur = ssm_out . gated" of "qwen35moe -- Forward-Pass Design
-// (Pantheon port)", section "Output path" (projection 4096 -> n_embd 2048).
+// gdn_gemm.cu -- the dense projections around the mixer on 5th-generation
+// tensor cores: y[m][n] = sum_k x[m][k] w[n][k], bf16 operands, fp32
+// accumulation. Both are in "qwen35moe -- Forward-Pass Design (Pantheon port)",
+// section "SSM block -- Gated-Delta-Net":
+//  - the input projections (from the normed x, K = n_embd 2048): attn_qkv ->
+//    qkv [8192], attn_gate -> z [4096], ssm_alpha -> alpha [32], ssm_beta -> beta
+//    [32], computed as one GEMM over the stacked weight [12352][2048], whose
+//    epilogue writes each column range to its own array;
+//  - the output projection "cur = ssm_out . gated" (section "Output path"),
+//    4096 -> 2048.
 //
-// Design. A persistent grid walks output tiles of 128 rows x 256 columns. Per
-// CTA:
+// Design. A persistent grid walks output tiles of 128 rows x 256 columns (the
+// last column tile may be partial: weight rows past N read as zero and their
+// columns are not stored). Per CTA:
 //  - warp 0, lane 0: the TMA producer. 2-D tensor-map copies bring 64-wide K
 //    slices of x (128 x 64) and w (256 x 64) into a ring of four shared-memory
 //    stages in the 128-byte-swizzle layout the tensor core reads directly.
@@ -14,8 +20,9 @@
 //    accumulators in tensor memory; commits release the stage, and after the
 //    last slice, the accumulator.
 //  - warps 2..5: the epilogue. Each thread owns one accumulator row (its TMEM
-//    lane) and writes its 256 outputs, while the MMA warp already fills the
-//    other accumulator with the next tile.
+//    lane) and writes its outputs 32 columns at a time to the array that owns
+//    those columns, while the MMA warp already fills the other accumulator with
+//    the next tile.
 // All waits are bounded; a wait that gives up records GDN_ERR_TIMEOUT.
 #include <cuda.h>
 
@@ -28,15 +35,21 @@ namespace gdn {
 __device__ unsigned int g_gemm_error;   // GDN_ERR_TIMEOUT if a bounded wait gave up
 
 constexpr int GM_BM = 128, GM_BN = 256, GM_BK = 64, GM_STAGES = 4;
-constexpr int GM_K = DI;                          // 4096
-constexpr int GM_N = GDN_HIDDEN;                  // 2048
-constexpr int GM_KB = GM_K / GM_BK;               // K slices per tile
 constexpr uint32_t GM_A_BYTES = GM_BM * GM_BK * 2;        // 16 KiB
 constexpr uint32_t GM_B_BYTES = GM_BN * GM_BK * 2;        // 32 KiB
 constexpr uint32_t GM_STAGE_BYTES = GM_A_BYTES + GM_B_BYTES;
 constexpr int GM_THREADS = 192;                   // TMA warp, MMA warp, 4 epilogue warps
 constexpr uint32_t GM_TMEM_COLS = 2 * GM_BN;      // two accumulators
-static_assert(GM_N % GM_BN == 0 && GM_K % GM_BK == 0, "tile shape");
+
+// Where the GEMM's output columns go: columns [c0[s], c0[s+1]) are written to
+// ptr[s] as rows of ld[s] elements (column c lands at ptr[s][m * ld[s] + c - c0[s]]).
+// Every boundary is a multiple of 32, so a 32-column chunk has one owner.
+struct ProjOut {
+    void *ptr[4];
+    int c0[5];
+    int ld[4];
+    int nseg;
+};
 
 struct GemmSmem {
     alignas(1024) unsigned char stage[GM_STAGES][GM_STAGE_BYTES];   // A tile | B tile, 1024-byte aligned
@@ -57,16 +70,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 }
 
 template <typename TO>
-__global__ void __launch_bounds__(GM_THREADS, 1) out_proj_kernel(const __grid_constant__ CUtensorMap mx,
-                                                                 const __grid_constant__ CUtensorMap mw,
-                                                                 TO *__restrict__ y, int M)
+__global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_constant__ CUtensorMap mx,
+                                                             const __grid_constant__ CUtensorMap mw,
+                                                             const ProjOut out, int M, int N, int K)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *blk = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     GemmSmem &sm = *reinterpret_cast<GemmSmem *>(blk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n_tiles = GM_N / GM_BN;
+    const int n_tiles = (N + GM_BN - 1) / GM_BN;
     const int n_work = ((M + GM_BM - 1) / GM_BM) * n_tiles;
+    const int kbn = K / GM_BK;                         // K slices per tile
     const volatile int &aborted = sm.abort;
 
     if (warp == 1) {
@@ -97,7 +111,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) out_proj_kernel(const __grid_co
             int it = 0;                                // K slices issued so far, over all tiles
             for (int w = blockIdx.x; w < n_work && !aborted; w += gridDim.x) {
                 const int mt = w / n_tiles, nt = w % n_tiles;
-                for (int kb = 0; kb < GM_KB; ++kb, ++it) {
+                for (int kb = 0; kb < kbn; ++kb, ++it) {
                     const int s = it % GM_STAGES;
                     if (it >= GM_STAGES &&
                         !mbar_wait_bounded(smem_u32(&sm.empty[s]), (uint32_t)((it / GM_STAGES - 1) & 1)))
@@ -126,7 +140,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) out_proj_kernel(const __grid_co
                     sm.abort = 1;
                 tc::fence_after_sync();
                 const uint32_t d = tm + (uint32_t)(GM_BN * ab);
-                for (int kb = 0; kb < GM_KB; ++kb, ++it) {
+                for (int kb = 0; kb < kbn; ++kb, ++it) {
                     const int s = it % GM_STAGES;
                     if (!mbar_wait_bounded(smem_u32(&sm.full[s]), (uint32_t)((it / GM_STAGES) & 1))) sm.abort = 1;
                     if (aborted) break;
@@ -154,7 +168,6 @@ __global__ void __launch_bounds__(GM_THREADS, 1) out_proj_kernel(const __grid_co
             if (aborted) break;
             tc::fence_after_sync();
             const int m = mt * GM_BM + row;
-            TO *dst = y + (size_t)m * GM_N + (size_t)nt * GM_BN;
 #pragma unroll 2
             for (int c = 0; c < GM_BN; c += 32) {
                 float v[32];
@@ -162,16 +175,20 @@ __global__ void __launch_bounds__(GM_THREADS, 1) out_proj_kernel(const __grid_co
                 tc::tmem_ld16(tc::tmem_addr(tm + (uint32_t)(GM_BN * ab), 32 * q, c + 16),
                               *reinterpret_cast<float(*)[16]>(v + 16));
                 tc::wait_ld();
-                if (m < M) {
+                const int n = nt * GM_BN + c;          // first output column of this chunk
+                int sg = 0;
+                while (sg + 1 < out.nseg && n >= out.c0[sg + 1]) ++sg;
+                TO *dst = static_cast<TO *>(out.ptr[sg]) + (size_t)m * out.ld[sg] + (n - out.c0[sg]);
+                if (m < M && n < N) {
                     if (sizeof(TO) == 4) {
-                        float4 *d4 = reinterpret_cast<float4 *>(dst + c);
+                        float4 *d4 = reinterpret_cast<float4 *>(dst);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) d4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                     } else {
                         __align__(16) bf16 o[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = from_f<bf16>(v[e]);
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) d4[e] = reinterpret_cast<const uint4 *>(o)[e];
                     }
@@ -210,14 +227,14 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Row-major bf16 matrix [rows][4096] read in boxes of 64 columns x box_rows rows,
+// Row-major bf16 matrix [rows][K] read in boxes of 64 columns x box_rows rows,
 // 128-byte swizzle; rows past the end read as zero.
-static bool make_map(CUtensorMap *map, const void *base, int rows, int box_rows)
+static bool make_map(CUtensorMap *map, const void *base, int rows, int K, int box_rows)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)GM_K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)GM_K * 2};
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)GM_BK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
@@ -227,24 +244,50 @@ static bool make_map(CUtensorMap *map, const void *base, int rows, int box_rows)
 
 int sm_count();
 
-cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s)
+// y[M][N] = x[M][K] w[N][K]^T with the output columns routed by `out`.
+static cudaError_t launch_proj(const void *x, const void *w, const ProjOut &out, int M, int N, int K,
+                               gdn_dtype out_dt, cudaStream_t s)
 {
     if (M <= 0) return cudaSuccess;
     CUtensorMap mx, mw;
-    if (!make_map(&mx, x, M, GM_BM) || !make_map(&mw, w, GM_N, GM_BN)) return cudaErrorInvalidValue;
-    const int n_work = ((M + GM_BM - 1) / GM_BM) * (GM_N / GM_BN);
+    if (!make_map(&mx, x, M, K, GM_BM) || !make_map(&mw, w, N, K, GM_BN)) return cudaErrorInvalidValue;
+    const int n_work = ((M + GM_BM - 1) / GM_BM) * ((N + GM_BN - 1) / GM_BN);
     const int n_sm = sm_count();
     if (n_sm <= 0) return cudaErrorInvalidDevice;
     const int grid = n_work < n_sm ? n_work : n_sm;
     cudaError_t e;
     if (out_dt == GDN_F32) {
-        e = cudaFuncSetAttribute(out_proj_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
-        if (e == cudaSuccess) out_proj_kernel<float><<<grid, GM_THREADS, GM_SMEM, s>>>(mx, mw, (float *)y, M);
+        e = cudaFuncSetAttribute(proj_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+        if (e == cudaSuccess) proj_kernel<float><<<grid, GM_THREADS, GM_SMEM, s>>>(mx, mw, out, M, N, K);
     } else {
-        e = cudaFuncSetAttribute(out_proj_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
-        if (e == cudaSuccess) out_proj_kernel<bf16><<<grid, GM_THREADS, GM_SMEM, s>>>(mx, mw, (bf16 *)y, M);
+        e = cudaFuncSetAttribute(proj_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
+        if (e == cudaSuccess) proj_kernel<bf16><<<grid, GM_THREADS, GM_SMEM, s>>>(mx, mw, out, M, N, K);
     }
     return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s)
+{
+    ProjOut o = {};
+    o.ptr[0] = y;
+    o.c0[0] = 0;
+    o.c0[1] = GDN_HIDDEN;
+    o.ld[0] = GDN_HIDDEN;
+    o.nseg = 1;
+    return launch_proj(x, w, o, M, GDN_HIDDEN, DI, out_dt, s);
+}
+
+// The input projections: columns 0..8191 -> qkv, 8192..12287 -> z,
+// 12288..12319 -> alpha, 12320..12351 -> beta.
+cudaError_t launch_in_proj(const void *h, const void *w_in, void *qkv, void *z, void *alpha, void *beta, int M,
+                           gdn_dtype act, cudaStream_t s)
+{
+    ProjOut o = {};
+    o.ptr[0] = qkv; o.ptr[1] = z; o.ptr[2] = alpha; o.ptr[3] = beta;
+    o.c0[0] = 0; o.c0[1] = CC; o.c0[2] = CC + DI; o.c0[3] = CC + DI + HV; o.c0[4] = CC + DI + 2 * HV;
+    o.ld[0] = CC; o.ld[1] = DI; o.ld[2] = HV; o.ld[3] = HV;
+    o.nseg = 4;
+    return launch_proj(h, w_in, o, M, CC + DI + 2 * HV, GDN_HIDDEN, act, s);
 }
 
 // Reads and clears this file's device error word (synchronous on `s`).

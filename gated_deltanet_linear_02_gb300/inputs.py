@@ -115,6 +115,16 @@ def out_proj_weight(seed: int, act_dtype=torch.bfloat16, device="cpu") -> torch.
     return (torch.randn(N_EMBD, D_INNER, generator=g, device=device) / 64.0).to(act_dtype)
 
 
+def in_proj_weights(seed: int, act_dtype=torch.bfloat16, device="cpu"):
+    """(attn_qkv [8192][2048], attn_gate [4096][2048], ssm_alpha [32][2048],
+    ssm_beta [32][2048]) ~ N(0, 1/2048) (variance), so the projected streams are
+    ~N(0, 1) like the synthetic streams; rounded once to the activation dtype."""
+    g = _gen(seed + 850_000, device)
+    sd = 1.0 / math.sqrt(N_EMBD)
+    return tuple((torch.randn(r, N_EMBD, generator=g, device=device) * sd).to(act_dtype)
+                 for r in (C_CONV, D_INNER, HV, HV))
+
+
 def varlen_lengths(seed: int, n: int = 8, lo: int = 256, hi: int = 32768) -> list[int]:
     """Sequence lengths drawn log-uniformly in [lo, hi] and rounded."""
     g = _gen(seed + 700_000, "cpu")

@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_decode_step.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 7 + [_int, _int, _int, _vp]
         L.gdn_decode_multi.restype = _int
         L.gdn_decode_multi.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 7 + [_int, _int, _int, _int, _vp]
+        L.gdn_in_proj.restype = _int
+        L.gdn_in_proj.argtypes = [_vp] * 6 + [_int, _int, _vp]
         L.gdn_out_proj.restype = _int
         L.gdn_out_proj.argtypes = [_vp, _vp, _vp, _int, _int, _vp]
         L.gdn_prefill.restype = _int
@@ -183,6 +185,23 @@ def decode_multi(params, qkv, z, alpha, beta, conv_state, ssm_state, out, stream
                                 _ptr(ssm_state, "ssm_state", (B, HV, DV, DK), torch.float32),
                                 _ptr(out, "out", (B, T, DI)), B, T, act, od, _stream(stream))
     _check(st, "gdn_decode_multi")
+
+
+IN_PROJ_ROWS = CC + DI + 2 * HV   # GDN_IN_PROJ_ROWS
+
+
+def in_proj(h, w_in, qkv, z, alpha, beta, stream=None):
+    """gdn_in_proj: the four input projections of the normed hidden states h
+    [M][2048] (bf16) through the stacked weight w_in [12352][2048] (bf16), into
+    qkv [M][8192], z [M][4096], alpha [M][32], beta [M][32] (fp32 or bf16)."""
+    M = h.shape[0]
+    act = _act_dtype(qkv)
+    dt = qkv.dtype
+    st = lib().gdn_in_proj(_ptr(h, "h", (M, N_EMBD), torch.bfloat16),
+                           _ptr(w_in, "w_in", (IN_PROJ_ROWS, N_EMBD), torch.bfloat16),
+                           _ptr(qkv, "qkv", (M, CC)), _ptr(z, "z", (M, DI), dt), _ptr(alpha, "alpha", (M, HV), dt),
+                           _ptr(beta, "beta", (M, HV), dt), M, act, _stream(stream))
+    _check(st, "gdn_in_proj")
 
 
 def out_proj(x, w, y, stream=None):

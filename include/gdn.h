@@ -54,7 +54,8 @@ extern "C" {
 #define GDN_CONV_CHANNELS 8192
 #define GDN_D_INNER 4096
 #define GDN_DECODE_MAX_T 8   /* tokens per sequence of gdn_decode_multi, at most */
-#define GDN_HIDDEN 2048      /* n_embd: the output width of the ssm_out projection */
+#define GDN_HIDDEN 2048      /* n_embd: the model width (in_proj input, ssm_out output) */
+#define GDN_IN_PROJ_ROWS 12352   /* stacked input-projection weight rows: 8192 + 4096 + 32 + 32 */
 
 typedef enum {
     GDN_OK = 0,
@@ -208,6 +209,24 @@ gdn_status gdn_prefill_static(const gdn_params *p, const void *qkv, const void *
                               const void *conv_state_in, void *conv_state_out,
                               const float *ssm_state_in, float *ssm_state_out, void *out,
                               gdn_dtype act, gdn_dtype out_dt, int chunk_size, void *stream);
+
+/*
+ * gdn_in_proj -- the four input projections of section "SSM block --
+ * Gated-Delta-Net", from the normed hidden state: attn_qkv -> qkv [8192],
+ * attn_gate -> z [4096], ssm_alpha -> alpha [32], ssm_beta -> beta [32]. They
+ * run as one tensor-core GEMM (bf16 operands, fp32 accumulation) over the four
+ * weights stacked by rows; the epilogue writes each column range to its own
+ * array, laid out as gdn_prefill and gdn_decode_step take them.
+ *   h      [M][2048] bf16, row-major: attn_norm'd hidden states
+ *   w_in   [12352][2048] bf16, row-major: attn_qkv.weight (rows 0..8191),
+ *          attn_gate.weight (8192..12287), ssm_alpha.weight (12288..12319),
+ *          ssm_beta.weight (12320..12351)
+ *   qkv [M][8192], z [M][4096], alpha [M][32], beta [M][32] in dtype act
+ * 0 <= M <= 2^24 (M == 0 is a no-op). Errors: GDN_ERR_INVALID_ARG, GDN_ERR_CUDA
+ * (also when the driver's tensor-map encoder is unavailable).
+ */
+gdn_status gdn_in_proj(const void *h, const void *w_in, void *qkv, void *z, void *alpha, void *beta, int M,
+                       gdn_dtype act, void *stream);
 
 /*
  * gdn_out_proj -- the projection right after the mixer, section "Output path":

@@ -177,6 +177,15 @@ def delta_rule_chunked(q, k, v, g, b, S0, scale, chunk):
 
 # --------------------------------------------------------------- whole mixer
 
+def in_proj(h, w_qkv, w_gate, w_alpha, w_beta):
+    """The four input projections of section "SSM block -- Gated-Delta-Net",
+    each from the normed hidden states h [M][n_embd]: attn_qkv -> qkv,
+    attn_gate -> z, ssm_alpha -> alpha, ssm_beta -> beta. Each weight holds one
+    row per output feature. Returns (qkv, z, alpha, beta) in fp64."""
+    h = _f64(h)
+    return tuple(h @ _f64(w).T for w in (w_qkv, w_gate, w_alpha, w_beta))
+
+
 def out_proj(x, w):
     """The projection after the mixer, section "Output path": cur = ssm_out .
     gated, 4096 -> n_embd. With x [M][K] (the gated output rows) and w [N][K]

@@ -127,6 +127,19 @@ def test_decode_multi_argument_checks(ops):
         assert call(p, bad, 4, 2) == ops.GDN_ERR_INVALID_ARG
 
 
+def test_in_proj_argument_checks(ops):
+    L = ops.lib()
+    assert L.gdn_in_proj(*([FAKE] * 6), 0, ops.GDN_BF16, None) == ops.GDN_OK      # empty: no-op
+    assert L.gdn_in_proj(*([FAKE] * 6), -1, ops.GDN_BF16, None) == ops.GDN_ERR_INVALID_ARG
+    assert L.gdn_in_proj(*([FAKE] * 6), 4, 3, None) == ops.GDN_ERR_INVALID_ARG
+    for i in range(6):
+        args = [FAKE] * 6
+        args[i] = 0
+        assert L.gdn_in_proj(*args, 4, ops.GDN_BF16, None) == ops.GDN_ERR_INVALID_ARG
+        args[i] = MIS
+        assert L.gdn_in_proj(*args, 4, ops.GDN_BF16, None) == ops.GDN_ERR_INVALID_ARG
+
+
 def test_out_proj_argument_checks(ops):
     L = ops.lib()
     assert L.gdn_out_proj(FAKE, FAKE, FAKE, 0, ops.GDN_BF16, None) == ops.GDN_OK      # empty: no-op

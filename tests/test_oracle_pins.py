@@ -413,3 +413,25 @@ def test_out_proj_rows_independent_and_linear(orc):
     y2 = orc.out_proj(2.0 * x[2:3], w)
     np.testing.assert_allclose(y2[0], 2.0 * y[2], rtol=1e-12, atol=1e-12)
 
+
+def test_in_proj_streams_and_order(orc):
+    """Each stream comes from its own weight, in the page's order; the first
+    n_embd rows of an identity-block attn_qkv weight copy h into qkv."""
+    rng = np.random.default_rng(14)
+    h = rng.standard_normal((3, 2048))
+    w_qkv = np.zeros((8192, 2048))
+    w_qkv[:2048] = np.eye(2048)
+    w_gate = np.zeros((4096, 2048))
+    w_gate[5, 7] = 2.0                      # z[:, 5] = 2 h[:, 7]
+    w_alpha = np.zeros((32, 2048))
+    w_alpha[0, 0] = 1.0
+    w_beta = np.zeros((32, 2048))
+    w_beta[31, 2047] = -1.0
+    qkv, z, al, be = orc.in_proj(h, w_qkv, w_gate, w_alpha, w_beta)
+    assert qkv.shape == (3, 8192) and z.shape == (3, 4096) and al.shape == (3, 32) and be.shape == (3, 32)
+    np.testing.assert_array_equal(qkv[:, :2048], h)
+    assert not qkv[:, 2048:].any()
+    np.testing.assert_array_equal(z[:, 5], 2.0 * h[:, 7])
+    np.testing.assert_array_equal(al[:, 0], h[:, 0])
+    np.testing.assert_array_equal(be[:, 31], -h[:, 2047])
+
