@@ -23,8 +23,16 @@
 //    lane) and writes its outputs 32 columns at a time to the array that owns
 //    those columns, while the MMA warp already fills the other accumulator with
 //    the next tile.
-// All waits are bounded; a wait that gives up records GDN_ERR_TIMEOUT.
+// Split K. When the tiles are too few to fill the GPU (a decode batch), each
+// tile's K range is split S ways (S = 2, 4 or 8) over the S CTAs of a
+// cluster, one tile per CTA. Each CTA stages its fp32 partial tile in the
+// shared memory its stages no longer need; after a cluster barrier, CTA r sums
+// rows [r 128/S, (r+1) 128/S) over all S partials through distributed shared
+// memory and writes them.
+// All mbarrier waits are bounded; a wait that gives up records GDN_ERR_TIMEOUT.
 #include <cuda.h>
+
+#include <mutex>
 
 #include "gdn_async.cuh"
 #include "gdn_common.cuh"
@@ -40,6 +48,8 @@ constexpr uint32_t GM_B_BYTES = GM_BN * GM_BK * 2;        // 32 KiB
 constexpr uint32_t GM_STAGE_BYTES = GM_A_BYTES + GM_B_BYTES;
 constexpr int GM_THREADS = 192;                   // TMA warp, MMA warp, 4 epilogue warps
 constexpr uint32_t GM_TMEM_COLS = 2 * GM_BN;      // two accumulators
+constexpr int GM_PART_LD = GM_BN + 4;             // fp32 partial row stride (floats): rows fall on other banks
+static_assert(GM_BM * GM_PART_LD * 4 <= GM_STAGES * GM_STAGE_BYTES, "split-K partial fits the stages");
 
 // Where the GEMM's output columns go: columns [c0[s], c0[s+1]) are written to
 // ptr[s] as rows of ld[s] elements (column c lands at ptr[s][m * ld[s] + c - c0[s]]).
@@ -72,15 +82,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 template <typename TO>
 __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_constant__ CUtensorMap mx,
                                                              const __grid_constant__ CUtensorMap mw,
-                                                             const ProjOut out, int M, int N, int K)
+                                                             const ProjOut out, int M, int N, int K, int splits)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *blk = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     GemmSmem &sm = *reinterpret_cast<GemmSmem *>(blk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_tiles = (N + GM_BN - 1) / GM_BN;
-    const int n_work = ((M + GM_BM - 1) / GM_BM) * n_tiles;
-    const int kbn = K / GM_BK;                         // K slices per tile
+    // persistent mode: CTAs stride over the tiles with all K slices each;
+    // split mode: CTA = (tile blockIdx.x / splits, K split blockIdx.x % splits)
+    const bool split = splits > 1;
+    const int n_work = split ? 1 : ((M + GM_BM - 1) / GM_BM) * n_tiles;
+    const int w0 = split ? (int)blockIdx.x / splits : (int)blockIdx.x;
+    const int wstep = split ? 1 : (int)gridDim.x;
+    const int wend = split ? w0 + 1 : n_work;
+    const int kbn = K / GM_BK / splits;                // K slices per work item
+    const int kb0 = split ? ((int)blockIdx.x % splits) * kbn : 0;
     const volatile int &aborted = sm.abort;
 
     if (warp == 1) {
@@ -109,9 +126,9 @@ __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_consta
         // ---- TMA producer
         if (lane == 0) {
             int it = 0;                                // K slices issued so far, over all tiles
-            for (int w = blockIdx.x; w < n_work && !aborted; w += gridDim.x) {
+            for (int w = w0; w < wend && !aborted; w += wstep) {
                 const int mt = w / n_tiles, nt = w % n_tiles;
-                for (int kb = 0; kb < kbn; ++kb, ++it) {
+                for (int kb = kb0; kb < kb0 + kbn; ++kb, ++it) {
                     const int s = it % GM_STAGES;
                     if (it >= GM_STAGES &&
                         !mbar_wait_bounded(smem_u32(&sm.empty[s]), (uint32_t)((it / GM_STAGES - 1) & 1)))
@@ -134,7 +151,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_consta
         if (lane == 0) {
             const uint32_t idesc = tc::instr_desc(tc::FMT_BF16, GM_BM, GM_BN);
             int it = 0, ti = 0;
-            for (int w = blockIdx.x; w < n_work && !aborted; w += gridDim.x, ++ti) {
+            for (int w = w0; w < wend && !aborted; w += wstep, ++ti) {
                 const int ab = ti & 1;
                 if (ti >= 2 && !mbar_wait_bounded(smem_u32(&sm.acc_empty[ab]), (uint32_t)(((ti >> 1) - 1) & 1)))
                     sm.abort = 1;
@@ -161,7 +178,22 @@ __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_consta
         const int q = warp & 3;
         const int row = 32 * q + lane;
         int ti = 0;
-        for (int w = blockIdx.x; w < n_work; w += gridDim.x, ++ti) {
+        if (split) {                                   // stage this CTA's fp32 partial tile in shared memory
+            if (!mbar_wait_bounded(smem_u32(&sm.acc_full[0]), 0)) sm.abort = 1;
+            tc::fence_after_sync();
+            float *part = reinterpret_cast<float *>(sm.stage[0]) + row * GM_PART_LD;
+            for (int c = 0; c < GM_BN; c += 64) {      // four TMEM loads per wait
+                float v[64];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, c + 16 * k), *reinterpret_cast<float(*)[16]>(v + 16 * k));
+                tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    reinterpret_cast<float4 *>(part + c)[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            }
+        }
+        for (int w = w0; w < wend && !split; w += wstep, ++ti) {
             const int ab = ti & 1;
             const int mt = w / n_tiles, nt = w % n_tiles;
             if (!mbar_wait_bounded(smem_u32(&sm.acc_full[ab]), (uint32_t)((ti >> 1) & 1))) sm.abort = 1;
@@ -197,6 +229,45 @@ __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_consta
             tc::fence_before_sync();
             mbar_arrive(smem_u32(&sm.acc_empty[ab]));  // the MMA warp may refill this accumulator
         }
+    }
+    if (split) {
+        // ---- the cluster's reduction: CTA r writes rows [r 128/S, (r+1) 128/S) of
+        //      the tile, each the sum of the S partials
+        cluster_sync_all();                            // every partial of the cluster is staged
+        if (warp >= 2 && !aborted) {
+            const int t = tid - 64;                    // 0..127
+            const int rows = GM_BM / splits, r0 = ((int)blockIdx.x % splits) * rows;
+            const int mt = w0 / n_tiles, nt = w0 % n_tiles;
+            const uint32_t pbase = smem_u32(sm.stage[0]);
+            for (int f = t; f < rows * (GM_BN / 4); f += 128) {
+                const int rr = r0 + f / (GM_BN / 4), col = 4 * (f % (GM_BN / 4));
+                const uint32_t off = pbase + (uint32_t)((rr * GM_PART_LD + col) * 4);
+                float4 p4[8];                          // all S remote loads in flight before the sum
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r < splits) p4[r] = ld_cluster_f32x4(mapa_shared(off, (uint32_t)r));
+                float4 acc = p4[0];
+#pragma unroll
+                for (int r = 1; r < 8; ++r)
+                    if (r < splits) {
+                        acc.x += p4[r].x; acc.y += p4[r].y; acc.z += p4[r].z; acc.w += p4[r].w;
+                    }
+                const int m = mt * GM_BM + rr, n = nt * GM_BN + col;
+                if (m < M && n < N) {
+                    int sg = 0;
+                    while (sg + 1 < out.nseg && n >= out.c0[sg + 1]) ++sg;
+                    TO *dst = static_cast<TO *>(out.ptr[sg]) + (size_t)m * out.ld[sg] + (n - out.c0[sg]);
+                    if (sizeof(TO) == 4) {
+                        *reinterpret_cast<float4 *>(dst) = acc;
+                    } else {
+                        __align__(8) bf16 o4[4] = {from_f<bf16>(acc.x), from_f<bf16>(acc.y), from_f<bf16>(acc.z),
+                                                   from_f<bf16>(acc.w)};
+                        *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<const uint2 *>(o4);
+                    }
+                }
+            }
+        }
+        cluster_sync_all();                            // no CTA leaves while others read its partial
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -244,6 +315,51 @@ static bool make_map(CUtensorMap *map, const void *base, int rows, int K, int bo
 
 int sm_count();
 
+// Per-device set-up of the projection kernels, done once: the shared-memory
+// attribute, and how many clusters of 2, 4 and 8 CTAs can be resident at once.
+struct ProjDevice {
+    int max_clusters[3];
+};
+
+static const ProjDevice *proj_device()
+{
+    static ProjDevice dev_info[64];
+    static bool ready[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+        if (cudaFuncSetAttribute(proj_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(proj_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM) !=
+                cudaSuccess)
+            return nullptr;
+        for (int k = 0; k < 3; ++k) {
+            const int cs = 2 << k;
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(cs);
+            q.blockDim = dim3(GM_THREADS);
+            q.dynamicSmemBytes = GM_SMEM;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = (unsigned)cs;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, proj_kernel<bf16>, &q) != cudaSuccess) {
+                cudaGetLastError();                    // a refused query: never split this far
+                n = 0;
+            }
+            dev_info[dev].max_clusters[k] = n;
+        }
+        ready[dev] = true;
+    }
+    return &dev_info[dev];
+}
+
 // y[M][N] = x[M][K] w[N][K]^T with the output columns routed by `out`.
 static cudaError_t launch_proj(const void *x, const void *w, const ProjOut &out, int M, int N, int K,
                                gdn_dtype out_dt, cudaStream_t s)
@@ -254,16 +370,29 @@ static cudaError_t launch_proj(const void *x, const void *w, const ProjOut &out,
     const int n_work = ((M + GM_BM - 1) / GM_BM) * ((N + GM_BN - 1) / GM_BN);
     const int n_sm = sm_count();
     if (n_sm <= 0) return cudaErrorInvalidDevice;
-    const int grid = n_work < n_sm ? n_work : n_sm;
-    cudaError_t e;
-    if (out_dt == GDN_F32) {
-        e = cudaFuncSetAttribute(proj_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
-        if (e == cudaSuccess) proj_kernel<float><<<grid, GM_THREADS, GM_SMEM, s>>>(mx, mw, out, M, N, K);
-    } else {
-        e = cudaFuncSetAttribute(proj_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM);
-        if (e == cudaSuccess) proj_kernel<bf16><<<grid, GM_THREADS, GM_SMEM, s>>>(mx, mw, out, M, N, K);
-    }
-    return e == cudaSuccess ? cudaGetLastError() : e;
+    const ProjDevice *pd = proj_device();
+    if (!pd) return cudaErrorInvalidDevice;
+    // Split K (2, 4 or 8 ways) while the tiles fill less than half of the SMs,
+    // and only as far as every cluster of that size can be resident at once:
+    // a cluster that waits for another to finish costs a whole tile's time.
+    int splits = 1;
+    while (splits < 8 && n_work * splits * 2 <= n_sm && (K / GM_BK) % (splits * 2) == 0 &&
+           pd->max_clusters[splits == 1 ? 0 : splits == 2 ? 1 : 2] >= n_work)
+        splits *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits > 1 ? n_work * splits : (n_work < n_sm ? n_work : n_sm));
+    cfg.blockDim = dim3(GM_THREADS);
+    cfg.dynamicSmemBytes = GM_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = splits > 1 ? 1 : 0;
+    return out_dt == GDN_F32 ? cudaLaunchKernelEx(&cfg, proj_kernel<float>, mx, mw, out, M, N, K, splits)
+                             : cudaLaunchKernelEx(&cfg, proj_kernel<bf16>, mx, mw, out, M, N, K, splits);
 }
 
 cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s)
