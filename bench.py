@@ -406,7 +406,8 @@ def profile_case(args):
     """A small, self-contained run of one path for profilers: no JSON line, no
     clocks, a few launches on a few GB. ``--case decode``: --layers layers of
     gdn_decode_step on --batch sequences; ``--case prefill``: gdn_prefill on one
-    sequence of --T tokens."""
+    sequence of --T tokens; ``--case out_proj`` / ``--case in_proj``: the
+    projection GEMMs on --T rows."""
     import torch
 
     from gated_deltanet_linear_02_gb300 import build as gbuild
@@ -427,6 +428,20 @@ def profile_case(args):
         for _ in range(n):
             for cp, conv, S, st, out in Ls:
                 ops.decode_step(None, st.qkv[0], st.z[0], st.alpha[0], st.beta[0], conv, S, out, cparams=cp)
+    elif args.case == "out_proj":
+        w = I.out_proj_weight(I.seed_of(2), device=dev)
+        x = torch.randn(args.T, I.D_INNER, device=dev).to(torch.bfloat16)
+        y = torch.empty(args.T, I.N_EMBD, dtype=torch.bfloat16, device=dev)
+        for _ in range(n):
+            ops.out_proj(x, w, y)
+        assert ops.device_error() == ops.GDN_OK
+    elif args.case == "in_proj":
+        w_in = torch.cat(I.in_proj_weights(I.seed_of(2), device=dev), dim=0)
+        h = torch.randn(args.T, I.N_EMBD, device=dev).to(torch.bfloat16)
+        outs = [torch.empty(args.T, m, dtype=torch.bfloat16, device=dev) for m in (I.C_CONV, I.D_INNER, I.HV, I.HV)]
+        for _ in range(n):
+            ops.in_proj(h, w_in, *outs)
+        assert ops.device_error() == ops.GDN_OK
     else:
         seed = I.seed_of(2)
         lp = I.layer_params(seed).to(dev)
@@ -451,7 +466,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--case", choices=["decode", "prefill", "out_proj", "in_proj"], default=None,
                     help="profiling run of one path (see profile_case); prints no JSON line")
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--layers", type=int, default=1)
