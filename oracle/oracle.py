@@ -197,6 +197,38 @@ def out_proj(x, w):
     return x @ w.T
 
 
+ATTN_Q_HEADS, ATTN_KV_HEADS, ATTN_HEAD_DIM = 16, 2, 256   # "Config (mini)" / "Full-attention block"
+
+
+def attn_decode(q, k_cache, v_cache, ctx_len, z):
+    """Decode attention of the full-attention layers, steps 5-6 of section
+    "Full-attention block": every query head h of sequence b attends over the
+    first ctx_len[b] cached positions of KV head h // (16 / 2) (GQA: 8 query
+    heads share one KV head), with scale 1/sqrt(head_dim); then the output gate
+    cur = attn_out * sigmoid(z). q and z are [B][16][256] (q after its RMSNorm
+    and RoPE), the caches [B][2][Lmax][256] (keys after theirs). An empty
+    context gives a zero output. fp64 over exact copies of the inputs; the
+    dot products are library matrix products."""
+    q, kc, vc, z = _f64(q), _f64(k_cache), _f64(v_cache), _f64(z)
+    B, Hq, D = q.shape
+    Hkv = kc.shape[1]
+    group = Hq // Hkv
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        L = int(ctx_len[b])
+        if L <= 0:
+            continue
+        for h in range(Hq):
+            g = h // group
+            K, V = kc[b, g, :L], vc[b, g, :L]
+            s = (K @ q[b, h]) / np.sqrt(D)          # scores of the L positions
+            p = np.exp(s - s.max())
+            p /= p.sum()                             # softmax
+            o = p @ V
+            out[b, h] = o / (1.0 + np.exp(-z[b, h]))   # o * sigmoid(z)
+    return out
+
+
 @dataclass
 class Params:
     """One layer's parameters as fp64 arrays (the page's tensor roles:
