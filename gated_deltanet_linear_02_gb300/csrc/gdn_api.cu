@@ -27,6 +27,11 @@ cudaError_t launch_prefill_chunked(const gdn_params *, const void *, const void 
                                    const int32_t *, int, int, const void *, void *, const float *, float *, void *,
                                    gdn_dtype, void *, cudaStream_t);
 cudaError_t take_chunk_error(unsigned int *word, cudaStream_t s);
+size_t attn_workspace_bytes(int B, int Lmax);
+cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
+                               const void *z, void *out, int B, int Lmax, void *ws, gdn_dtype out_dt,
+                               cudaStream_t s);
+cudaError_t take_attn_error(unsigned int *word, cudaStream_t s);
 }  // namespace gdn
 
 using namespace gdn;
@@ -172,6 +177,33 @@ gdn_status gdn_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype 
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_out_proj");
 }
 
+size_t gdn_attn_decode_workspace_size(int B, int Lmax)
+{
+    if (B < 1 || B > MAX_B || Lmax < 1 || (long long)B * GDN_ATTN_KV_HEADS * Lmax > (1ll << 30)) return 0;
+    return attn_workspace_bytes(B, Lmax);
+}
+
+gdn_status gdn_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
+                           const void *z, void *out, int B, int Lmax, void *workspace, size_t workspace_bytes,
+                           gdn_dtype out_dt, void *stream)
+{
+    if (!ok_dtype(out_dt)) return fail(GDN_ERR_INVALID_ARG, "unknown output dtype");
+    if (B < 0 || B > MAX_B) return fail(GDN_ERR_INVALID_ARG, "B out of range [0, 65535]");
+    if (B == 0) return GDN_OK;
+    if (Lmax < 1 || (long long)B * GDN_ATTN_KV_HEADS * Lmax > (1ll << 30))
+        return fail(GDN_ERR_INVALID_ARG, "Lmax out of range: need 1 <= Lmax and B * 2 * Lmax <= 2^30");
+    if (!ok_ptr(q) || !ok_ptr(k_cache) || !ok_ptr(v_cache) || !ok_ptr(z) || !ok_ptr(out))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    if (ctx_len == nullptr || (reinterpret_cast<uintptr_t>(ctx_len) & 3u) != 0)
+        return fail(GDN_ERR_INVALID_ARG, "ctx_len is NULL or not 4-byte aligned");
+    if (!ok_ptr(workspace)) return fail(GDN_ERR_WORKSPACE, "workspace is NULL or not 16-byte aligned");
+    if (workspace_bytes < attn_workspace_bytes(B, Lmax))
+        return fail(GDN_ERR_WORKSPACE, "workspace smaller than gdn_attn_decode_workspace_size(B, Lmax)");
+    cudaError_t e = launch_attn_decode(q, k_cache, v_cache, ctx_len, z, out, B, Lmax, workspace, out_dt,
+                                       (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_attn_decode");
+}
+
 size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_size)
 {
     if (N < 0 || N > MAX_N || T_total < 0 || T_total > MAX_T || !ok_dtype(act)) return 0;
@@ -230,12 +262,14 @@ gdn_status gdn_device_error(void *stream)
     unsigned int word2 = 0;
     unsigned int word3 = 0;
     unsigned int word4 = 0;
+    unsigned int word5 = 0;
     cudaError_t e = take_decode_error(&word, s);
     if (e == cudaSuccess) e = take_chunk_error(&word2, s);
     if (e == cudaSuccess) e = take_multi_error(&word3, s);
     if (e == cudaSuccess) e = take_gemm_error(&word4, s);
+    if (e == cudaSuccess) e = take_attn_error(&word5, s);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_error");
-    return (word | word2 | word3 | word4) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
+    return (word | word2 | word3 | word4 | word5) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
 }
 
 }  // extern "C"

@@ -37,6 +37,7 @@
 #include "gdn_async.cuh"
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
+#include "gdn_tma.cuh"
 
 namespace gdn {
 
@@ -50,6 +51,7 @@ constexpr int GM_THREADS = 192;                   // TMA warp, MMA warp, 4 epilo
 constexpr uint32_t GM_TMEM_COLS = 2 * GM_BN;      // two accumulators
 constexpr int GM_PART_LD = GM_BN + 4;             // fp32 partial row stride (floats): rows fall on other banks
 static_assert(GM_BM * GM_PART_LD * 4 <= GM_STAGES * GM_STAGE_BYTES, "split-K partial fits the stages");
+static_assert(GM_BK == 64, "K slices are the 64-column boxes of make_bf16_sw128_map");
 
 // Where the GEMM's output columns go: columns [c0[s], c0[s+1]) are written to
 // ptr[s] as rows of ld[s] elements (column c lands at ptr[s][m * ld[s] + c - c0[s]]).
@@ -70,14 +72,6 @@ struct GemmSmem {
     int abort;
 };
 constexpr size_t GM_SMEM = sizeof(GemmSmem) + 1024;   // + slack to align the block to 1024 bytes
-
-// 2-D tiled TMA load of the box at element coordinates (x = K, y = row).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-                 "[%0], [%1, {%2, %3}], [%4];"
-                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
-}
 
 template <typename TO>
 __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_constant__ CUtensorMap mx,
@@ -298,15 +292,15 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Row-major bf16 matrix [rows][K] read in boxes of 64 columns x box_rows rows,
-// 128-byte swizzle; rows past the end read as zero.
-static bool make_map(CUtensorMap *map, const void *base, int rows, int K, int box_rows)
+// Row-major bf16 matrix [rows][cols] read in boxes of 64 columns x box_rows
+// rows, 128-byte swizzle; elements past either end read as zero.
+bool make_bf16_sw128_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_rows)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)GM_BK, (cuuint32_t)box_rows};
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -366,7 +360,7 @@ static cudaError_t launch_proj(const void *x, const void *w, const ProjOut &out,
 {
     if (M <= 0) return cudaSuccess;
     CUtensorMap mx, mw;
-    if (!make_map(&mx, x, M, K, GM_BM) || !make_map(&mw, w, N, K, GM_BN)) return cudaErrorInvalidValue;
+    if (!make_bf16_sw128_map(&mx, x, M, K, GM_BM) || !make_bf16_sw128_map(&mw, w, N, K, GM_BN)) return cudaErrorInvalidValue;
     const int n_work = ((M + GM_BM - 1) / GM_BM) * ((N + GM_BN - 1) / GM_BN);
     const int n_sm = sm_count();
     if (n_sm <= 0) return cudaErrorInvalidDevice;

@@ -125,6 +125,41 @@ def in_proj_weights(seed: int, act_dtype=torch.bfloat16, device="cpu"):
                  for r in (C_CONV, D_INNER, HV, HV))
 
 
+ATTN_HQ, ATTN_HKV, ATTN_D = 16, 2, 256   # full-attention layers: 16 query / 2 KV heads, head_dim 256
+
+
+@dataclass
+class AttnInputs:
+    q: torch.Tensor          # [B][16][256] bf16
+    k_cache: torch.Tensor    # [B][2][Lmax][256] bf16
+    v_cache: torch.Tensor    # [B][2][Lmax][256] bf16
+    ctx_len: torch.Tensor    # [B] int32
+    z: torch.Tensor          # [B][16][256] bf16
+
+    def to(self, device) -> "AttnInputs":
+        return AttnInputs(*(t.to(device) for t in (self.q, self.k_cache, self.v_cache, self.ctx_len, self.z)))
+
+
+def attn_inputs(seed: int, B: int, Lmax: int, ctx_len=None, device="cpu") -> AttnInputs:
+    """One decode step of a full-attention layer. q and the cached keys come out
+    of per-head RMSNorms (unit RMS per head, then partial RoPE, a rotation), so
+    they are drawn N(0, 1) per element; values and the gate logits z too. Rows
+    at or past each sequence's ctx_len hold NaN, which the attention must
+    never let through. ctx_len defaults to Lmax for every sequence."""
+    g = _gen(seed + 900_000, device)
+    q = torch.randn(B, ATTN_HQ, ATTN_D, generator=g, device=device).to(torch.bfloat16)
+    k = torch.randn(B, ATTN_HKV, Lmax, ATTN_D, generator=g, device=device)
+    v = torch.randn(B, ATTN_HKV, Lmax, ATTN_D, generator=g, device=device)
+    z = torch.randn(B, ATTN_HQ, ATTN_D, generator=g, device=device).to(torch.bfloat16)
+    cl = torch.full((B,), Lmax, dtype=torch.int32) if ctx_len is None else \
+        torch.as_tensor(ctx_len, dtype=torch.int32).reshape(B)
+    pos = torch.arange(Lmax, device=device)
+    past = (pos[None, :] >= cl.to(device)[:, None])[:, None, :, None]
+    k = torch.where(past, torch.full_like(k, float("nan")), k)
+    v = torch.where(past, torch.full_like(v, float("nan")), v)
+    return AttnInputs(q, k.to(torch.bfloat16), v.to(torch.bfloat16), cl.to(device), z)
+
+
 def varlen_lengths(seed: int, n: int = 8, lo: int = 256, hi: int = 32768) -> list[int]:
     """Sequence lengths drawn log-uniformly in [lo, hi] and rounded."""
     g = _gen(seed + 700_000, "cpu")

@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_prefill_static.restype = _int
         L.gdn_prefill_static.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 5 + [_int, _int] + [_vp] * 5 + \
             [_int, _int, _int, _vp]
+        L.gdn_attn_decode.restype = _int
+        L.gdn_attn_decode.argtypes = [_vp] * 6 + [_int, _int, _vp, _sz, _int, _vp]
+        L.gdn_attn_decode_workspace_size.restype = _sz
+        L.gdn_attn_decode_workspace_size.argtypes = [_int, _int]
         L.gdn_prefill_workspace_size.restype = _sz
         L.gdn_prefill_workspace_size.argtypes = [_int, _int, _int, _int]
         L.gdn_device_error.restype = _int
@@ -212,6 +216,35 @@ def out_proj(x, w, y, stream=None):
     st = lib().gdn_out_proj(_ptr(x, "x", (M, DI), torch.bfloat16), _ptr(w, "w", (N_EMBD, DI), torch.bfloat16),
                             _ptr(y, "y", (M, N_EMBD)), M, od, _stream(stream))
     _check(st, "gdn_out_proj")
+
+
+ATTN_HQ, ATTN_HKV, ATTN_D = 16, 2, 256   # GDN_ATTN_Q_HEADS, GDN_ATTN_KV_HEADS, GDN_ATTN_HEAD_DIM
+
+
+def attn_decode_workspace_size(B: int, Lmax: int) -> int:
+    return int(lib().gdn_attn_decode_workspace_size(int(B), int(Lmax)))
+
+
+def attn_decode(q, k_cache, v_cache, ctx_len, z, out, workspace=None, stream=None):
+    """gdn_attn_decode: one decode step of GQA attention (16 query / 2 KV heads,
+    head_dim 256) with the sigmoid output gate. q, z [B][16][256] bf16; caches
+    [B][2][Lmax][256] bf16; ctx_len [B] int32; out [B][16][256] fp32 or bf16.
+    Allocates the workspace through torch when none is given."""
+    B = q.shape[0]
+    Lmax = k_cache.shape[2] if k_cache.dim() == 4 else 0
+    od = _act_dtype(out)
+    need = attn_decode_workspace_size(B, Lmax) if B > 0 else 0
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().gdn_attn_decode(_ptr(q, "q", (B, ATTN_HQ, ATTN_D), torch.bfloat16),
+                               _ptr(k_cache, "k_cache", (B, ATTN_HKV, Lmax, ATTN_D), torch.bfloat16),
+                               _ptr(v_cache, "v_cache", (B, ATTN_HKV, Lmax, ATTN_D), torch.bfloat16),
+                               _ptr(ctx_len, "ctx_len", (B,), torch.int32),
+                               _ptr(z, "z", (B, ATTN_HQ, ATTN_D), torch.bfloat16),
+                               _ptr(out, "out", (B, ATTN_HQ, ATTN_D)), B, Lmax, _ptr(workspace, "workspace"),
+                               workspace.numel() * workspace.element_size(), od, _stream(stream))
+    _check(st, "gdn_attn_decode")
+    return workspace
 
 
 def prefill_workspace_size(N: int, T_total: int, act=torch.bfloat16, chunk_size: int = 0) -> int:

@@ -56,6 +56,11 @@ extern "C" {
 #define GDN_DECODE_MAX_T 8   /* tokens per sequence of gdn_decode_multi, at most */
 #define GDN_HIDDEN 2048      /* n_embd: the model width (in_proj input, ssm_out output) */
 #define GDN_IN_PROJ_ROWS 12352   /* stacked input-projection weight rows: 8192 + 4096 + 32 + 32 */
+/* The full-attention layers (section "Full-attention block"): GQA with 16
+ * query heads and 2 KV heads of head_dim 256; query head h reads KV head h / 8. */
+#define GDN_ATTN_Q_HEADS 16
+#define GDN_ATTN_KV_HEADS 2
+#define GDN_ATTN_HEAD_DIM 256
 
 typedef enum {
     GDN_OK = 0,
@@ -244,6 +249,41 @@ gdn_status gdn_in_proj(const void *h, const void *w_in, void *qkv, void *z, void
  * that gives up is reported afterwards by gdn_device_error.
  */
 gdn_status gdn_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, void *stream);
+
+/*
+ * gdn_attn_decode -- decode attention of the full-attention layers, steps 5-6
+ * of section "Full-attention block" (the other layer type of the same model):
+ * for every sequence b and query head h, with g = h / 8 (GQA: 8 query heads
+ * share one KV head) and L = ctx_len[b],
+ *   o   = sum_{p < L} softmax_p(k[b][g][p] . q[b][h] / sqrt(256)) v[b][g][p]
+ *   out = o * sigmoid(z[b][h])            (elementwise over the 256 dims)
+ *   q        [B][16][256] bf16: the new token's queries after their RMSNorm
+ *            and partial RoPE (steps 2-4)
+ *   k_cache, v_cache [B][2][Lmax][256] bf16: the KV cache, keys after their
+ *            RMSNorm and RoPE, the new token's row already appended
+ *   ctx_len  [B] int32 (device): cached positions of each sequence, clamped to
+ *            [0, Lmax]; rows at or past ctx_len are never used, whatever they
+ *            hold; ctx_len 0 gives out = 0
+ *   z        [B][16][256] bf16: the output gate (second half of each head of
+ *            the joint Q+gate projection)
+ *   out      [B][16][256] out_dt
+ *   workspace: device scratch of gdn_attn_decode_workspace_size(B, Lmax)
+ *            bytes, 16-byte aligned, owned by the caller; contents on entry
+ *            and exit are unspecified
+ * The softmax weights enter the value product rounded to bf16 (fp32
+ * accumulation), as the kernel's tensor cores take them.
+ * 1 <= B <= 65535 (B == 0 is a no-op), 1 <= Lmax, B * 2 * Lmax <= 2^30.
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_WORKSPACE, GDN_ERR_CUDA (also when the
+ * driver's tensor-map encoder is unavailable). A bounded device wait that gives
+ * up is reported afterwards by gdn_device_error.
+ */
+gdn_status gdn_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
+                           const void *z, void *out, int B, int Lmax, void *workspace, size_t workspace_bytes,
+                           gdn_dtype out_dt, void *stream);
+
+/* Bytes of workspace gdn_attn_decode needs for (B, Lmax); 0 if they are out of
+ * range. Pure host arithmetic. */
+size_t gdn_attn_decode_workspace_size(int B, int Lmax);
 
 /* Bytes of workspace gdn_prefill needs for these sizes (0 if the arguments are
  * invalid; never 0 for valid ones). Pure host arithmetic. */

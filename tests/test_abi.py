@@ -31,6 +31,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gdn_conv_step", "gdn_decode_step", "gdn_decode_multi", "gdn_prefill", "gdn_prefill_workspace_size",
+              "gdn_in_proj", "gdn_out_proj", "gdn_attn_decode", "gdn_attn_decode_workspace_size",
               "gdn_device_error", "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
         assert n in names
 
@@ -152,6 +153,33 @@ def test_out_proj_argument_checks(ops):
         assert L.gdn_out_proj(*args, 4, ops.GDN_F32, None) == ops.GDN_ERR_INVALID_ARG
         args[i] = MIS
         assert L.gdn_out_proj(*args, 4, ops.GDN_F32, None) == ops.GDN_ERR_INVALID_ARG
+
+
+def test_attn_decode_argument_checks(ops):
+    L = ops.lib()
+    ws = L.gdn_attn_decode_workspace_size(256, 4096)
+    # 256 sequences x 2 KV heads x 8 blocks of 512 positions, each 8 x 256 outputs + 8 (max, sum) pairs
+    assert ws == 256 * 2 * 8 * (8 * 256 + 16) * 4
+    assert L.gdn_attn_decode_workspace_size(1, 300) == 2 * 3 * (8 * 256 + 16) * 4   # small batch: 1-tile blocks
+    assert L.gdn_attn_decode_workspace_size(0, 10) == 0 and L.gdn_attn_decode_workspace_size(3, 0) == 0
+    assert L.gdn_attn_decode_workspace_size(3, 1 << 28) == 0                        # B * 2 * Lmax > 2^30
+
+    def call(q=FAKE, k=FAKE, v=FAKE, cl=FAKE, z=FAKE, out=FAKE, B=4, Lmax=64, w=FAKE, wb=1 << 30, od=1):
+        return L.gdn_attn_decode(q, k, v, cl, z, out, B, Lmax, w, wb, od, None)
+
+    assert call(B=0) == ops.GDN_OK                                        # empty: no-op
+    assert call(B=-1) == ops.GDN_ERR_INVALID_ARG
+    assert call(B=65536) == ops.GDN_ERR_INVALID_ARG
+    assert call(Lmax=0) == ops.GDN_ERR_INVALID_ARG
+    assert call(B=3, Lmax=1 << 28) == ops.GDN_ERR_INVALID_ARG
+    assert call(od=7) == ops.GDN_ERR_INVALID_ARG
+    for name in ("q", "k", "v", "z", "out"):
+        assert call(**{name: 0}) == ops.GDN_ERR_INVALID_ARG
+        assert call(**{name: MIS}) == ops.GDN_ERR_INVALID_ARG
+    assert call(cl=0) == ops.GDN_ERR_INVALID_ARG
+    assert call(cl=FAKE + 2) == ops.GDN_ERR_INVALID_ARG
+    assert call(w=0) == ops.GDN_ERR_WORKSPACE
+    assert call(wb=L.gdn_attn_decode_workspace_size(4, 64) - 1) == ops.GDN_ERR_WORKSPACE
 
 
 def test_conv_step_argument_checks(ops):
