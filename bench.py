@@ -55,6 +55,18 @@ MULTI_T = 4
 # (M o Q K^T) V_new and the state update K^T V_new per V-head, with C=64.
 PREFILL_FLOP_PER_TOKEN = 5_242_880
 
+# Decode attention of the full-attention layers (gdn_attn_decode): the 10
+# attention layers of the stack, each with its own bf16 KV cache, B=256
+# sequences at a 4096-position context. Algorithmic bytes per call: the cache
+# read once (B x 2 KV heads x ctx x 256 dims x 2 (K, V) x 2 B), q and z read and
+# the bf16 output written once (3 x B x 16 x 256 x 2 B), ctx_len (B x 4 B).
+ATTN_LAYERS, ATTN_CTX = 10, 4096
+ATTN_BYTES_PER_CALL = BATCH * 2 * ATTN_CTX * 256 * 2 * 2 + 3 * BATCH * 16 * 256 * 2 + BATCH * 4
+# DRAM traffic of one attn_block_kernel launch at B=256, scaled by 4 from the
+# ncu capture at B=64 (the blocks and their bytes grow with B), from
+# profiles/attn_decode_B256_ctx4096.md. None once the kernel changes.
+ATTN_TRAFFIC_PER_CALL = (537_517_312 + 8_822_784) * 4
+
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch at B=256
 # (one layer, cold L2), from the ncu capture in
 # profiles/decode_step_kernel_B256.md. Set to None whenever the kernel changes
@@ -336,9 +348,35 @@ def run_gpu(args, rank, world, dev):
     ip = dict(us=ip_ms * 1e3, tflops=2.0 * PREFILL_T * w_in.shape[0] * I.N_EMBD / (ip_ms / 1e3) / 1e12)
     del w_in, h_in, outs_in
     assert ops.device_error() == ops.GDN_OK
+    torch.cuda.empty_cache()
+    # ---------------- decode attention of the 10 full-attention layers (gdn_attn_decode)
+    att = [I.attn_inputs(I.seed_of(5, layer), BATCH, ATTN_CTX, device=dev) for layer in range(ATTN_LAYERS)]
+    att_out = [torch.empty(BATCH, 16, 256, dtype=torch.bfloat16, device=dev) for _ in range(ATTN_LAYERS)]
+    att_ws = torch.empty(ops.attn_decode_workspace_size(BATCH, ATTN_CTX), dtype=torch.uint8, device=dev)
+
+    def attn_step():
+        for a_in, a_out in zip(att, att_out):
+            ops.attn_decode(a_in.q, a_in.k_cache, a_in.v_cache, a_in.ctx_len, a_in.z, a_out, workspace=att_ws)
+
+    for _ in range(args.warmup):
+        attn_step()
+    barrier_sync()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        attn_step()
+    ev1.record(stream)
+    barrier_sync()
+    sampler.mark(t_wall0, time.time())
+    at_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    at_call_s = at_ms / 1e3 / (ATTN_LAYERS * args.steps)
+    at = dict(tok_s=job_rate(BATCH * args.steps, world, at_ms), call_s=at_call_s,
+              achieved=ATTN_BYTES_PER_CALL / at_call_s / 1e9)
+    assert ops.device_error() == ops.GDN_OK
+    del att, att_out, att_ws
     clocks = sampler.stop()
 
-    return dict(ip=ip, op=op, mt=mt, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
+    return dict(at=at, ip=ip, op=op, mt=mt, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
                 bytes_per_launch=bytes_per_launch, launches=launches, e2e_tok_s=e2e_tok_s, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, pf_ms=pf_ms, pf_tok_s=pf_tok_s, pf_tflops=pf_tflops, hbm_peak=hbm_peak,
                 tc_peak=tc_peak, peak_src=peak_src, clocks=clocks)
@@ -407,7 +445,8 @@ def profile_case(args):
     clocks, a few launches on a few GB. ``--case decode``: --layers layers of
     gdn_decode_step on --batch sequences; ``--case prefill``: gdn_prefill on one
     sequence of --T tokens; ``--case out_proj`` / ``--case in_proj``: the
-    projection GEMMs on --T rows."""
+    projection GEMMs on --T rows; ``--case attn``: gdn_attn_decode on --batch
+    sequences with a --T position context."""
     import torch
 
     from gated_deltanet_linear_02_gb300 import build as gbuild
@@ -434,6 +473,12 @@ def profile_case(args):
         y = torch.empty(args.T, I.N_EMBD, dtype=torch.bfloat16, device=dev)
         for _ in range(n):
             ops.out_proj(x, w, y)
+        assert ops.device_error() == ops.GDN_OK
+    elif args.case == "attn":
+        a_in = I.attn_inputs(I.seed_of(5), args.batch, args.T, device=dev)
+        out = torch.empty(args.batch, 16, 256, dtype=torch.bfloat16, device=dev)
+        for _ in range(n):
+            ops.attn_decode(a_in.q, a_in.k_cache, a_in.v_cache, a_in.ctx_len, a_in.z, out)
         assert ops.device_error() == ops.GDN_OK
     elif args.case == "in_proj":
         w_in = torch.cat(I.in_proj_weights(I.seed_of(2), device=dev), dim=0)
@@ -466,7 +511,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["decode", "prefill", "out_proj", "in_proj"], default=None,
+    ap.add_argument("--case", choices=["decode", "prefill", "out_proj", "in_proj", "attn"], default=None,
                     help="profiling run of one path (see profile_case); prints no JSON line")
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--layers", type=int, default=1)
@@ -566,6 +611,15 @@ def main():
                                       "roofline": {"bound": "hbm", "achieved": r["op"][BATCH]["gbs"],
                                                    "peak": r["hbm_peak"], "unit": "GB/s",
                                                    "frac": r["op"][BATCH]["gbs"] / r["hbm_peak"]}}},
+        "attn_decode": {"workload": f"attn_decode_{ATTN_LAYERS}L_B{BATCH}_ctx{ATTN_CTX}_bf16",
+                        "op": "GQA 16q/2kv, head_dim 256, softmax(q k^T / 16) v * sigmoid(z)",
+                        "value": r["at"]["tok_s"], "unit": "tok/s", "us_per_call": r["at"]["call_s"] * 1e6,
+                        "kernels_per_call": 2, "l2": "inputs larger than L2 (2 GiB of cache per call)",
+                        "roofline": {"bound": "hbm", "achieved": r["at"]["achieved"], "peak": r["hbm_peak"],
+                                     "unit": "GB/s", "frac": r["at"]["achieved"] / r["hbm_peak"],
+                                     "algorithmic_bytes_per_call": ATTN_BYTES_PER_CALL,
+                                     "traffic": ATTN_TRAFFIC_PER_CALL, "kernel": "attn_block_kernel<bf16>",
+                                     "timed": "whole call: attn_block_kernel + attn_combine_kernel"}},
         "decode_multi": {"workload": f"decode_multi_30L_B{BATCH}_T{MULTI_T}_bf16", "value": r["mt"]["tok_s"],
                          "unit": "tok/s", "tokens_per_sequence_per_call": MULTI_T,
                          "launch_us": r["mt"]["launch_s"] * 1e6,

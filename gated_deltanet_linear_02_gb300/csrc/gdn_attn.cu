@@ -12,8 +12,8 @@
 //  - GQA packing: the 8 query heads that share a KV head are served by one CTA,
 //    which reads each key and value row once for all 8;
 //  - fixed blocks: the context is cut into blocks of 128 * tps positions that
-//    CTAs process in parallel, and a combine step merges the blocks' partial
-//    softmax sums. Long contexts and small batches still fill the GPU.
+//    CTAs process in parallel, and the blocks' partial softmax sums are merged
+//    at the end. Long contexts and small batches still fill the GPU.
 //
 // Per CTA = (sequence b, KV head g, block s), tiles of 128 positions:
 //  - warp 0, lane 0, TMA producer: per tile, four 32 KiB copies (keys dims
@@ -31,11 +31,16 @@
 //    and stored as the P^T operand. For outputs, thread r holds dims r and
 //    128 + r of all 8 heads and rescales its running sums by the factor
 //    2^(m_old - m_new) before adding the tile's O^T.
-// The block's unnormalised output, its maximum and its sum go to a workspace;
-// the combine kernel merges the blocks of each (sequence, head), divides by the
-// sum and applies the gate. Positions at or past the context length are masked
-// (their scores), and their value rows in shared memory are zeroed, so nothing
-// stored past ctx_len can reach the output. An empty context gives zeros.
+// A context that fits one block is finished in place: o = acc / sum, times
+// sigmoid(z). Otherwise each block stores its unnormalised output, maximum and
+// sum in the workspace, and a combine kernel (one warp per sequence and query
+// head) merges them. Merging inside the last block to
+// finish was measured slower: its dependent L2 round trips hold an SM slot that
+// streaming blocks need. Positions at or past the context
+// length are masked (their scores), and their value rows in shared memory are
+// zeroed, so nothing stored past ctx_len can reach the output. An empty context
+// gives zeros. The TMA producer starts as soon as the barriers exist; the Q
+// operand and the TMEM allocation are ready before the first MMA.
 //
 // Every mbarrier wait is bounded; a wait that gives up records GDN_ERR_TIMEOUT.
 #include <cuda.h>
@@ -85,9 +90,12 @@ struct AttnSmall {
 };
 constexpr size_t AT_SMEM = SA_SMALL + sizeof(AttnSmall) + 1024;   // + slack to align the block
 
+template <typename TO>
 struct AttnArgs {
     const bf16 *q;            // [B][16][256]
+    const bf16 *z;            // [B][16][256]
     const int32_t *ctx_len;   // [B]
+    TO *out;                  // [B][16][256]
     float *part_o;            // [items][8][256]: unnormalised block outputs
     float *part_ml;           // [items][8][2]: block maximum (log2 units), block sum
     int Lmax, S, tps;         // cache rows per (sequence, KV head), blocks per (b, g), tiles per block
@@ -124,9 +132,12 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo)
     return tc::smem_desc(saddr, lbo, 1024u) | ((uint64_t)2 << 61);
 }
 
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+template <typename TO>
 __global__ void __launch_bounds__(AT_THREADS, 2) attn_block_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                    const __grid_constant__ CUtensorMap vmap,
-                                                                   const AttnArgs a)
+                                                                   const AttnArgs<TO> a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *blk = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -139,20 +150,15 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_block_kernel(const __grid_
     const int p0 = sp * a.tps * AT_TILE;               // this block's positions [p0, p1)
     const int p1 = min(L, p0 + a.tps * AT_TILE);
     const int nt = p1 > p0 ? (p1 - p0 + AT_TILE - 1) / AT_TILE : 0;
-    float *pml = a.part_ml + (size_t)item * AT_G * 2;
-    if (nt == 0) {                                     // nothing cached here: an empty block
-        if (tid < AT_G) {
-            pml[2 * tid] = -INFINITY;
-            pml[2 * tid + 1] = 0.0f;
-        }
+    const int nb = (L + a.tps * AT_TILE - 1) / (a.tps * AT_TILE);   // non-empty blocks of (b, g)
+    const size_t hout = ((size_t)b * AT_HQ + (size_t)AT_G * g) * AT_D;   // the group's first output
+    if (nt == 0) {                                     // nothing cached here
+        if (L == 0 && sp == 0)                         // an empty context: zeros
+            for (int i = tid; i < AT_G * AT_D; i += AT_THREADS) a.out[hout + i] = from_f<TO>(0.0f);
         return;
     }
     const volatile int &aborted = ss.abort;
 
-    if (warp == 1) {
-        tc::tmem_alloc(smem_u32(&ss.tmem), AT_TMEM_COLS);
-        tc::tmem_relinquish();
-    }
     if (tid == 0) {
         for (int s = 0; s < AT_SLOTS; ++s) {
             mbar_init(smem_u32(&ss.full[s]), 1);
@@ -166,6 +172,11 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_block_kernel(const __grid_
         }
         ss.abort = 0;
         fence_mbar_init();
+    }
+    __syncthreads();                                   // barriers exist: the producer may start
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(&ss.tmem), AT_TMEM_COLS);
+        tc::tmem_relinquish();
     }
     if (warp >= 2) {
         // Q^T operand: the group's 8 query heads, scaled by 1/sqrt(256) = 1/16
@@ -183,10 +194,12 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_block_kernel(const __grid_
         }
         fence_proxy_async_smem();
     }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tm = ss.tmem;
+    if (warp >= 1) {                                   // Q^T and TMEM ready for the issuer and softmax
+        tc::fence_before_sync();
+        asm volatile("bar.sync 2, 160;" ::: "memory");
+        tc::fence_after_sync();
+    }
+    const uint32_t tm = warp >= 1 ? ss.tmem : 0u;
     auto slot_addr = [&](int i) { return sb + SA_RING + (uint32_t)(i % AT_SLOTS) * AT_SLOT_BYTES; };
     auto wait_full = [&](int i) {
         return mbar_wait_bounded(smem_u32(&ss.full[i % AT_SLOTS]), (uint32_t)((i / AT_SLOTS) & 1));
@@ -365,15 +378,27 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_block_kernel(const __grid_
                 if (lane == 0) ss.lred[q4][h] = l;
             }
             softmax_bar();
-            float *po = a.part_o + (size_t)item * AT_G * AT_D;
+            if (nb == 1) {
+                // the whole context in this block: normalise and gate in place
 #pragma unroll
-            for (int h = 0; h < AT_G; ++h) {
-                po[h * AT_D + r] = acc0[h];
-                po[h * AT_D + 128 + r] = acc1[h];
-            }
-            if (r < AT_G) {
-                pml[2 * r] = m[r];
-                pml[2 * r + 1] = ss.lred[0][r] + ss.lred[1][r] + ss.lred[2][r] + ss.lred[3][r];
+                for (int h = 0; h < AT_G; ++h) {
+                    const float inv = 1.0f / (ss.lred[0][h] + ss.lred[1][h] + ss.lred[2][h] + ss.lred[3][h]);
+                    const size_t o = hout + (size_t)h * AT_D + r;
+                    a.out[o] = from_f<TO>(acc0[h] * inv * sigmoid_f(to_f(a.z[o])));
+                    a.out[o + 128] = from_f<TO>(acc1[h] * inv * sigmoid_f(to_f(a.z[o + 128])));
+                }
+            } else {
+                float *po = a.part_o + (size_t)item * AT_G * AT_D;
+                float *pml = a.part_ml + (size_t)item * AT_G * 2;
+#pragma unroll
+                for (int h = 0; h < AT_G; ++h) {
+                    po[h * AT_D + r] = acc0[h];
+                    po[h * AT_D + 128 + r] = acc1[h];
+                }
+                if (r < AT_G) {
+                    pml[2 * r] = m[r];
+                    pml[2 * r + 1] = ss.lred[0][r] + ss.lred[1][r] + ss.lred[2][r] + ss.lred[3][r];
+                }
             }
         } else if (r == 0) {
             ss.abort = 1;
@@ -388,43 +413,71 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_block_kernel(const __grid_
     if (tid == 0 && ss.abort) atomicExch(&g_attn_error, (unsigned int)GDN_ERR_TIMEOUT);
 }
 
-// Merges the blocks of each (sequence, query head): with block maxima m_s (log2
-// units), sums l_s and unnormalised outputs o_s, M = max m_s and
-//   out = (sum_s 2^(m_s - M) o_s) / (sum_s 2^(m_s - M) l_s) * sigmoid(z).
-// One warp per (sequence, head), 8 dims per lane.
+// Merges the blocks of each (sequence, query head) whose context spans nb > 1
+// blocks: with block maxima m_s (log2 units), sums l_s and unnormalised outputs
+// o_s, M = max m_s, w_s = 2^(m_s - M) and
+//   out = (sum_s w_s o_s) / (sum_s w_s l_s) * sigmoid(z).
+// One warp per (sequence, head), 8 dims per lane. Blocks are taken 8 at a time
+// with all their loads issued before any is used (one memory round trip per 8
+// blocks), and merged online with a running maximum.
 template <typename TO>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restrict__ part_o,
                                                            const float *__restrict__ part_ml,
+                                                           const int32_t *__restrict__ ctx_len,
                                                            const bf16 *__restrict__ z, TO *__restrict__ out, int B,
-                                                           int S)
+                                                           int Lmax, int S, int tps)
 {
-    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (w >= B * AT_HQ) return;
-    const int b = w / AT_HQ, h = w % AT_HQ, g = h / AT_G, hl = h % AT_G;
-    const size_t item0 = ((size_t)b * AT_HKV + g) * S;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(part_ml + ((item0 + s) * AT_G + hl) * 2));
-    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float l = 0.0f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
-            const size_t it = (item0 + s) * AT_G + hl;
-            const float ms = __ldg(part_ml + it * 2);
-            if (ms == -INFINITY) continue;             // an empty block
-            const float wgt = exp2f(ms - M);
-            l += wgt * __ldg(part_ml + it * 2 + 1);
-            const float4 *src = reinterpret_cast<const float4 *>(part_o + it * AT_D) + 2 * lane;
-            const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
-            o[0] += wgt * v0.x; o[1] += wgt * v0.y; o[2] += wgt * v0.z; o[3] += wgt * v0.w;
-            o[4] += wgt * v1.x; o[5] += wgt * v1.y; o[6] += wgt * v1.z; o[7] += wgt * v1.w;
-        }
-    }
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;      // an empty context gives zeros
-    const size_t o0 = (size_t)w * AT_D + 8 * lane;
-    const uint4 zr = __ldg(reinterpret_cast<const uint4 *>(z + o0));
-    const bf16 *zz = reinterpret_cast<const bf16 *>(&zr);
+    const int bh = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (bh >= B * AT_HQ) return;
+    const int b = bh / AT_HQ, h = bh % AT_HQ, g = h / AT_G, hl = h % AT_G;
+    const int L = min(max(__ldg(ctx_len + b), 0), Lmax);
+    const int nb = (L + tps * AT_TILE - 1) / (tps * AT_TILE);
+    if (nb <= 1) return;                               // finished in place (or an empty context)
+    const size_t it0 = ((size_t)b * AT_HKV + g) * S * AT_G + hl;   // (block 0, head hl) of this (b, g)
+    float M = -INFINITY, l = 0.0f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < nb; s0 += 8) {
+        float mv[8], lv[8];
+        float4 va[8], vb[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) out[o0 + e] = from_f<TO>(o[e] * inv / (1.0f + expf(-to_f(zz[e]))));
+        for (int j = 0; j < 8; ++j) {
+            if (s0 + j < nb) {
+                const size_t it = it0 + (size_t)(s0 + j) * AT_G;
+                mv[j] = __ldg(part_ml + it * 2);
+                lv[j] = __ldg(part_ml + it * 2 + 1);
+                const float4 *src = reinterpret_cast<const float4 *>(part_o + it * AT_D) + 2 * lane;
+                va[j] = __ldg(src);
+                vb[j] = __ldg(src + 1);
+            } else {
+                mv[j] = -INFINITY;
+                lv[j] = 0.0f;
+                va[j] = vb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float Mc = M;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) Mc = fmaxf(Mc, mv[j]);
+        const float sc = exp2f(M - Mc);                // 0 for the first 8 blocks
+        l *= sc;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] *= sc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float w = exp2f(mv[j] - Mc);         // 0 for the padding entries
+            l += w * lv[j];
+            o[0] += w * va[j].x; o[1] += w * va[j].y; o[2] += w * va[j].z; o[3] += w * va[j].w;
+            o[4] += w * vb[j].x; o[5] += w * vb[j].y; o[6] += w * vb[j].z; o[7] += w * vb[j].w;
+        }
+        M = Mc;
+    }
+    const float inv = 1.0f / l;
+    const size_t o0 = (size_t)bh * AT_D + 8 * lane;
+    const uint4 zr = __ldg(reinterpret_cast<const uint4 *>(z + o0));
+    const uint32_t zw[4] = {zr.x, zr.y, zr.z, zr.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float zz = __uint_as_float((e & 1) ? (zw[e >> 1] & 0xFFFF0000u) : (zw[e >> 1] << 16));
+        out[o0 + e] = from_f<TO>(o[e] * inv * sigmoid_f(zz));
+    }
 }
 
 // ------------------------------------------------------------------ launcher
@@ -445,17 +498,17 @@ static int attn_blocks(int B, int Lmax)
     return (tiles + tps - 1) / tps;
 }
 
+// Workspace: the partials of every block.
 size_t attn_workspace_bytes(int B, int Lmax)
 {
     const size_t items = (size_t)B * AT_HKV * attn_blocks(B, Lmax);
     return items * (AT_G * AT_D + 2 * AT_G) * sizeof(float);
 }
 
-cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
-                               const void *z, void *out, int B, int Lmax, void *ws, gdn_dtype out_dt,
-                               cudaStream_t s)
+template <typename TO>
+static cudaError_t launch_attn_typed(const CUtensorMap &km, const CUtensorMap &vm, AttnArgs<TO> a, int B,
+                                     cudaStream_t s)
 {
-    if (B <= 0) return cudaSuccess;
     static std::mutex mu;
     static bool attr_set[64] = {};
     int dev = 0;
@@ -464,34 +517,41 @@ cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-            e = cudaFuncSetAttribute(attn_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AT_SMEM);
+            e = cudaFuncSetAttribute(attn_block_kernel<TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)AT_SMEM);
             if (e != cudaSuccess) return e;
             if (dev >= 0 && dev < 64) attr_set[dev] = true;
         }
     }
+    const size_t items = (size_t)B * AT_HKV * a.S;
+    attn_block_kernel<TO><<<(unsigned)items, AT_THREADS, AT_SMEM, s>>>(km, vm, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || a.S == 1) return e;        // one block per context: nothing to merge
+    attn_combine_kernel<TO><<<(unsigned)((B * AT_HQ + 7) / 8), 256, 0, s>>>(a.part_o, a.part_ml, a.ctx_len, a.z,
+                                                                            a.out, B, a.Lmax, a.S, a.tps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
+                               const void *z, void *out, int B, int Lmax, void *ws, gdn_dtype out_dt,
+                               cudaStream_t s)
+{
+    if (B <= 0) return cudaSuccess;
     CUtensorMap km, vm;
     const long long rows = (long long)B * AT_HKV * Lmax;
     if (!make_bf16_sw128_map(&km, k_cache, rows, AT_D, AT_TILE) ||
         !make_bf16_sw128_map(&vm, v_cache, rows, AT_D, AT_TILE))
         return cudaErrorInvalidValue;
-    AttnArgs a;
-    a.q = (const bf16 *)q;
-    a.ctx_len = ctx_len;
-    a.Lmax = Lmax;
-    a.tps = attn_tiles_per_block(B, Lmax);
-    a.S = attn_blocks(B, Lmax);
-    const size_t items = (size_t)B * AT_HKV * a.S;
-    a.part_o = (float *)ws;
-    a.part_ml = a.part_o + items * AT_G * AT_D;
-    attn_block_kernel<<<(unsigned)items, AT_THREADS, AT_SMEM, s>>>(km, vm, a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const unsigned cgrid = (unsigned)((B * AT_HQ + 7) / 8);
-    if (out_dt == GDN_F32)
-        attn_combine_kernel<float><<<cgrid, 256, 0, s>>>(a.part_o, a.part_ml, (const bf16 *)z, (float *)out, B, a.S);
-    else
-        attn_combine_kernel<bf16><<<cgrid, 256, 0, s>>>(a.part_o, a.part_ml, (const bf16 *)z, (bf16 *)out, B, a.S);
-    return cudaGetLastError();
+    const int tps = attn_tiles_per_block(B, Lmax), S = attn_blocks(B, Lmax);
+    const size_t items = (size_t)B * AT_HKV * S;
+    float *part_o = (float *)ws;
+    float *part_ml = part_o + items * AT_G * AT_D;
+    if (out_dt == GDN_F32) {
+        AttnArgs<float> a{(const bf16 *)q, (const bf16 *)z, ctx_len, (float *)out, part_o, part_ml, Lmax, S, tps};
+        return launch_attn_typed(km, vm, a, B, s);
+    }
+    AttnArgs<bf16> a{(const bf16 *)q, (const bf16 *)z, ctx_len, (bf16 *)out, part_o, part_ml, Lmax, S, tps};
+    return launch_attn_typed(km, vm, a, B, s);
 }
 
 // Reads and clears this file's device error word (synchronous on `s`).
