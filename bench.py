@@ -247,19 +247,45 @@ def run_gpu(args, rank, world, dev):
     h2d = sum(t.numel() * t.element_size() for h in host_in for t in h)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
 
+    # The copies run on two copy streams and overlap the kernels: layer l's
+    # inputs go up while earlier layers compute, and its output comes back while
+    # later layers compute. Events order each layer's buffers: a step's upload
+    # of layer l waits until the previous step's kernel of layer l has read
+    # them, and the kernel waits until the previous download of its output is
+    # done.
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    n_l = len(layers)
+    ev = lambda: [torch.cuda.Event() for _ in range(n_l)]
+    in_ready, computed, downloaded = ev(), ev(), ev()
+
     def e2e_step():
-        for L, h, d, ho in zip(layers, host_in, dev_in, host_out):
-            for src, dst in zip(h, d):
-                dst.copy_(src, non_blocking=True)
-            ops.decode_step(None, d[0], d[1], d[2], d[3], L["conv"], L["S"], L["out"], cparams=L["cp"])
-            ho.copy_(L["out"], non_blocking=True)
+        for l, (h, d) in enumerate(zip(host_in, dev_in)):
+            up.wait_event(computed[l])
+            with torch.cuda.stream(up):
+                for src, dst in zip(h, d):
+                    dst.copy_(src, non_blocking=True)
+                in_ready[l].record(up)
+        for l, (L, d, ho) in enumerate(zip(layers, dev_in, host_out)):
+            stream.wait_event(in_ready[l])
+            stream.wait_event(downloaded[l])
+            ops.decode_step(None, d[0], d[1], d[2], d[3], L["conv"], L["S"], L["out"], cparams=L["cp"],
+                            stream=stream)
+            computed[l].record(stream)
+            down.wait_event(computed[l])
+            with torch.cuda.stream(down):
+                ho.copy_(L["out"], non_blocking=True)
+                downloaded[l].record(down)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
     barrier_sync()
     ev0.record(stream)
+    up.wait_event(ev0)
+    down.wait_event(ev0)
     for _ in range(args.steps):
         e2e_step()
+    stream.wait_stream(up)
+    stream.wait_stream(down)
     ev1.record(stream)
     barrier_sync()
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1))
@@ -443,7 +469,8 @@ def cpu_baseline(n_seq=None):
 def profile_case(args):
     """A small, self-contained run of one path for profilers: no JSON line, no
     clocks, a few launches on a few GB. ``--case decode``: --layers layers of
-    gdn_decode_step on --batch sequences; ``--case prefill``: gdn_prefill on one
+    gdn_decode_step on --batch sequences; ``--case multi``: the same with
+    gdn_decode_multi, MULTI_T tokens per sequence; ``--case prefill``: gdn_prefill on one
     sequence of --T tokens; ``--case out_proj`` / ``--case in_proj``: the
     projection GEMMs on --T rows; ``--case attn``: gdn_attn_decode on --batch
     sequences with a --T position context."""
@@ -473,6 +500,19 @@ def profile_case(args):
         y = torch.empty(args.T, I.N_EMBD, dtype=torch.bfloat16, device=dev)
         for _ in range(n):
             ops.out_proj(x, w, y)
+        assert ops.device_error() == ops.GDN_OK
+    elif args.case == "multi":
+        Ls = []
+        for layer in range(args.layers):
+            seed = I.seed_of(3, layer)
+            lp = I.layer_params(seed).to(dev)
+            conv, S = I.initial_states(seed, args.batch, torch.bfloat16, device=dev)
+            st = I.streams(seed, MULTI_T, torch.bfloat16, device=dev, lead=(args.batch,))
+            out = torch.empty(args.batch, MULTI_T, I.D_INNER, dtype=torch.bfloat16, device=dev)
+            Ls.append((ops.make_params(lp), conv, S, st, out))
+        for _ in range(n):
+            for cp, conv, S, st, out in Ls:
+                ops.decode_multi(None, st.qkv, st.z, st.alpha, st.beta, conv, S, out, cparams=cp)
         assert ops.device_error() == ops.GDN_OK
     elif args.case == "attn":
         a_in = I.attn_inputs(I.seed_of(5), args.batch, args.T, device=dev)
@@ -511,7 +551,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["decode", "prefill", "out_proj", "in_proj", "attn"], default=None,
+    ap.add_argument("--case", choices=["decode", "multi", "prefill", "out_proj", "in_proj", "attn"], default=None,
                     help="profiling run of one path (see profile_case); prints no JSON line")
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--layers", type=int, default=1)

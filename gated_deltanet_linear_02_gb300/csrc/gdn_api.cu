@@ -32,6 +32,8 @@ cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v
                                const void *z, void *out, int B, int Lmax, void *ws, gdn_dtype out_dt,
                                cudaStream_t s);
 cudaError_t take_attn_error(unsigned int *word, cudaStream_t s);
+cudaError_t launch_wait_timeout(cudaStream_t s);
+cudaError_t take_selftest_error(unsigned int *word, cudaStream_t s);
 }  // namespace gdn
 
 using namespace gdn;
@@ -263,13 +265,21 @@ gdn_status gdn_device_error(void *stream)
     unsigned int word3 = 0;
     unsigned int word4 = 0;
     unsigned int word5 = 0;
+    unsigned int word6 = 0;
     cudaError_t e = take_decode_error(&word, s);
     if (e == cudaSuccess) e = take_chunk_error(&word2, s);
     if (e == cudaSuccess) e = take_multi_error(&word3, s);
     if (e == cudaSuccess) e = take_gemm_error(&word4, s);
     if (e == cudaSuccess) e = take_attn_error(&word5, s);
+    if (e == cudaSuccess) e = take_selftest_error(&word6, s);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_error");
-    return (word | word2 | word3 | word4 | word5) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
+    return (word | word2 | word3 | word4 | word5 | word6) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
+}
+
+gdn_status gdn_selftest_wait_timeout(void *stream)
+{
+    cudaError_t e = launch_wait_timeout((cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_selftest_wait_timeout");
 }
 
 }  // extern "C"

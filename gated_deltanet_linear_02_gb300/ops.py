@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_attn_decode_workspace_size.argtypes = [_int, _int]
         L.gdn_prefill_workspace_size.restype = _sz
         L.gdn_prefill_workspace_size.argtypes = [_int, _int, _int, _int]
+        L.gdn_selftest_wait_timeout.restype = _int
+        L.gdn_selftest_wait_timeout.argtypes = [_vp]
         L.gdn_device_error.restype = _int
         L.gdn_device_error.argtypes = [_vp]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -283,6 +285,12 @@ def device_error(stream=None) -> int:
     """Synchronises the stream, then reads and clears the library's device error
     word: GDN_OK, or GDN_ERR_TIMEOUT if a bounded device-side wait gave up."""
     return lib().gdn_device_error(_stream(stream))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """gdn_selftest_wait_timeout: enqueue the kernel whose bounded wait runs
+    out (about 2 s); the next device_error() then reports GDN_ERR_TIMEOUT."""
+    _check(lib().gdn_selftest_wait_timeout(_stream(stream)), "gdn_selftest_wait_timeout")
 
 
 STATIC_SCRATCH_BYTES = 64 << 20

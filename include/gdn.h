@@ -297,6 +297,14 @@ size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_s
  * current device gave up since the word was last cleared. */
 gdn_status gdn_device_error(void *stream);
 
+/* Diagnostic of the failure path above: enqueues one small kernel that waits
+ * on an mbarrier nothing ever completes, through the library's bounded wait.
+ * After the limit (2 s) the kernel records GDN_ERR_TIMEOUT and returns
+ * normally, so the next gdn_device_error on this stream reports
+ * GDN_ERR_TIMEOUT (and clears it) and the context stays usable. Errors:
+ * GDN_ERR_CUDA. */
+gdn_status gdn_selftest_wait_timeout(void *stream);
+
 /* Human-readable name of a status (static storage). */
 const char *gdn_status_string(gdn_status s);
 

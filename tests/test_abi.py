@@ -32,6 +32,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gdn_conv_step", "gdn_decode_step", "gdn_decode_multi", "gdn_prefill", "gdn_prefill_workspace_size",
               "gdn_in_proj", "gdn_out_proj", "gdn_attn_decode", "gdn_attn_decode_workspace_size",
+              "gdn_selftest_wait_timeout",
               "gdn_device_error", "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
         assert n in names
 
