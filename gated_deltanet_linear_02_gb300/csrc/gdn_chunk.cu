@@ -35,6 +35,7 @@
 #include "gdn_async.cuh"
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
+#include "gdn_tma.cuh"
 
 namespace gdn {
 
@@ -140,21 +141,27 @@ constexpr uint32_t S1_SMALL = 229376;
 // by the row: rows written one per lane spread over the banks, and a row still
 // reads as float4 groups of 4 consecutive s.
 __device__ __forceinline__ int lb_at(int t, int s) { return t * CH + (((s >> 2) ^ (t & 15)) << 2) + (s & 3); }
-// Raw bf16 inputs of the chunk, staged before the conv: 67 rows (positions
-// -3..63) x 512 channels, row stride padded to 1040 B. It overlays the
-// L / T / (Gamma K)^T area, which is written only after the conv.
+// Raw bf16 inputs of the chunk, staged before the conv by four 2-D TMA copies,
+// one per 128-channel block (q, k, v of head 0, v of head 1): 67 rows
+// (positions -3..63) of 136 channels. The 8 extra channels pad each row to
+// 272 bytes, which spreads consecutive rows over the banks. The staging
+// overlays the L / T / (Gamma K)^T area, which is written only after the conv.
 constexpr uint32_t S1_RAW = 131072;
 constexpr int RAW_ROWS = CH + KC - 1;
-constexpr int RAW_STRIDE = 1040;
+constexpr int RAW_COLS = 136;
+constexpr int RAW_ROWB = RAW_COLS * 2;                              // 272-byte rows
+constexpr uint32_t RAW_BOX_BYTES = RAW_ROWS * RAW_ROWB;             // 18,224
+constexpr uint32_t RAW_SEG = (RAW_BOX_BYTES + 127) / 128 * 128;    // 128-byte aligned block stride
 // conv taps of the 512 channels (4 blocks x 128 channels x 16 B), staged with the rows
-constexpr uint32_t S1_CW = 200832;
-static_assert(S1_RAW + RAW_ROWS * RAW_STRIDE <= S1_CW && S1_CW + 4 * 2048 <= S1_SMALL, "staging overlap");
+constexpr uint32_t S1_CW = S1_RAW + 4 * RAW_SEG;
+static_assert(S1_CW % 128 == 0 && S1_CW + 4 * 2048 <= S1_SMALL, "staging overlap");
 struct P1Small {
     float G[2][CH];     // chunk-local cumulative log-decay per V-head
     float B[2][CH];     // beta
     float gam[2][CH];   // exp(G)
     float ktf[2][CH];   // exp(G_n - G_t), the row factor of K~
-    uint64_t bar;
+    uint64_t bar;       // tensor-core completions
+    uint64_t bar_ld;    // the staging copies
     uint32_t tmem;
     int abort;
 };
@@ -164,7 +171,8 @@ constexpr uint32_t T1_KK = 0, T1_QK = 64, T1_U = 128, T1_W = 256, T1_COLS = 512;
 
 template <int ES> __device__ __forceinline__ uint32_t km(int r, int k, int Kd) { return tc::kmajor_offset<ES>(r, k, Kd); }
 
-__global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkArgs a)
+__global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_constant__ CUtensorMap qkv_map,
+                                                                  const ChunkArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = smem_aligned128(smem_raw);
@@ -188,50 +196,24 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
         tc::tmem_alloc(smem_u32(&ss.tmem), T1_COLS);
         tc::tmem_relinquish();
     }
+    // ---- B1. stage the raw q|k|v inputs of chunk positions -3..63 (the 512
+    //      channels of this K-head pair) and their conv taps: one thread issues
+    //      four 2-D tensor copies and four 2 KiB bulk copies on one mbarrier.
+    //      Rows past the chunk's last token hold whatever follows (the next
+    //      sequence, or zeros past the end); only outputs of valid tokens are
+    //      kept, and those never read such rows.
+    const int chan0[4] = {Q_OFF + kh * DK, K_OFF + kh * DK, V_OFF + kh * DV, V_OFF + (kh + HK) * DV};
     if (tid == 0) {
         mbar_init(smem_u32(&ss.bar), 1);
+        mbar_init(smem_u32(&ss.bar_ld), 1);
         ss.abort = 0;
         fence_mbar_init();
-    }
-    __syncwarp();
-
-    // ---- B1. stage the raw q|k|v inputs of chunk positions -3..63 (the 512
-    //      channels of this K-head pair: four 256-byte segments per row) and the
-    //      conv taps of those channels in shared memory. All 256 threads issue
-    //      their 16-byte loads at once, so the whole stage costs one memory latency.
-    const int chan0[4] = {Q_OFF + kh * DK, K_OFF + kh * DK, V_OFF + kh * DV, V_OFF + (kh + HK) * DV};
-    auto raw_src = [&](int r) -> const bf16 * {
-        const int p = r - 3;
-        if (p >= nv) return nullptr;                       // padding after the chunk's last token
-        const int pos = CH * lc + p;                       // relative to the sequence start
-        if (pos >= 0) return a.qkv + (size_t)(seq0 + pos) * CC;
-        return a.cs_in ? a.cs_in + ((size_t)n * (KC - 1) + (pos + KC - 1)) * CC : nullptr;
-    };
-    {
-        constexpr int RAW_U4 = RAW_ROWS * 64;              // 16-byte pieces of row data
-        constexpr int CW_U4 = 4 * DK;                      // 16-byte pieces of conv taps
-        constexpr int ITER = (RAW_U4 + CW_U4 + P1_THREADS - 1) / P1_THREADS;
-        uint4 v[ITER];
+        const uint32_t bl = smem_u32(&ss.bar_ld);
+        mbar_arrive_expect_tx(bl, 4 * RAW_BOX_BYTES + 4 * 2048);
 #pragma unroll
-        for (int k = 0; k < ITER; ++k) {
-            const int e = tid + k * P1_THREADS;
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (e < RAW_U4) {
-                const bf16 *src = raw_src(e >> 6);
-                if (src) x = __ldg(reinterpret_cast<const uint4 *>(src + chan0[(e >> 4) & 3]) + (e & 15));
-            } else if (e < RAW_U4 + CW_U4) {
-                const int f = e - RAW_U4;                  // channel block f >> 7, channel f & 127
-                x = __ldg(reinterpret_cast<const uint4 *>(a.conv_w + (size_t)chan0[f >> 7] * KC) + (f & 127));
-            }
-            v[k] = x;
-        }
-#pragma unroll
-        for (int k = 0; k < ITER; ++k) {
-            const int e = tid + k * P1_THREADS;
-            if (e < RAW_U4)
-                *reinterpret_cast<uint4 *>(sm + S1_RAW + (e >> 6) * RAW_STRIDE + ((e >> 4) & 3) * 256 + (e & 15) * 16) = v[k];
-            else if (e < RAW_U4 + CW_U4)
-                *reinterpret_cast<uint4 *>(sm + S1_CW + (e - RAW_U4) * 16) = v[k];
+        for (int sg = 0; sg < 4; ++sg) {
+            tma_load_2d(sbase + S1_RAW + sg * RAW_SEG, &qkv_map, chan0[sg], t0 - (KC - 1), bl);
+            bulk_g2s(sbase + S1_CW + sg * 2048, a.conv_w + (size_t)chan0[sg] * KC, 2048, bl);
         }
     }
     // gates of both V-heads; padded tokens get g = 0, beta = 0
@@ -246,6 +228,16 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
         }
         ss.G[h][p] = gg;
         ss.B[h][p] = bb;
+    }
+    __syncthreads();
+    if (!mbar_wait_bounded(smem_u32(&ss.bar_ld), 0)) ss.abort = 1;
+    if (lc == 0 && tid < 3 * 4 * 16) {
+        // the first chunk of a sequence: positions -3..-1 are its conv_state
+        // (zeros without one), not the rows before the sequence
+        const int r = tid >> 6, sg = (tid >> 4) & 3, pc = tid & 15;
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (a.cs_in) x = __ldg(reinterpret_cast<const uint4 *>(a.cs_in + ((size_t)n * (KC - 1) + r) * CC + chan0[sg]) + pc);
+        *reinterpret_cast<uint4 *>(sm + S1_RAW + sg * RAW_SEG + r * RAW_ROWB + pc * 16) = x;
     }
     __syncthreads();
 
@@ -266,7 +258,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
             const int d = 4 * (kgh * 4 + (lane >> 3));                // 4 consecutive channels d..d+3
 #pragma unroll
             for (int m = 0; m < 4; ++m)                               // positions p-3+m = rows p+m
-                pr[k][m] = *reinterpret_cast<const uint2 *>(raw + (p + m) * RAW_STRIDE + (tile * DK + d) * 2);
+                pr[k][m] = *reinterpret_cast<const uint2 *>(raw + tile * RAW_SEG + (p + m) * RAW_ROWB + d * 2);
 #pragma unroll
             for (int e = 0; e < 4; ++e) w4[k][e] = reinterpret_cast<const float4 *>(sm + S1_CW + tile * 2048)[d + e];
         }
@@ -303,7 +295,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const ChunkAr
             w4[k] = reinterpret_cast<const float4 *>(sm + S1_CW + (2 + hv) * 2048)[d];
 #pragma unroll
             for (int m = 0; m < 7; ++m)                               // positions p0-3 .. p0+3
-                xr[k][m] = *reinterpret_cast<const bf16 *>(raw + (p0 + m) * RAW_STRIDE + ((2 + hv) * DV + d) * 2);
+                xr[k][m] = *reinterpret_cast<const bf16 *>(raw + (2 + hv) * RAW_SEG + (p0 + m) * RAW_ROWB + d * 2);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -959,8 +951,12 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
         e = cudaFuncSetAttribute(chunk_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P2_SMEM);
     if (e != cudaSuccess) return e;
 
+    CUtensorMap qkv_map;
+    if (T_total > 0 && !make_bf16_plain_map(&qkv_map, qkv, T_total, CC, RAW_COLS, RAW_ROWS))
+        return cudaErrorInvalidValue;
     chunk_schedule_kernel<<<1, 1024, 0, s>>>(cu, N, T_total, a.max_chunks, a.chunk_off, a.chunk_info);
-    if (a.max_chunks > 0) chunk_prep_kernel<<<dim3(a.max_chunks, HK), P1_THREADS, P1_SMEM, s>>>(a);
+    if (a.max_chunks > 0 && T_total > 0)
+        chunk_prep_kernel<<<dim3(a.max_chunks, HK), P1_THREADS, P1_SMEM, s>>>(qkv_map, a);
     chunk_carry_kernel<<<dim3(N, HV, NJB), P2_THREADS, P2_SMEM, s>>>(a);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = launch_gated_norm_bf16(p->norm_w, p->norm_eps, z, a.ybuf, out, T_total, out_dt, s);

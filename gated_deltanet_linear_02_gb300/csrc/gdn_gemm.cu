@@ -292,19 +292,30 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Row-major bf16 matrix [rows][cols] read in boxes of 64 columns x box_rows
-// rows, 128-byte swizzle; elements past either end read as zero.
-bool make_bf16_sw128_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_rows)
+static bool encode_bf16_2d(CUtensorMap *map, const void *base, long long rows, int cols, int box_cols, int box_rows,
+                           CUtensorMapSwizzle swz)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major bf16 matrix [rows][cols] read in boxes of 64 columns x box_rows
+// rows, 128-byte swizzle; elements past either end read as zero.
+bool make_bf16_sw128_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_rows)
+{
+    return encode_bf16_2d(map, base, rows, cols, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_bf16_plain_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_cols, int box_rows)
+{
+    return encode_bf16_2d(map, base, rows, cols, box_cols, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int sm_count();

@@ -25,4 +25,9 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 // False if the driver's encoder is unavailable or rejects the arguments.
 bool make_bf16_sw128_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_rows);
 
+// The same matrix read in boxes of box_cols x box_rows elements without
+// swizzle: a box lands in shared memory as box_rows dense rows of box_cols * 2
+// bytes (box_cols a multiple of 8, at most 256; box_rows at most 256).
+bool make_bf16_plain_map(CUtensorMap *map, const void *base, long long rows, int cols, int box_cols, int box_rows);
+
 }  // namespace gdn
