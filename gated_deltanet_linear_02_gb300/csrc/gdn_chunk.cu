@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     __syncthreads();
 
     // ---- B2. conv + SiLU from the staged rows. q and k go raw into their tf32
-    //      tiles (normalised below); v^T of both heads goes straight into its
-    //      tiles. Lanes map onto the 8 rows of a core matrix, so each 16-byte
+    //      tiles (normalised below); v^T follows once the first products are
+    //      issued. Lanes map onto the 8 rows of a core matrix, so each 16-byte
     //      store of a warp phase fills one contiguous 128-byte core matrix.
     const unsigned char *raw = sm + S1_RAW;
     // Each pass loads the inputs of four iterations before it stores anything,
@@ -282,37 +282,6 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
                 o[e] = p < nv ? silu_fast(u) : 0.0f;
             }
             *reinterpret_cast<float4 *>(sm + (tile ? S1_KS : S1_QS) + km<4>(p, d, DK)) = make_float4(o[0], o[1], o[2], o[3]);
-        }
-    }
-    for (int it0 = warp; it0 < 128; it0 += 4 * NW1) {                // v^T: (head, row octet of j, token group)
-        bf16 xr[4][7];
-        float4 w4[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int it = it0 + k * NW1, hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
-            const int d = dob * 8 + (lane & 7);
-            const int p0 = 4 * (pgh * 4 + (lane >> 3));              // tokens p0..p0+3
-            w4[k] = reinterpret_cast<const float4 *>(sm + S1_CW + (2 + hv) * 2048)[d];
-#pragma unroll
-            for (int m = 0; m < 7; ++m)                               // positions p0-3 .. p0+3
-                xr[k][m] = *reinterpret_cast<const bf16 *>(raw + (2 + hv) * RAW_SEG + (p0 + m) * RAW_ROWB + d * 2);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int it = it0 + k * NW1, hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
-            const int d = dob * 8 + (lane & 7);
-            const int p0 = 4 * (pgh * 4 + (lane >> 3));
-            const float4 w = w4[k];
-            float x[7];
-#pragma unroll
-            for (int m = 0; m < 7; ++m) x[m] = to_f(xr[k][m]);
-            float o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float u = w.x * x[e] + w.y * x[e + 1] + w.z * x[e + 2] + w.w * x[e + 3];
-                o[e] = (p0 + e) < nv ? tc::tf32_rn(silu_fast(u)) : 0.0f;
-            }
-            *reinterpret_cast<float4 *>(sm + (hv ? S1_VT1 : S1_VT0) + km<4>(d, p0, CH)) = make_float4(o[0], o[1], o[2], o[3]);
         }
     }
     __syncthreads();
@@ -366,6 +335,40 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
         tc::mma_tile<true>(tm + T1_QK, sbase + S1_QS, DK, sbase + S1_KS, DK, DK, id, false);
         tc::mma_commit(smem_u32(&ss.bar));
     }
+    // The value stream's conv runs while the tensor core computes K K^T and Q K^T:
+    // v^T of both heads goes straight into its tiles.
+    for (int it0 = warp; it0 < 128; it0 += 4 * NW1) {                // v^T: (head, row octet of j, token group)
+        bf16 xr[4][7];
+        float4 w4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int it = it0 + k * NW1, hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
+            const int d = dob * 8 + (lane & 7);
+            const int p0 = 4 * (pgh * 4 + (lane >> 3));              // tokens p0..p0+3
+            w4[k] = reinterpret_cast<const float4 *>(sm + S1_CW + (2 + hv) * 2048)[d];
+#pragma unroll
+            for (int m = 0; m < 7; ++m)                               // positions p0-3 .. p0+3
+                xr[k][m] = *reinterpret_cast<const bf16 *>(raw + (2 + hv) * RAW_SEG + (p0 + m) * RAW_ROWB + d * 2);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int it = it0 + k * NW1, hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
+            const int d = dob * 8 + (lane & 7);
+            const int p0 = 4 * (pgh * 4 + (lane >> 3));
+            const float4 w = w4[k];
+            float x[7];
+#pragma unroll
+            for (int m = 0; m < 7; ++m) x[m] = to_f(xr[k][m]);
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float u = w.x * x[e] + w.y * x[e + 1] + w.z * x[e + 2] + w.w * x[e + 3];
+                o[e] = (p0 + e) < nv ? tc::tf32_rn(silu_fast(u)) : 0.0f;
+            }
+            *reinterpret_cast<float4 *>(sm + (hv ? S1_VT1 : S1_VT0) + km<4>(d, p0, CH)) = make_float4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    __syncthreads();                                   // every read of the staged rows is done
     if (!mbar_wait_bounded(smem_u32(&ss.bar), 0)) ss.abort = 1;
     tc::fence_after_sync();
 
@@ -374,7 +377,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     blob[1] = a.blobs + ((size_t)g * HV + kh + HK) * BLOB_BYTES;
 
     // ---- E. P = Mask o QK^T and beta * L from the M=64 accumulators (row t in
-    //      TMEM lane 32*(t/16) + t%16), then Q~, K~^T and gamma_n. Warp w reads
+    //      TMEM lane 32*(t/16) + t%16), then Q~ and gamma_n. Warp w reads
     //      columns [16 (w / 4), +16) of its lane quarter w % 4.
     {
         const int q = warp & 3, hf = warp >> 2;
@@ -422,19 +425,6 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
                                    from_f<bf16>(x0.w * gm), from_f<bf16>(x1.x * gm), from_f<bf16>(x1.y * gm),
                                    from_f<bf16>(x1.z * gm), from_f<bf16>(x1.w * gm)};
         *reinterpret_cast<uint4 *>(blob[h] + BLOB_Q + km<2>(t, i8 * 8, DK)) = *reinterpret_cast<const uint4 *>(o);
-    }
-    // K~^T [i][t] = exp(G_n - G_t) k^[t][i] -> tf32 K-major (Kd 64), 4 tokens per
-    // store; lanes cover 4 whole core matrices, so a warp writes 512 contiguous bytes
-    for (int it = warp; it < 2 * 16 * 4; it += P1_THREADS / 32) {
-        const int h = it >> 6, i = ((it >> 2) & 15) * 8 + (lane & 7), t4 = (it & 3) * 4 + (lane >> 3);
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int t = t4 * 4 + e;
-            v[e] = ss.ktf[h][t] * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(t, i, DK));
-        }
-        *reinterpret_cast<float4 *>(blob[h] + BLOB_KT + km<4>(i, t4 * 4, CH)) =
-            tc::tf32_rn(make_float4(v[0], v[1], v[2], v[3]));
     }
     if (tid < 2) *reinterpret_cast<float *>(blob[tid] + BLOB_G) = ss.gam[tid][CH - 1];
     tc::fence_before_sync();
@@ -567,6 +557,21 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
             tc::mma_tile<true>(tm + T1_W + 64 * h, sbase + (h ? S1_GK1 : S1_QS), CH, ts, CH, CH, id, false);
         }
         tc::mma_commit(smem_u32(&ss.bar));
+    }
+    // While the tensor core computes U and W: K~^T to the blob (k^ stays intact
+    // in its tile until the kernel ends).
+    // K~^T [i][t] = exp(G_n - G_t) k^[t][i] -> tf32 K-major (Kd 64), 4 tokens per
+    // store; lanes cover 4 whole core matrices, so a warp writes 512 contiguous bytes
+    for (int it = warp; it < 2 * 16 * 4; it += P1_THREADS / 32) {
+        const int h = it >> 6, i = ((it >> 2) & 15) * 8 + (lane & 7), t4 = (it & 3) * 4 + (lane >> 3);
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int t = t4 * 4 + e;
+            v[e] = ss.ktf[h][t] * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(t, i, DK));
+        }
+        *reinterpret_cast<float4 *>(blob[h] + BLOB_KT + km<4>(i, t4 * 4, CH)) =
+            tc::tf32_rn(make_float4(v[0], v[1], v[2], v[3]));
     }
     if (!ss.abort && !mbar_wait_bounded(smem_u32(&ss.bar), 1)) ss.abort = 1;
     tc::fence_after_sync();
