@@ -92,6 +92,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
+// ---- programmatic dependent launch
+// A kernel launched with the programmatic-stream-serialization attribute may
+// start before the kernel ahead of it in the stream has finished. It must call
+// grid_dep_wait() before touching memory that kernel writes (or reads and it
+// overwrites): the wait returns once that kernel has completed and its memory
+// operations are visible. In a kernel launched without the attribute it
+// returns at once. grid_dep_launch() lets the kernel behind this one start
+// early; it only changes scheduling, never what the waiting kernel sees.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- thread-block clusters and distributed shared memory
 
 // This CTA's rank within its cluster.

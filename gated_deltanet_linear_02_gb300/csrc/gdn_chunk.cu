@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(1024) chunk_schedule_kernel(const int32_t *__r
                                                               int4 *__restrict__ chunk_info)
 {
     __shared__ int warp_part[32];
+    grid_dep_launch();                                 // the prep kernel may be scheduled now
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (N + 1023) / 1024;
     const int lo = min(tid * per, N), hi = min(lo + per, N);
@@ -180,6 +181,8 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x, kh = blockIdx.y;
 
+    grid_dep_wait();                                   // chunk_info comes from the schedule kernel
+    grid_dep_launch();
     const int4 ci = __ldg(a.chunk_info + g);
     if (ci.x < 0) return;                              // no chunk here (uniform for the whole CTA)
     const int n = ci.x;                                // sequence
@@ -702,6 +705,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
     const bool trow = lane < 16;
     const int j0 = JB * jb + 16 * hf;                  // first of this thread's 16 value columns
     const size_t sbase_g = ((size_t)n * HV + vh) * (DV * DK);
+    grid_dep_wait();                                   // the blobs come from the prep kernel
+    grid_dep_launch();
     const int g0 = __ldg(a.chunk_off + n);
     const int nc = max(0, __ldg(a.chunk_off + n + 1) - g0);
     const int seq0 = cu_clamp(a.cu, n, 0, a.T_total);
@@ -914,9 +919,9 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
 // ---------------------------------------------------------------- launcher
 
 cudaError_t launch_conv_state_out_bf16(const int32_t *cu, int N, int T_total, const void *qkv, const void *cs_in,
-                                       void *cs_out, cudaStream_t s);
+                                       void *cs_out, cudaStream_t s, bool pdl);
 cudaError_t launch_gated_norm_bf16(const float *norm_w, float norm_eps, const void *z, const float *y, void *out,
-                                   int T_total, gdn_dtype out_dt, cudaStream_t s);
+                                   int T_total, gdn_dtype out_dt, cudaStream_t s, bool pdl);
 
 static size_t off_info(int N) { return ((size_t)(N + 1) * sizeof(int32_t) + 255) & ~(size_t)255; }
 static size_t off_blobs(int N, int T_total)
@@ -959,13 +964,17 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
     CUtensorMap qkv_map;
     if (T_total > 0 && !make_bf16_plain_map(&qkv_map, qkv, T_total, CC, RAW_COLS, RAW_ROWS))
         return cudaErrorInvalidValue;
+    // The kernels after the schedule kernel are launched with programmatic
+    // stream serialization: each may start while the one ahead finishes, and
+    // waits (grid_dep_wait) before it reads that kernel's results.
     chunk_schedule_kernel<<<1, 1024, 0, s>>>(cu, N, T_total, a.max_chunks, a.chunk_off, a.chunk_info);
-    if (a.max_chunks > 0 && T_total > 0)
-        chunk_prep_kernel<<<dim3(a.max_chunks, HK), P1_THREADS, P1_SMEM, s>>>(qkv_map, a);
-    chunk_carry_kernel<<<dim3(N, HV, NJB), P2_THREADS, P2_SMEM, s>>>(a);
     e = cudaGetLastError();
-    if (e == cudaSuccess) e = launch_gated_norm_bf16(p->norm_w, p->norm_eps, z, a.ybuf, out, T_total, out_dt, s);
-    if (e == cudaSuccess && cs_out) e = launch_conv_state_out_bf16(cu, N, T_total, qkv, cs_in, cs_out, s);
+    if (e == cudaSuccess && a.max_chunks > 0 && T_total > 0)
+        e = launch_pdl(chunk_prep_kernel, dim3(a.max_chunks, HK), dim3(P1_THREADS), P1_SMEM, s, qkv_map, a);
+    if (e == cudaSuccess) e = launch_pdl(chunk_carry_kernel, dim3(N, HV, NJB), dim3(P2_THREADS), P2_SMEM, s, a);
+    if (e == cudaSuccess)
+        e = launch_gated_norm_bf16(p->norm_w, p->norm_eps, z, a.ybuf, out, T_total, out_dt, s, true);
+    if (e == cudaSuccess && cs_out) e = launch_conv_state_out_bf16(cu, N, T_total, qkv, cs_in, cs_out, s, true);
     return e;
 }
 

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/gdn.h"
 
 namespace gdn {
@@ -71,6 +73,27 @@ __device__ __forceinline__ void gates_f(float A_log, float dt_bias, float alpha,
     const float g = -expf(A_log) * softplus_f(alpha + dt_bias);
     a = expf(g);
     b = 1.0f / (1.0f + expf(-beta_logit));
+}
+
+// Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialization allowed: the kernel may start before the one ahead of it in the
+// stream has finished, and must call grid_dep_wait() (gdn_async.cuh) before it
+// touches that kernel's results.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace gdn

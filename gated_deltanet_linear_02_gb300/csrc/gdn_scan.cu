@@ -18,6 +18,7 @@
 //   4. conv out:  the last three raw inputs of each sequence, taken from its
 //                 tail or from conv_state_in, become conv_state_out.
 // Kernel 4 runs last, so conv_state_out may alias conv_state_in.
+#include "gdn_async.cuh"
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -194,6 +195,8 @@ __global__ void __launch_bounds__(256) scan_norm_kernel(const float *__restrict_
 {
     const size_t t = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dep_wait();                                   // y comes from the kernel ahead
+    grid_dep_launch();
     const float4 w = *reinterpret_cast<const float4 *>(norm_w + lane * 4);
 #pragma unroll
     for (int hh = 0; hh < HV / 8; ++hh) {
@@ -219,6 +222,7 @@ __global__ void __launch_bounds__(256) conv_state_out_kernel(const int32_t *__re
 {
     const int n = blockIdx.y;
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    grid_dep_wait();                                   // cs_out may alias cs_in, which earlier kernels read
     const int start = cu_at(cu, n, 0, T_total), L = cu_at(cu, n + 1, start, T_total) - start;
     TA nv[KC - 1];
 #pragma unroll
@@ -294,25 +298,37 @@ namespace gdn {
 
 // The gated RMSNorm . silu(z) over a [T][4096] fp32 buffer of y (scale
 // applied), for the chunked path (bf16 activations).
+// pdl: launched with programmatic stream serialization (the kernels wait for
+// the kernel ahead before reading its results).
 cudaError_t launch_gated_norm_bf16(const float *norm_w, float norm_eps, const void *z, const float *y, void *out,
-                                   int T_total, gdn_dtype out_dt, cudaStream_t s)
+                                   int T_total, gdn_dtype out_dt, cudaStream_t s, bool pdl)
 {
     if (T_total <= 0) return cudaSuccess;
     ScanWs ws;
     ws.x = nullptr;
     ws.g = nullptr;
     ws.y = const_cast<float *>(y);
-    if (out_dt == GDN_F32)
-        scan_norm_kernel<bf16, float><<<T_total, 256, 0, s>>>(norm_w, norm_eps, (const bf16 *)z, (float *)out, ws);
-    else
-        scan_norm_kernel<bf16, bf16><<<T_total, 256, 0, s>>>(norm_w, norm_eps, (const bf16 *)z, (bf16 *)out, ws);
+    const bf16 *zb = (const bf16 *)z;
+    if (out_dt == GDN_F32) {
+        if (pdl) return launch_pdl(scan_norm_kernel<bf16, float>, dim3(T_total), dim3(256), 0, s, norm_w, norm_eps, zb,
+                                   (float *)out, ws);
+        scan_norm_kernel<bf16, float><<<T_total, 256, 0, s>>>(norm_w, norm_eps, zb, (float *)out, ws);
+    } else {
+        if (pdl) return launch_pdl(scan_norm_kernel<bf16, bf16>, dim3(T_total), dim3(256), 0, s, norm_w, norm_eps, zb,
+                                   (bf16 *)out, ws);
+        scan_norm_kernel<bf16, bf16><<<T_total, 256, 0, s>>>(norm_w, norm_eps, zb, (bf16 *)out, ws);
+    }
     return cudaGetLastError();
 }
 
 // conv_state_out for the chunked path (bf16 activations); same rule as above.
 cudaError_t launch_conv_state_out_bf16(const int32_t *cu, int N, int T_total, const void *qkv, const void *cs_in,
-                                       void *cs_out, cudaStream_t s)
+                                       void *cs_out, cudaStream_t s, bool pdl)
 {
+    if (N <= 0) return cudaSuccess;
+    if (pdl)
+        return launch_pdl(conv_state_out_kernel<bf16>, dim3(CC / 256, N), dim3(256), 0, s, cu, T_total,
+                          (const bf16 *)qkv, (const bf16 *)cs_in, (bf16 *)cs_out);
     conv_state_out_kernel<bf16><<<dim3(CC / 256, N), 256, 0, s>>>(cu, T_total, (const bf16 *)qkv,
                                                                   (const bf16 *)cs_in, (bf16 *)cs_out);
     return cudaGetLastError();
