@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_block_kernel(const __grid_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int item = blockIdx.x;
     const int sp = item % a.S, bg = item / a.S, b = bg / AT_HKV, g = bg % AT_HKV;
+    grid_dep_wait();                                   // q, the cache and ctx_len may come from the kernel ahead
+    grid_dep_launch();
     const int L = min(max(__ldg(a.ctx_len + b), 0), a.Lmax);
     const int p0 = sp * a.tps * AT_TILE;               // this block's positions [p0, p1)
     const int p1 = min(L, p0 + a.tps * AT_TILE);
@@ -430,6 +432,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restri
     const int bh = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (bh >= B * AT_HQ) return;
     const int b = bh / AT_HQ, h = bh % AT_HQ, g = h / AT_G, hl = h % AT_G;
+    grid_dep_wait();                                   // the partials come from the block kernel
     const int L = min(max(__ldg(ctx_len + b), 0), Lmax);
     const int nb = (L + tps * AT_TILE - 1) / (tps * AT_TILE);
     if (nb <= 1) return;                               // finished in place (or an empty context)
@@ -524,12 +527,12 @@ static cudaError_t launch_attn_typed(const CUtensorMap &km, const CUtensorMap &v
         }
     }
     const size_t items = (size_t)B * AT_HKV * a.S;
-    attn_block_kernel<TO><<<(unsigned)items, AT_THREADS, AT_SMEM, s>>>(km, vm, a);
-    e = cudaGetLastError();
+    // both kernels use programmatic stream serialization (see grid_dep_wait)
+    e = launch_pdl(attn_block_kernel<TO>, dim3((unsigned)items), dim3(AT_THREADS), AT_SMEM, s, km, vm, a);
     if (e != cudaSuccess || a.S == 1) return e;        // one block per context: nothing to merge
-    attn_combine_kernel<TO><<<(unsigned)((B * AT_HQ + 7) / 8), 256, 0, s>>>(a.part_o, a.part_ml, a.ctx_len, a.z,
-                                                                            a.out, B, a.Lmax, a.S, a.tps);
-    return cudaGetLastError();
+    return launch_pdl(attn_combine_kernel<TO>, dim3((unsigned)((B * AT_HQ + 7) / 8)), dim3(256), 0, s,
+                      (const float *)a.part_o, (const float *)a.part_ml, a.ctx_len, a.z, a.out, B, a.Lmax, a.S,
+                      a.tps);
 }
 
 cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,

@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
         fence_mbar_init();
     }
     __syncthreads();
+    grid_dep_wait();                                   // inputs and states may come from the kernel ahead
+    grid_dep_launch();
 
     if (warp == DEC_WARPS) {
         // ---- producer: unit u goes into slot u % DEC_SLOTS once the compute
@@ -361,8 +363,9 @@ static cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s)
     const int n_sm = sm_count();
     if (n_sm <= 0) return cudaErrorInvalidDevice;
     const int grid = a.n_items < n_sm ? a.n_items : n_sm;
-    decode_step_kernel<TA, TO><<<grid, DEC_THREADS, DEC_SMEM, s>>>(a);
-    return cudaGetLastError();
+    // programmatic stream serialization: this launch may start while the kernel
+    // ahead drains; the kernel waits for it before its first global access
+    return launch_pdl(decode_step_kernel<TA, TO>, dim3(grid), dim3(DEC_THREADS), DEC_SMEM, s, a);
 }
 
 cudaError_t launch_decode_step(const gdn_params *p, const void *qkv, const void *z, const void *alpha,

@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
         fence_mbar_init();
     }
     __syncthreads();
+    grid_dep_wait();                                   // inputs and states may come from the kernel ahead
+    grid_dep_launch();
 
     if (warp == MD_WARPS) {
         // ---- producer: unit u goes into slot u % MD_SLOTS once the compute warps
@@ -343,8 +345,7 @@ static cudaError_t launch_multi_t(const MultiArgs &a, cudaStream_t s)
     const int n_sm = sm_count();
     if (n_sm <= 0) return cudaErrorInvalidDevice;
     const int grid = a.n_items < n_sm ? a.n_items : n_sm;
-    decode_multi_kernel<TA, TO><<<grid, MD_THREADS, MD_SMEM, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_multi_kernel<TA, TO>, dim3(grid), dim3(MD_THREADS), MD_SMEM, s, a);
 }
 
 cudaError_t launch_decode_multi(const gdn_params *p, const void *qkv, const void *z, const void *alpha,

@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_consta
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = sm.tmem;
+    grid_dep_wait();                                   // the operands may come from the kernel ahead
+    grid_dep_launch();
 
     if (warp == 0) {
         // ---- TMA producer
@@ -389,13 +391,17 @@ static cudaError_t launch_proj(const void *x, const void *w, const ProjOut &out,
     cfg.blockDim = dim3(GM_THREADS);
     cfg.dynamicSmemBytes = GM_SMEM;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    // programmatic stream serialization (the kernel waits for the kernel ahead
+    // before its first global access), plus the cluster shape when splitting K
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)splits;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = splits > 1 ? 1 : 0;
+    cfg.numAttrs = splits > 1 ? 2 : 1;
     return out_dt == GDN_F32 ? cudaLaunchKernelEx(&cfg, proj_kernel<float>, mx, mw, out, M, N, K, splits)
                              : cudaLaunchKernelEx(&cfg, proj_kernel<bf16>, mx, mw, out, M, N, K, splits);
 }
