@@ -242,55 +242,60 @@ def run_gpu(args, rank, world, dev):
     for L in layers:
         st = L["st"]
         host_in.append([t[0].cpu().pin_memory() for t in (st.qkv, st.z, st.alpha, st.beta)])
-    dev_in = [[torch.empty_like(t, device=dev) for t in h] for h in host_in]
+    # Device inputs and host outputs are double-buffered by step parity, so that
+    # step k's uploads and downloads overlap the kernels of neighbouring steps:
+    # the upload stream fills the inputs of step k+1 while step k computes, and
+    # the download stream drains step k's outputs while step k+1 computes. Each
+    # stream waits on one event per step; the 30 kernels of a step run back to
+    # back on the compute stream.
+    dev_in = [[[torch.empty_like(t, device=dev) for t in h] for h in host_in] for _ in range(2)]
+    dev_out = [[torch.empty(BATCH, I.D_INNER, dtype=torch.bfloat16, device=dev) for _ in layers] for _ in range(2)]
     host_out = [torch.empty(BATCH, I.D_INNER, dtype=torch.bfloat16).pin_memory() for _ in layers]
     h2d = sum(t.numel() * t.element_size() for h in host_in for t in h)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-
-    # The copies run on two copy streams and overlap the kernels: layer l's
-    # inputs go up while earlier layers compute, and its output comes back while
-    # later layers compute. Events order each layer's buffers: a step's upload
-    # of layer l waits until the previous step's kernel of layer l has read
-    # them, and the kernel waits until the previous download of its output is
-    # done.
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    n_l = len(layers)
-    ev = lambda: [torch.cuda.Event() for _ in range(n_l)]
-    in_ready, computed, downloaded = ev(), ev(), ev()
+    uploaded = [torch.cuda.Event() for _ in range(2)]     # inputs of the step with this parity are in
+    computed = [torch.cuda.Event() for _ in range(2)]     # kernels of the step with this parity are done
+    downloaded = [torch.cuda.Event() for _ in range(2)]   # outputs of the step with this parity are out
 
-    def e2e_step():
-        for l, (h, d) in enumerate(zip(host_in, dev_in)):
-            up.wait_event(computed[l])
-            with torch.cuda.stream(up):
+    def upload(k):
+        up.wait_event(computed[k % 2])                     # step k-2 has finished reading these buffers
+        with torch.cuda.stream(up):
+            for h, d in zip(host_in, dev_in[k % 2]):
                 for src, dst in zip(h, d):
                     dst.copy_(src, non_blocking=True)
-                in_ready[l].record(up)
-        for l, (L, d, ho) in enumerate(zip(layers, dev_in, host_out)):
-            stream.wait_event(in_ready[l])
-            stream.wait_event(downloaded[l])
-            ops.decode_step(None, d[0], d[1], d[2], d[3], L["conv"], L["S"], L["out"], cparams=L["cp"],
-                            stream=stream)
-            computed[l].record(stream)
-            down.wait_event(computed[l])
-            with torch.cuda.stream(down):
-                ho.copy_(L["out"], non_blocking=True)
-                downloaded[l].record(down)
+            uploaded[k % 2].record(up)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    def e2e_step(k):
+        upload(k + 1)
+        stream.wait_event(uploaded[k % 2])
+        stream.wait_event(downloaded[k % 2])               # step k-2's outputs have left these buffers
+        for L, d, o in zip(layers, dev_in[k % 2], dev_out[k % 2]):
+            ops.decode_step(None, d[0], d[1], d[2], d[3], L["conv"], L["S"], o, cparams=L["cp"], stream=stream)
+        computed[k % 2].record(stream)
+        down.wait_event(computed[k % 2])
+        with torch.cuda.stream(down):
+            for o, ho in zip(dev_out[k % 2], host_out):
+                ho.copy_(o, non_blocking=True)
+            downloaded[k % 2].record(down)
+
+    upload(0)
+    for k in range(max(1, args.warmup)):
+        e2e_step(k)
     barrier_sync()
+    k0 = max(1, args.warmup)
     ev0.record(stream)
     up.wait_event(ev0)
     down.wait_event(ev0)
-    for _ in range(args.steps):
-        e2e_step()
+    for k in range(k0, k0 + args.steps):
+        e2e_step(k)
     stream.wait_stream(up)
     stream.wait_stream(down)
     ev1.record(stream)
     barrier_sync()
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1))
     e2e_tok_s = job_rate(BATCH * args.steps, world, e2e_ms)
-    del layers, host_in, dev_in, host_out
+    del layers, host_in, dev_in, dev_out, host_out
     torch.cuda.empty_cache()
 
     # ---------------- prefill @ T=4096 (bf16, zero initial state)
