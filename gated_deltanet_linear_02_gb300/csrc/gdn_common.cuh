@@ -39,6 +39,25 @@ template <> __device__ __forceinline__ float from_f<float>(float x) { return x; 
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
 
 // SiLU(x) = x * sigmoid(x) (the conv activation and the output gate silu(z)).
+// 4 consecutive elements (8-byte aligned for bf16, 16-byte for fp32) as one
+// vector load or store
+__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 load4(const bf16 *p)
+{
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void store4(bf16 *p, float4 v)
+{
+    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.x)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.y)) << 16);
+    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.z)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v.w)) << 16);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(lo, hi);
+}
+
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
 // SiLU with the fast exponential and division intrinsics (a few ulp). Used only

@@ -201,14 +201,13 @@ __global__ void __launch_bounds__(256) scan_norm_kernel(const float *__restrict_
 #pragma unroll
     for (int hh = 0; hh < HV / 8; ++hh) {
         const int vh = warp * (HV / 8) + hh;
-        const size_t o = t * DI + vh * DV + lane * 4;
+        const size_t o = t * DI + vh * DV + lane * 4;      // 4 consecutive elements: one vector access each
         const float4 y = *reinterpret_cast<const float4 *>(ws.y + o);
+        const float4 zz = load4(z + o);
         const float ms = warp_sum(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w) * (1.0f / DV);
         const float rr = rsqrtf(ms + norm_eps);
-        out[o + 0] = from_f<TO>(y.x * rr * w.x * silu_f(to_f(z[o + 0])));
-        out[o + 1] = from_f<TO>(y.y * rr * w.y * silu_f(to_f(z[o + 1])));
-        out[o + 2] = from_f<TO>(y.z * rr * w.z * silu_f(to_f(z[o + 2])));
-        out[o + 3] = from_f<TO>(y.w * rr * w.w * silu_f(to_f(z[o + 3])));
+        store4(out + o, make_float4(y.x * rr * w.x * silu_f(zz.x), y.y * rr * w.y * silu_f(zz.y),
+                                    y.z * rr * w.z * silu_f(zz.z), y.w * rr * w.w * silu_f(zz.w)));
     }
 }
 
