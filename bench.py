@@ -62,10 +62,10 @@ PREFILL_FLOP_PER_TOKEN = 5_242_880
 # the bf16 output written once (3 x B x 16 x 256 x 2 B), ctx_len (B x 4 B).
 ATTN_LAYERS, ATTN_CTX = 10, 4096
 ATTN_BYTES_PER_CALL = BATCH * 2 * ATTN_CTX * 256 * 2 * 2 + 3 * BATCH * 16 * 256 * 2 + BATCH * 4
-# DRAM traffic of one attn_block_kernel launch at B=256, scaled by 4 from the
-# ncu capture at B=64 (the blocks and their bytes grow with B), from
-# profiles/attn_decode_B256_ctx4096.md. None once the kernel changes.
-ATTN_TRAFFIC_PER_CALL = (537_517_312 + 8_822_784) * 4
+# DRAM traffic of one attn_block_kernel launch at B=256 (ncu capture in
+# profiles/attn_decode_B256_ctx4096.md). None once the kernel or its launch
+# shape changes without a new capture.
+ATTN_TRAFFIC_PER_CALL = None
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch at B=256
 # (one layer, cold L2), from the ncu capture in

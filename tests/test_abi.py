@@ -159,8 +159,8 @@ def test_out_proj_argument_checks(ops):
 def test_attn_decode_argument_checks(ops):
     L = ops.lib()
     ws = L.gdn_attn_decode_workspace_size(256, 4096)
-    # 256 sequences x 2 KV heads x 8 blocks of 512 positions, each 8 x 256 outputs + 8 (max, sum) pairs
-    assert ws == 256 * 2 * 8 * (8 * 256 + 16) * 4
+    # 256 sequences x 2 KV heads x 4 blocks of 1024 positions, each 8 x 256 outputs + 8 (max, sum) pairs
+    assert ws == 256 * 2 * 4 * (8 * 256 + 16) * 4
     assert L.gdn_attn_decode_workspace_size(1, 300) == 2 * 3 * (8 * 256 + 16) * 4   # small batch: 1-tile blocks
     assert L.gdn_attn_decode_workspace_size(0, 10) == 0 and L.gdn_attn_decode_workspace_size(3, 0) == 0
     assert L.gdn_attn_decode_workspace_size(3, 1 << 28) == 0                        # B * 2 * Lmax > 2^30

@@ -99,13 +99,14 @@ def test_attn_one_tile_blocks(ops):
 
 
 def test_attn_two_tile_blocks_sampled(ops):
-    # B = 8 at 16K: 2-tile blocks; sequences sampled for the oracle
-    inp = I.attn_inputs(I.seed_of(23), 8, 16384, [16384, 16000, 1, 8191, 8193, 300, 16384, 129], device=DEV)
-    check(ops, inp, seqs=[0, 1, 3, 4, 7], label="B=8 L=16384")
+    # B = 16 at 16K: 2-tile blocks; sequences sampled for the oracle
+    lens = [16384, 16000, 1, 8191, 8193, 300, 16384, 129, 256, 255, 257, 1024, 1023, 1025, 4000, 9999]
+    inp = I.attn_inputs(I.seed_of(23), 16, 16384, lens, device=DEV)
+    check(ops, inp, seqs=[0, 1, 3, 4, 7, 10, 13], label="B=16 L=16384")
 
 
 def test_attn_decode_batch_full_size_sampled(ops):
-    # the benchmarked step: B = 256 sequences at 4K context, 4-tile blocks;
+    # the benchmarked step: B = 256 sequences at 4K context, 8-tile blocks;
     # sampled sequences against the oracle, the others only checked finite
     inp = I.attn_inputs(I.seed_of(24), 256, 4096, device=DEV)
     out = check(ops, inp, seqs=[0, 1, 77, 128, 255], label="B=256 L=4096")
