@@ -9,7 +9,8 @@
 //  - the output projection "cur = ssm_out . gated" (section "Output path"),
 //    4096 -> 2048.
 //
-// Design. A persistent grid walks output tiles of 128 rows x 256 columns (the
+// Design. A persistent grid walks output tiles of 128 rows x 256 columns, or
+// x 128 columns when the 256-wide tiles would fill less than half the GPU (the
 // last column tile may be partial: weight rows past N read as zero and their
 // columns are not stored). Per CTA:
 //  - warp 0, lane 0: the TMA producer. 2-D tensor-map copies bring 64-wide K
@@ -43,15 +44,23 @@ namespace gdn {
 
 __device__ unsigned int g_gemm_error;   // GDN_ERR_TIMEOUT if a bounded wait gave up
 
-constexpr int GM_BM = 128, GM_BN = 256, GM_BK = 64, GM_STAGES = 4;
+constexpr int GM_BM = 128, GM_BK = 64;
 constexpr uint32_t GM_A_BYTES = GM_BM * GM_BK * 2;        // 16 KiB
-constexpr uint32_t GM_B_BYTES = GM_BN * GM_BK * 2;        // 32 KiB
-constexpr uint32_t GM_STAGE_BYTES = GM_A_BYTES + GM_B_BYTES;
 constexpr int GM_THREADS = 192;                   // TMA warp, MMA warp, 4 epilogue warps
-constexpr uint32_t GM_TMEM_COLS = 2 * GM_BN;      // two accumulators
-constexpr int GM_PART_LD = GM_BN + 4;             // fp32 partial row stride (floats): rows fall on other banks
-static_assert(GM_BM * GM_PART_LD * 4 <= GM_STAGES * GM_STAGE_BYTES, "split-K partial fits the stages");
 static_assert(GM_BK == 64, "K slices are the 64-column boxes of make_bf16_sw128_map");
+
+// Tile width BN = 256 (large M), or 128 when the 256-wide tiles would leave
+// most SMs idle (a decode batch): twice the tiles, each half as long to issue.
+template <int BN>
+struct GemmCfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr uint32_t B_BYTES = BN * GM_BK * 2;
+    static constexpr uint32_t STAGE_BYTES = GM_A_BYTES + B_BYTES;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;         // two accumulators
+    static constexpr int PART_LD = BN + 4;                // fp32 partial row stride (floats): rows fall on other banks
+    static_assert(GM_BM * PART_LD * 4 <= STAGES * STAGE_BYTES, "split-K partial fits the stages");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+};
 
 // Where the GEMM's output columns go: columns [c0[s], c0[s+1]) are written to
 // ptr[s] as rows of ld[s] elements (column c lands at ptr[s][m * ld[s] + c - c0[s]]).
@@ -63,24 +72,30 @@ struct ProjOut {
     int nseg;
 };
 
+template <int BN>
 struct GemmSmem {
-    alignas(1024) unsigned char stage[GM_STAGES][GM_STAGE_BYTES];   // A tile | B tile, 1024-byte aligned
-    alignas(8) uint64_t full[GM_STAGES], empty[GM_STAGES];
+    static constexpr int STAGES = GemmCfg<BN>::STAGES;
+    alignas(1024) unsigned char stage[STAGES][GemmCfg<BN>::STAGE_BYTES];   // A tile | B tile, 1024-byte aligned
+    alignas(8) uint64_t full[STAGES], empty[STAGES];
     uint64_t acc_full[2], acc_empty[2];
-    int last_it[GM_STAGES];                       // last K slice loaded into each stage (for an abort)
+    int last_it[STAGES];                          // last K slice loaded into each stage (for an abort)
     uint32_t tmem;
     int abort;
 };
-constexpr size_t GM_SMEM = sizeof(GemmSmem) + 1024;   // + slack to align the block to 1024 bytes
+template <int BN>
+constexpr size_t gm_smem() { return sizeof(GemmSmem<BN>) + 1024; }   // + slack to align the block to 1024 bytes
 
-template <typename TO>
+template <typename TO, int BN>
 __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_constant__ CUtensorMap mx,
                                                              const __grid_constant__ CUtensorMap mw,
                                                              const ProjOut out, int M, int N, int K, int splits)
 {
+    using Cfg = GemmCfg<BN>;
+    constexpr int GM_BN = BN, GM_STAGES = Cfg::STAGES, GM_PART_LD = Cfg::PART_LD;
+    constexpr uint32_t GM_TMEM_COLS = Cfg::TMEM_COLS, GM_STAGE_BYTES = Cfg::STAGE_BYTES;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *blk = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    GemmSmem &sm = *reinterpret_cast<GemmSmem *>(blk);
+    GemmSmem<BN> &sm = *reinterpret_cast<GemmSmem<BN> *>(blk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_tiles = (N + GM_BN - 1) / GM_BN;
     // persistent mode: CTAs stride over the tiles with all K slices each;
@@ -323,10 +338,42 @@ bool make_bf16_plain_map(CUtensorMap *map, const void *base, long long rows, int
 int sm_count();
 
 // Per-device set-up of the projection kernels, done once: the shared-memory
-// attribute, and how many clusters of 2, 4 and 8 CTAs can be resident at once.
+// attribute, and how many clusters of 2, 4 and 8 CTAs can be resident at once,
+// for each tile width.
 struct ProjDevice {
-    int max_clusters[3];
+    int max_clusters[2][3];   // [BN == 128][cluster size 2, 4, 8]
 };
+
+template <int BN>
+static bool proj_setup(int (&max_clusters)[3])
+{
+    if (cudaFuncSetAttribute(proj_kernel<float, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gm_smem<BN>()) != cudaSuccess ||
+        cudaFuncSetAttribute(proj_kernel<bf16, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gm_smem<BN>()) != cudaSuccess)
+        return false;
+    for (int k = 0; k < 3; ++k) {
+        const int cs = 2 << k;
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(cs);
+        q.blockDim = dim3(GM_THREADS);
+        q.dynamicSmemBytes = gm_smem<BN>();
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = (unsigned)cs;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, proj_kernel<bf16, BN>, &q) != cudaSuccess) {
+            cudaGetLastError();                        // a refused query: never split this far
+            n = 0;
+        }
+        max_clusters[k] = n;
+    }
+    return true;
+}
 
 static const ProjDevice *proj_device()
 {
@@ -337,59 +384,32 @@ static const ProjDevice *proj_device()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
     if (!ready[dev]) {
-        if (cudaFuncSetAttribute(proj_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(proj_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GM_SMEM) !=
-                cudaSuccess)
+        if (!proj_setup<256>(dev_info[dev].max_clusters[0]) || !proj_setup<128>(dev_info[dev].max_clusters[1]))
             return nullptr;
-        for (int k = 0; k < 3; ++k) {
-            const int cs = 2 << k;
-            cudaLaunchConfig_t q = {};
-            q.gridDim = dim3(cs);
-            q.blockDim = dim3(GM_THREADS);
-            q.dynamicSmemBytes = GM_SMEM;
-            cudaLaunchAttribute qa[1];
-            qa[0].id = cudaLaunchAttributeClusterDimension;
-            qa[0].val.clusterDim.x = (unsigned)cs;
-            qa[0].val.clusterDim.y = 1;
-            qa[0].val.clusterDim.z = 1;
-            q.attrs = qa;
-            q.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, proj_kernel<bf16>, &q) != cudaSuccess) {
-                cudaGetLastError();                    // a refused query: never split this far
-                n = 0;
-            }
-            dev_info[dev].max_clusters[k] = n;
-        }
         ready[dev] = true;
     }
     return &dev_info[dev];
 }
 
-// y[M][N] = x[M][K] w[N][K]^T with the output columns routed by `out`.
-static cudaError_t launch_proj(const void *x, const void *w, const ProjOut &out, int M, int N, int K,
-                               gdn_dtype out_dt, cudaStream_t s)
+template <int BN>
+static cudaError_t launch_proj_bn(const void *x, const void *w, const ProjOut &out, int M, int N, int K,
+                                  gdn_dtype out_dt, cudaStream_t s, int n_sm, const int (&max_clusters)[3])
 {
-    if (M <= 0) return cudaSuccess;
     CUtensorMap mx, mw;
-    if (!make_bf16_sw128_map(&mx, x, M, K, GM_BM) || !make_bf16_sw128_map(&mw, w, N, K, GM_BN)) return cudaErrorInvalidValue;
-    const int n_work = ((M + GM_BM - 1) / GM_BM) * ((N + GM_BN - 1) / GM_BN);
-    const int n_sm = sm_count();
-    if (n_sm <= 0) return cudaErrorInvalidDevice;
-    const ProjDevice *pd = proj_device();
-    if (!pd) return cudaErrorInvalidDevice;
+    if (!make_bf16_sw128_map(&mx, x, M, K, GM_BM) || !make_bf16_sw128_map(&mw, w, N, K, BN))
+        return cudaErrorInvalidValue;
+    const int n_work = ((M + GM_BM - 1) / GM_BM) * ((N + BN - 1) / BN);
     // Split K (2, 4 or 8 ways) while the tiles fill less than half of the SMs,
     // and only as far as every cluster of that size can be resident at once:
     // a cluster that waits for another to finish costs a whole tile's time.
     int splits = 1;
     while (splits < 8 && n_work * splits * 2 <= n_sm && (K / GM_BK) % (splits * 2) == 0 &&
-           pd->max_clusters[splits == 1 ? 0 : splits == 2 ? 1 : 2] >= n_work)
+           max_clusters[splits == 1 ? 0 : splits == 2 ? 1 : 2] >= n_work)
         splits *= 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits > 1 ? n_work * splits : (n_work < n_sm ? n_work : n_sm));
     cfg.blockDim = dim3(GM_THREADS);
-    cfg.dynamicSmemBytes = GM_SMEM;
+    cfg.dynamicSmemBytes = gm_smem<BN>();
     cfg.stream = s;
     // programmatic stream serialization (the kernel waits for the kernel ahead
     // before its first global access), plus the cluster shape when splitting K
@@ -402,8 +422,23 @@ static cudaError_t launch_proj(const void *x, const void *w, const ProjOut &out,
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = splits > 1 ? 2 : 1;
-    return out_dt == GDN_F32 ? cudaLaunchKernelEx(&cfg, proj_kernel<float>, mx, mw, out, M, N, K, splits)
-                             : cudaLaunchKernelEx(&cfg, proj_kernel<bf16>, mx, mw, out, M, N, K, splits);
+    return out_dt == GDN_F32 ? cudaLaunchKernelEx(&cfg, proj_kernel<float, BN>, mx, mw, out, M, N, K, splits)
+                             : cudaLaunchKernelEx(&cfg, proj_kernel<bf16, BN>, mx, mw, out, M, N, K, splits);
+}
+
+// y[M][N] = x[M][K] w[N][K]^T with the output columns routed by `out`.
+static cudaError_t launch_proj(const void *x, const void *w, const ProjOut &out, int M, int N, int K,
+                               gdn_dtype out_dt, cudaStream_t s)
+{
+    if (M <= 0) return cudaSuccess;
+    const int n_sm = sm_count();
+    if (n_sm <= 0) return cudaErrorInvalidDevice;
+    const ProjDevice *pd = proj_device();
+    if (!pd) return cudaErrorInvalidDevice;
+    const int n_work256 = ((M + GM_BM - 1) / GM_BM) * ((N + 255) / 256);
+    if (n_work256 * 2 <= n_sm)                         // 256-wide tiles would leave most SMs idle
+        return launch_proj_bn<128>(x, w, out, M, N, K, out_dt, s, n_sm, pd->max_clusters[1]);
+    return launch_proj_bn<256>(x, w, out, M, N, K, out_dt, s, n_sm, pd->max_clusters[0]);
 }
 
 cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s)
