@@ -640,7 +640,7 @@ constexpr int P2_THREADS = 32 * (P2_EPI_WARPS + 2);
 constexpr int JB = 32;                 // value columns per CTA
 constexpr int NJB = DV / JB;           // CTAs per V-head
 constexpr uint32_t S2_SS = 0;          // S block bf16, MN-major (N = 32 j, K = 128 i)    8 KiB
-constexpr uint32_t S2_VN = 8192;       // Vnew^T block tf32 [32 j][64 t] Kd64, chunk c at + 8 KiB (c % 2)
+constexpr uint32_t S2_VN = 8192;       // Vnew^T block tf32 [32 j][64 t], 128-byte swizzle, chunk c at + 8 KiB (c % 2)
 constexpr uint32_t S2_WQ0 = 24576;     // W | Q~ (bf16 [t][i] Kd128, 16 KiB each), stage 0
 constexpr uint32_t S2_WQ1 = 57344;     //                                          stage 1
 constexpr uint32_t S2_PK0 = 90112;     // P (tf32 [t][s] Kd64) | K~^T (tf32 [i][t] Kd64), stage 0
@@ -673,6 +673,25 @@ __device__ __forceinline__ void carry_issue(const unsigned char *blob, uint32_t 
         mbar_arrive_expect_tx(smem_u32(&ss.bar_pk[st]), 49152);
         bulk_g2s(sb + (st ? S2_PK1 : S2_PK0), blob + BLOB_P, 49152, smem_u32(&ss.bar_pk[st]));
     }
+}
+
+// Byte offset of Vnew^T element (j, t) in its tile: K-major with the 128-byte
+// swizzle, two atoms of 32 tokens (128-byte rows) x 32 columns j, 4 KiB apart.
+// The 16-byte chunk of row j is permuted by XOR with j % 8, so the 16 tokens a
+// warp stores for one column land in 16 different banks.
+__device__ __forceinline__ uint32_t vn_offset(int j, int t)
+{
+    return (uint32_t)((t >> 5) * 4096 + j * 128 + ((((t & 31) >> 2) ^ (j & 7)) << 4) + (t & 3) * 4);
+}
+
+// D (+)= A B^T over 4 tf32 K steps of 8: A a K-major no-swizzle tile (two core
+// matrices, 256 bytes, per step), B the swizzled Vnew^T atom (32 bytes per step).
+__device__ __forceinline__ void mma_vn(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       bool accumulate)
+{
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+        tc::mma_tf32(d_tmem, a_desc + 16u * s, b_desc + 2u * s, idesc, (accumulate || s > 0) ? 1u : 0u);
 }
 
 // Thread (key row i, column half hf) stores its 16 state values S[i][j], j in
@@ -830,11 +849,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
                 if (!mbar_wait_bounded(smem_u32(&ss.bar_pk[st]), spar)) ss.abort = 1;
                 if (aborted) break;
                 tc::fence_after_sync();
-                const uint64_t vn = tc::kmajor_desc<4>(vnb, 32 * ik, CH);
-                tc::mma_steps<true>(tm + (ik ? T2_DS : T2_S), tc::kmajor_desc<4>(pk + 16384, 32 * ik, CH), vn, 4, id2s,
-                                    ik == 0);
+                const uint64_t vn = tc::sw128_desc(vnb + 4096u * ik);   // tokens [32k, 32k+32): atom k
+                mma_vn(tm + (ik ? T2_DS : T2_S), tc::kmajor_desc<4>(pk + 16384, 32 * ik, CH), vn, id2s, ik == 0);
                 tc::mma_commit(smem_u32(&ss.bar_m2[ik]));
-                tc::mma_steps<true>(tm + ycol, tc::kmajor_desc<4>(pk, 32 * ik, CH), vn, 4, id2y, true);
+                mma_vn(tm + ycol, tc::kmajor_desc<4>(pk, 32 * ik, CH), vn, id2y, true);
                 tc::mma_commit(smem_u32(&ss.bar_y[st][ik]));
             }
         }
@@ -865,7 +883,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
                     const float *u = reinterpret_cast<const float *>(u_cur);
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        *reinterpret_cast<float *>(sm + S2_VN + 8192u * st + km<4>(16 * hf + e, t, CH)) =
+                        *reinterpret_cast<float *>(sm + S2_VN + 8192u * st + vn_offset(16 * hf + e, t)) =
                             tc::tf32_rn(u[e] - (d[e] + d1[e]));
                 }
             }
