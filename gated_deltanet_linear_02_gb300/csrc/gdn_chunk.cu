@@ -633,8 +633,9 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
 // its half of Y += P Vnew behind its half of the state update. Eight more warps
 // run the tensor-memory epilogues. The issuers take no part in CTA-wide
 // barriers (they would hold them up while an issue blocks): the epilogue warps
-// hand over through two mbarriers that all 256 epilogue threads arrive on,
-// "Vnew written" and "next state block written".
+// hand over through two mbarriers, "Vnew written" and "next state block
+// written", which each epilogue warp arrives on once its lanes have written
+// and fenced.
 constexpr int P2_EPI_WARPS = 8;
 constexpr int P2_THREADS = 32 * (P2_EPI_WARPS + 2);
 constexpr int JB = 32;                 // value columns per CTA
@@ -762,8 +763,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
             mbar_init(smem_u32(&ss.bar_y[0][k]), 1);
             mbar_init(smem_u32(&ss.bar_y[1][k]), 1);
         }
-        mbar_init(smem_u32(&ss.bar_vn), 32 * P2_EPI_WARPS);
-        mbar_init(smem_u32(&ss.bar_s), 32 * P2_EPI_WARPS);
+        mbar_init(smem_u32(&ss.bar_vn), P2_EPI_WARPS);   // one arrival per epilogue warp
+        mbar_init(smem_u32(&ss.bar_s), P2_EPI_WARPS);
         ss.abort = 0;
         fence_mbar_init();
         for (int c = 0; c < 2 && c < nc; ++c) {        // both stages in flight from the start
@@ -888,9 +889,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
                 }
             }
             tc::wait_st();
-            fence_proxy_async_smem();
+            fence_proxy_async_smem();                  // each thread: its stores -> the tensor core
             tc::fence_before_sync();
-            mbar_arrive(smem_u32(&ss.bar_vn));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ss.bar_vn));
             if (c > 0) {                               // y of the previous chunk, while the state update runs
                 drain_y(c - 1);
                 // that chunk's P | K~^T stage was last read by its Y += P Vnew
@@ -916,7 +918,8 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
                 store_s_bf16(sm, i, hf, sdec);
                 fence_proxy_async_smem();
                 tc::fence_before_sync();
-                mbar_arrive(smem_u32(&ss.bar_s));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ss.bar_s));
             } else if (a.S_out) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) a.S_out[sbase_g + (size_t)(j0 + e) * DK + i] = sdec[e];
