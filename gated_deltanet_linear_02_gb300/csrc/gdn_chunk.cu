@@ -652,6 +652,7 @@ struct P2Small {
     uint64_t bar_m1[2], bar_m2[2];     // chain products, per issuer
     uint64_t bar_y[2][2];              // all of a chunk's products, per Y buffer and issuer
     uint64_t bar_vn, bar_s;            // epilogue -> issuers: Vnew written; next state block written
+    uint64_t bar_yfree;                // epilogue -> issuers: a Y buffer has been drained
     uint32_t tmem;
     int abort;
 };
@@ -765,6 +766,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
         }
         mbar_init(smem_u32(&ss.bar_vn), P2_EPI_WARPS);   // one arrival per epilogue warp
         mbar_init(smem_u32(&ss.bar_s), P2_EPI_WARPS);
+        mbar_init(smem_u32(&ss.bar_yfree), P2_EPI_WARPS);
         ss.abort = 0;
         fence_mbar_init();
         for (int c = 0; c < 2 && c < nc; ++c) {        // both stages in flight from the start
@@ -843,6 +845,10 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
                 const uint64_t bs = tc::smem_desc(sb + S2_SS + 1024u * ik, 128u, (uint32_t)DK * 16u);
                 tc::mma_steps<false>(tm + T2_VN + 32 * ik, tc::kmajor_desc<2>(wq, 64 * ik, DK), bs, 4, id1, false);
                 tc::mma_commit(smem_u32(&ss.bar_m1[ik]));
+                // this Y buffer last held chunk c - 2, drained after chunk c - 1's state block
+                if (c >= 2 && !mbar_wait_bounded(smem_u32(&ss.bar_yfree), (uint32_t)((c - 2) & 1))) ss.abort = 1;
+                if (aborted) break;
+                tc::fence_after_sync();
                 tc::mma_steps<false>(tm + ycol, tc::kmajor_desc<2>(wq + 16384, 64 * ik, DK), bs, 4, id1, false);
                 // (2) K half t in [32k, 32k+32) of the state update, into S (k = 0)
                 //     or dS (k = 1), committed alone, then the same half of Y += P Vnew
@@ -893,15 +899,13 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ss.bar_vn));
-            if (c > 0) {                               // y of the previous chunk, while the state update runs
-                drain_y(c - 1);
-                // that chunk's P | K~^T stage was last read by its Y += P Vnew
-                if (tid == 0 && c + 1 < nc) carry_issue<false>(blob_of(c + 1), sb, ss, c + 1);
-            }
             if (!mbar_wait_bounded(smem_u32(&ss.bar_m2[0]), par) || !mbar_wait_bounded(smem_u32(&ss.bar_m2[1]), par))
                 ss.abort = 1;
             if (aborted) break;
             tc::fence_after_sync();
+            // chunk c - 1's P | K~^T stage was last read by its Y += P Vnew, which
+            // completed before this chunk's state update (same issuers, in order)
+            if (tid == 0 && c > 0 && c + 1 < nc) carry_issue<false>(blob_of(c + 1), sb, ss, c + 1);
             // W | Q~ of this stage were last read by Y = Q~ S, issued before each state update
             if (tid == 0 && c + 2 < nc) carry_issue<true>(blob_of(c + 2), sb, ss, c + 2);
             // state block S + dS: bf16 copy for the next chunk (its decay waits
@@ -923,6 +927,12 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
             } else if (a.S_out) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) a.S_out[sbase_g + (size_t)(j0 + e) * DK + i] = sdec[e];
+            }
+            if (c > 0) {                               // y of the previous chunk, off the chain
+                drain_y(c - 1);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ss.bar_yfree));
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) u_cur[e] = u_nxt[e];
