@@ -312,12 +312,16 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
             *reinterpret_cast<float4 *>(reinterpret_cast<unsigned char *>(tile) + km<4>(t, 4 * (4 * m + kgl), DK)) = tc::tf32_rn(x);
         }
     }
-    if (lane == 0 && warp < 2) {                      // warp 0: head 0, warp 1: head 1
-        float run = 0.0f;
-        for (int p = 0; p < CH; ++p) {
-            run += ss.G[warp][p];
-            ss.G[warp][p] = run;
+    if (warp < 2) {                                   // warp h: inclusive scan of head h's log-decays
+        const float g0 = ss.G[warp][2 * lane], g1 = ss.G[warp][2 * lane + 1];
+        float run = g0 + g1;                           // lane l holds tokens 2l, 2l+1
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float up = __shfl_up_sync(0xffffffffu, run, o);
+            if (lane >= o) run += up;
         }
+        ss.G[warp][2 * lane] = run - g1;
+        ss.G[warp][2 * lane + 1] = run;
     }
     __syncthreads();
     if (tid < 2 * CH) {
