@@ -405,12 +405,103 @@ def run_gpu(args, rank, world, dev):
               achieved=ATTN_BYTES_PER_CALL / at_call_s / 1e9)
     assert ops.device_error() == ops.GDN_OK
     del att, att_out, att_ws
+    torch.cuda.empty_cache()
+    cfgs = other_configs(args, torch, I, ops, dev, stream, flush, barrier_sync, max_over_ranks, sampler)
     clocks = sampler.stop()
 
-    return dict(at=at, ip=ip, op=op, mt=mt, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
+    return dict(cfgs=cfgs, at=at, ip=ip, op=op, mt=mt, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
                 bytes_per_launch=bytes_per_launch, launches=launches, e2e_tok_s=e2e_tok_s, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, pf_ms=pf_ms, pf_tok_s=pf_tok_s, pf_tflops=pf_tflops, hbm_peak=hbm_peak,
                 tc_peak=tc_peak, peak_src=peak_src, clocks=clocks)
+
+
+def other_configs(args, torch, I, ops, dev, stream, flush, barrier_sync, max_over_ranks, sampler):
+    """The other configurations of the metric, timed beside the headline:
+    0) one layer, T=64, fp32, zero states: the prefill (exact scan) and 64
+       decode steps; 1) one layer, B=64, 128 sequential decode steps, bf16;
+    4) the varlen prefill of 8 sequences (seeded log-uniform lengths in
+    [256, 32768]), bf16, random initial states. L2 is flushed before every
+    timed call."""
+    reps = max(3, min(args.steps, 10))
+
+    def time_calls(fn):
+        for _ in range(2):
+            fn()
+        barrier_sync()
+        times = []
+        t_wall0 = time.time()
+        for _ in range(reps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            times.append((a, b))
+        barrier_sync()
+        sampler.mark(t_wall0, time.time())
+        return max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))   # ms per call
+
+    out = {}
+    # ---- config 0
+    seed = I.seed_of(0)
+    lp = I.layer_params(seed).to(dev)
+    cp = ops.make_params(lp)
+    st = I.streams(seed, 64, torch.float32, device=dev)
+    cu = I.cu_seqlens([64]).to(dev)
+    o = torch.empty(64, I.D_INNER, device=dev)
+    ws = torch.empty(max(ops.prefill_workspace_size(1, 64, torch.float32, 0), 256), dtype=torch.uint8, device=dev)
+    pf_ms = time_calls(lambda: ops.prefill(None, st.qkv, st.z, st.alpha, st.beta, cu, o, workspace=ws, cparams=cp))
+    conv, S = I.initial_states(seed, 1, torch.float32, device=dev, zero=True)
+    sd = I.streams(seed, 1, torch.float32, device=dev, lead=(64,))
+    od = torch.empty(1, I.D_INNER, device=dev)
+
+    def dec0():
+        for k in range(64):
+            ops.decode_step(None, sd.qkv[k], sd.z[k], sd.alpha[k], sd.beta[k], conv, S, od, cparams=cp)
+    dec_ms = time_calls(dec0)
+    out["T64_fp32"] = {"prefill_us_per_call": pf_ms * 1e3, "decode_64_steps_us": dec_ms * 1e3,
+                       "decode_us_per_step": dec_ms * 1e3 / 64, "bound": "latency"}
+    # ---- config 1
+    seed = I.seed_of(1)
+    lp = I.layer_params(seed).to(dev)
+    cp = ops.make_params(lp)
+    conv, S = I.initial_states(seed, 64, torch.bfloat16, device=dev)
+    sd = I.streams(seed, 64, torch.bfloat16, device=dev, lead=(128,))
+    od = torch.empty(64, I.D_INNER, dtype=torch.bfloat16, device=dev)
+
+    def dec1():
+        for k in range(128):
+            ops.decode_step(None, sd.qkv[k], sd.z[k], sd.alpha[k], sd.beta[k], conv, S, od, cparams=cp)
+    ms = time_calls(dec1)
+    step_s = ms / 1e3 / 128
+    gbs = (64 * DECODE_BYTES_PER_TOKEN_LAYER + DECODE_PARAM_BYTES_PER_LAUNCH) / step_s / 1e9
+    out["decode_B64_128_steps_bf16"] = {"value": 64 * 128 / (ms / 1e3), "unit": "tok/s (one layer)",
+                                        "us_per_step": step_s * 1e6, "achieved_GBs": gbs,
+                                        "note": "state 128 MiB, about the size of L2: steps after the "
+                                                "first find part of it there"}
+    del conv, S, sd, od
+    # ---- config 4
+    seed = I.seed_of(4)
+    lens = I.varlen_lengths(seed)
+    T4 = sum(lens)
+    lp = I.layer_params(seed).to(dev)
+    cp = ops.make_params(lp)
+    st = I.streams(seed, T4, torch.bfloat16, device=dev)
+    conv, S = I.initial_states(seed, len(lens), torch.bfloat16, device=dev)
+    cu = I.cu_seqlens(lens).to(dev)
+    o = torch.empty(T4, I.D_INNER, dtype=torch.bfloat16, device=dev)
+    cout, sout = torch.empty_like(conv), torch.empty_like(S)
+    ws = torch.empty(ops.prefill_workspace_size(len(lens), T4, torch.bfloat16, 0), dtype=torch.uint8, device=dev)
+    ms = time_calls(lambda: ops.prefill(None, st.qkv, st.z, st.alpha, st.beta, cu, o, conv, cout, S, sout,
+                                        workspace=ws, cparams=cp))
+    tflops = PREFILL_FLOP_PER_TOKEN * T4 / (ms / 1e3) / 1e12
+    io = T4 * DECODE_IO_BYTES_PER_TOKEN + len(lens) * DECODE_STATE_CONV_BYTES   # streams, states in and out
+    out["varlen_prefill_8seq_bf16"] = {"lengths": lens, "tokens": T4, "value": T4 / (ms / 1e3), "unit": "tok/s",
+                                       "ms_per_call": ms, "tflops": tflops,
+                                       "io_GBs": io / (ms / 1e3) / 1e9}
+    del st, conv, S, o, cout, sout, ws
+    assert ops.device_error() == ops.GDN_OK
+    return out
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -463,10 +554,13 @@ def cpu_baseline(n_seq=None):
     threads = host_threads()
     n_seq = n_seq or BATCH                # one whole decode step: ~1 s wall on 16 cores
     secs, toks = oracle_decode_sample(n_seq, threads)
+    secs1, toks1 = oracle_decode_sample(8, 1)     # one core, on a smaller sample
     return {"value": toks / secs, "unit": "tok/s", "cores": threads, "kind": "oracle",
             "sample": f"one decode token through all 30 layers for {n_seq} of the {BATCH} sequences "
                       f"(fp64 oracle, {threads} threads over sequences), {secs:.1f} s wall, "
-                      f"{secs * threads:.0f} core-seconds"}
+                      f"{secs * threads:.0f} core-seconds",
+            "value_one_core": toks1 / secs1,
+            "sample_one_core": f"the same for 8 sequences on 1 thread, {secs1:.1f} s"}
 
 
 # ------------------------------------------------------------------- main
@@ -665,6 +759,7 @@ def main():
                                      "algorithmic_bytes_per_call": ATTN_BYTES_PER_CALL,
                                      "traffic": ATTN_TRAFFIC_PER_CALL, "kernel": "attn_block_kernel<bf16>",
                                      "timed": "whole call: attn_block_kernel + attn_combine_kernel"}},
+        "other_configs": r["cfgs"],
         "decode_multi": {"workload": f"decode_multi_30L_B{BATCH}_T{MULTI_T}_bf16", "value": r["mt"]["tok_s"],
                          "unit": "tok/s", "tokens_per_sequence_per_call": MULTI_T,
                          "launch_us": r["mt"]["launch_s"] * 1e6,

@@ -146,7 +146,7 @@ def attn_inputs(seed: int, B: int, Lmax: int, ctx_len=None, device="cpu") -> Att
     they are drawn N(0, 1) per element; values and the gate logits z too. Rows
     at or past each sequence's ctx_len hold NaN, which the attention must
     never let through. ctx_len defaults to Lmax for every sequence."""
-    g = _gen(seed + 900_000, device)
+    g = _gen(seed + 950_000, device)
     q = torch.randn(B, ATTN_HQ, ATTN_D, generator=g, device=device).to(torch.bfloat16)
     k = torch.randn(B, ATTN_HKV, Lmax, ATTN_D, generator=g, device=device)
     v = torch.randn(B, ATTN_HKV, Lmax, ATTN_D, generator=g, device=device)
