@@ -122,3 +122,17 @@ def test_attn_deterministic(ops):
         outs.append(out)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("Lmax,lens", [(1, [1, 0]), (129, [129, 128]), (128, [128, 127])])
+def test_attn_tile_edges(ops, Lmax, lens):
+    # a one-row cache, a context one position past a tile, and an exact tile
+    inp = I.attn_inputs(I.seed_of(26), len(lens), Lmax, lens)
+    check(ops, inp, label=f"Lmax={Lmax}")
+
+
+def test_attn_single_sequence_long_context(ops):
+    # one sequence at a 128K-token context: 1-tile blocks, 1024 of them per KV
+    # head, merged by the combine kernel 8 blocks at a time
+    inp = I.attn_inputs(I.seed_of(27), 1, 131072, [131072 - 77], device=DEV)
+    check(ops, inp, label="B=1 L=128K")
