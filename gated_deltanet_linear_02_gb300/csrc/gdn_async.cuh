@@ -105,14 +105,6 @@ __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol
 
 // ---- thread-block clusters and distributed shared memory
 
-// This CTA's rank within its cluster.
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 // The shared::cluster address of the shared-memory location `addr` in the CTA
 // of rank `rank` of this cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
