@@ -37,6 +37,8 @@
 #include "gdn_tc.cuh"
 #include "gdn_tma.cuh"
 
+#include <algorithm>
+
 namespace gdn {
 
 __device__ unsigned int g_chunk_error;   // GDN_ERR_TIMEOUT if a bounded wait gave up
@@ -179,53 +181,79 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     unsigned char *sm = smem_aligned128(smem_raw);
     P1Small &ss = *reinterpret_cast<P1Small *>(sm + S1_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.x, kh = blockIdx.y;
+    const uint32_t sbase = smem_u32(sm);
+    float *Qs = reinterpret_cast<float *>(sm + S1_QS);
+    float *Ks = reinterpret_cast<float *>(sm + S1_KS);
 
     grid_dep_wait();                                   // chunk_info comes from the schedule kernel
     grid_dep_launch();
-    const int4 ci = __ldg(a.chunk_info + g);
-    if (ci.x < 0) return;                              // no chunk here (uniform for the whole CTA)
-    const int n = ci.x;                                // sequence
-    const int lc = ci.y;                               // chunk index inside the sequence
-    const int seq0 = ci.z;                             // the sequence's first row
-    const int t0 = seq0 + CH * lc;
-    const int nv = ci.w;                               // valid tokens in this chunk (1..64)
-
-    float *Qs = reinterpret_cast<float *>(sm + S1_QS);
-    float *Ks = reinterpret_cast<float *>(sm + S1_KS);
-    const uint32_t sbase = smem_u32(sm);
-
+    // Persistent: CTA b takes items b, b + grid, ... (item = chunk * 16 + K-head),
+    // skipping unused chunk slots. The next item's raw rows are staged while the
+    // current item writes its outputs.
+    const int n_items = a.max_chunks * HK;
+    auto next_valid = [&](int it) {
+        while (it < n_items && __ldg(a.chunk_info + it / HK).x < 0) it += (int)gridDim.x;
+        return it;
+    };
+    // ---- B1. stage an item's raw q|k|v inputs of chunk positions -3..63 (the
+    //      512 channels of its K-head pair) and their conv taps: one thread
+    //      issues four 2-D tensor copies and four 2 KiB bulk copies on one
+    //      mbarrier. Rows past the chunk's last token hold whatever follows (the
+    //      next sequence, or zeros past the end); only outputs of valid tokens
+    //      are kept, and those never read such rows.
+    auto stage = [&](int it) {                         // caller: thread 0
+        const int4 c = __ldg(a.chunk_info + it / HK);
+        const int k2 = it % HK;
+        const int ch[4] = {Q_OFF + k2 * DK, K_OFF + k2 * DK, V_OFF + k2 * DV, V_OFF + (k2 + HK) * DV};
+        const uint32_t bl = smem_u32(&ss.bar_ld);
+        mbar_arrive_expect_tx(bl, 4 * RAW_BOX_BYTES + 4 * 2048);
+#pragma unroll
+        for (int sg = 0; sg < 4; ++sg) {
+            tma_load_2d(sbase + S1_RAW + sg * RAW_SEG, &qkv_map, ch[sg], c.z + CH * c.y - (KC - 1), bl);
+            bulk_g2s(sbase + S1_CW + sg * 2048, a.conv_w + (size_t)ch[sg] * KC, 2048, bl);
+        }
+    };
     if (warp == 0) {
         tc::tmem_alloc(smem_u32(&ss.tmem), T1_COLS);
         tc::tmem_relinquish();
     }
-    // ---- B1. stage the raw q|k|v inputs of chunk positions -3..63 (the 512
-    //      channels of this K-head pair) and their conv taps: one thread issues
-    //      four 2-D tensor copies and four 2 KiB bulk copies on one mbarrier.
-    //      Rows past the chunk's last token hold whatever follows (the next
-    //      sequence, or zeros past the end); only outputs of valid tokens are
-    //      kept, and those never read such rows.
-    const int chan0[4] = {Q_OFF + kh * DK, K_OFF + kh * DK, V_OFF + kh * DV, V_OFF + (kh + HK) * DV};
+    int item = next_valid((int)blockIdx.x);
+    int done = 0;                                      // items finished by this CTA
+    bool staged = false;                               // thread 0: a staging copy is in flight
+    float al_next = 0.0f, be_next = 0.0f;              // threads < 128: the next item's gate logits
     if (tid == 0) {
         mbar_init(smem_u32(&ss.bar), 1);
         mbar_init(smem_u32(&ss.bar_ld), 1);
         ss.abort = 0;
         fence_mbar_init();
-        const uint32_t bl = smem_u32(&ss.bar_ld);
-        mbar_arrive_expect_tx(bl, 4 * RAW_BOX_BYTES + 4 * 2048);
-#pragma unroll
-        for (int sg = 0; sg < 4; ++sg) {
-            tma_load_2d(sbase + S1_RAW + sg * RAW_SEG, &qkv_map, chan0[sg], t0 - (KC - 1), bl);
-            bulk_g2s(sbase + S1_CW + sg * 2048, a.conv_w + (size_t)chan0[sg] * KC, 2048, bl);
+        if (item < n_items) {
+            stage(item);
+            staged = true;
         }
     }
-    // gates of both V-heads; padded tokens get g = 0, beta = 0
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = ss.tmem;
+
+    for (; item < n_items; ++done) {
+    const int g = item / HK, kh = item % HK;
+    const int4 ci = __ldg(a.chunk_info + g);
+    const int n = ci.x;                                // sequence
+    const int lc = ci.y;                               // chunk index inside the sequence
+    const int seq0 = ci.z;                             // the sequence's first row
+    const int t0 = seq0 + CH * lc;
+    const int nv = ci.w;                               // valid tokens in this chunk (1..64)
+    const int nit = next_valid(item + (int)gridDim.x);
+    const int chan0[4] = {Q_OFF + kh * DK, K_OFF + kh * DK, V_OFF + kh * DV, V_OFF + (kh + HK) * DV};
+    // gates of both V-heads; padded tokens get g = 0, beta = 0. After the first
+    // item the logits were loaded ahead, during the previous item's stores.
     if (tid < 2 * CH) {
         const int h = tid >> 6, p = tid & 63, vh = kh + HK * h;
         float gg = 0.0f, bb = 0.0f;
         if (p < nv) {
-            const float al = to_f(a.alpha[(size_t)(t0 + p) * HV + vh]);
-            const float be = to_f(a.beta[(size_t)(t0 + p) * HV + vh]);
+            const float al = done == 0 ? to_f(a.alpha[(size_t)(t0 + p) * HV + vh]) : al_next;
+            const float be = done == 0 ? to_f(a.beta[(size_t)(t0 + p) * HV + vh]) : be_next;
             gg = -expf(a.A_log[vh]) * softplus_f(al + a.dt_bias[vh]);
             bb = 1.0f / (1.0f + expf(-be));
         }
@@ -233,7 +261,8 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
         ss.B[h][p] = bb;
     }
     __syncthreads();
-    if (!mbar_wait_bounded(smem_u32(&ss.bar_ld), 0)) ss.abort = 1;
+    if (!mbar_wait_bounded(smem_u32(&ss.bar_ld), (uint32_t)(done & 1))) ss.abort = 1;
+    if (tid == 0) staged = false;
     if (lc == 0 && tid < 3 * 4 * 16) {
         // the first chunk of a sequence: positions -3..-1 are its conv_state
         // (zeros without one), not the rows before the sequence
@@ -333,7 +362,6 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     tc::fence_before_sync();
     __syncthreads();
 
-    const uint32_t tm = ss.tmem;
     // ---- D. K K^T and Q K^T (tf32, M=64, N=64, K=128)
     if (tid == 0) {
         tc::fence_after_sync();
@@ -582,6 +610,21 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     }
     if (!ss.abort && !mbar_wait_bounded(smem_u32(&ss.bar), 1)) ss.abort = 1;
     tc::fence_after_sync();
+    // U and W have been read out of shared memory: the staging area (which
+    // overlaps L, T and (Gamma K)^T) takes the next item's rows during H
+    if (tid == 0 && nit < n_items && !ss.abort) {
+        stage(nit);
+        staged = true;
+    }
+    if (tid < 2 * CH && nit < n_items) {              // and the next item's gate logits
+        const int4 c = __ldg(a.chunk_info + nit / HK);
+        const int h = tid >> 6, p = tid & 63, vh = nit % HK + HK * h;
+        if (p < c.w) {
+            const size_t row = (size_t)(c.z + CH * c.y + p) * HV + vh;
+            al_next = to_f(a.alpha[row]);
+            be_next = to_f(a.beta[row]);
+        }
+    }
 
     // ---- H. U -> blob as [t][j] fp32; W -> blob as bf16 K-major [t][i]. Warp w
     //      reads token columns [16 (w / 4), +16) of its lane quarter w % 4.
@@ -604,6 +647,13 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
             }
         }
     }
+    tc::fence_before_sync();
+    __syncthreads();                                   // the next item rewrites gates, tiles and TMEM
+    if (ss.abort) break;
+    item = nit;
+    }
+    if (tid == 0 && staged)                            // after an abort: the copy in flight lands first
+        mbar_wait_bounded(smem_u32(&ss.bar_ld), (uint32_t)(done & 1));
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, T1_COLS);
@@ -955,6 +1005,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1) chunk_carry_kernel(const ChunkA
 
 cudaError_t launch_conv_state_out_bf16(const int32_t *cu, int N, int T_total, const void *qkv, const void *cs_in,
                                        void *cs_out, cudaStream_t s, bool pdl);
+int sm_count();
 cudaError_t launch_gated_norm_bf16(const float *norm_w, float norm_eps, const void *z, const float *y, void *out,
                                    int T_total, gdn_dtype out_dt, cudaStream_t s, bool pdl);
 
@@ -999,13 +1050,16 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
     CUtensorMap qkv_map;
     if (T_total > 0 && !make_bf16_plain_map(&qkv_map, qkv, T_total, CC, RAW_COLS, RAW_ROWS))
         return cudaErrorInvalidValue;
+    const int n_sm = sm_count();                       // the prep grid is persistent: one CTA per SM
+    if (n_sm <= 0) return cudaErrorInvalidDevice;
     // The kernels after the schedule kernel are launched with programmatic
     // stream serialization: each may start while the one ahead finishes, and
     // waits (grid_dep_wait) before it reads that kernel's results.
     chunk_schedule_kernel<<<1, 1024, 0, s>>>(cu, N, T_total, a.max_chunks, a.chunk_off, a.chunk_info);
     e = cudaGetLastError();
     if (e == cudaSuccess && a.max_chunks > 0 && T_total > 0)
-        e = launch_pdl(chunk_prep_kernel, dim3(a.max_chunks, HK), dim3(P1_THREADS), P1_SMEM, s, qkv_map, a);
+        e = launch_pdl(chunk_prep_kernel, dim3((unsigned)std::min(a.max_chunks * HK, n_sm)), dim3(P1_THREADS),
+                       P1_SMEM, s, qkv_map, a);
     if (e == cudaSuccess) e = launch_pdl(chunk_carry_kernel, dim3(N, HV, NJB), dim3(P2_THREADS), P2_SMEM, s, a);
     if (e == cudaSuccess)
         e = launch_gated_norm_bf16(p->norm_w, p->norm_eps, z, a.ybuf, out, T_total, out_dt, s, true);
