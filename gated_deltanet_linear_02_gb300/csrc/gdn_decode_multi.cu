@@ -27,7 +27,9 @@ namespace gdn {
 
 __device__ unsigned int g_multi_error;   // GDN_ERR_TIMEOUT if a bounded wait gave up
 
-constexpr int MT = GDN_DECODE_MAX_T;                        // tokens per sequence, at most
+constexpr int MT_MAX = GDN_DECODE_MAX_T;                    // tokens per sequence, at most
+// The kernel is instantiated for a token capacity MT of 4 or 8: a call with
+// T <= 4 takes the smaller one, whose per-token arrays use fewer registers.
 constexpr int MD_WARPS = 16;                                // compute warps
 constexpr int MD_COMPUTE = 32 * MD_WARPS;
 constexpr int MD_THREADS = MD_COMPUTE + 32;                 // + the producer warp
@@ -48,6 +50,7 @@ struct MultiArgs {
     int T;
 };
 
+template <int MT>
 struct MultiSmem {
     alignas(128) float slot[MD_SLOTS][MD_SLOT_ROWS * DK];   // TMA destinations
     alignas(16) float q[MT][DK];                     // L2-normalised q of each token (float4 reads)
@@ -62,12 +65,14 @@ struct MultiSmem {
     int pending[MD_SLOTS];
     int abort;
 };
-constexpr size_t MD_SMEM = sizeof(MultiSmem) + 128;
-static_assert(MD_SMEM <= 232448, "decode_multi shared memory");
+template <int MT>
+constexpr size_t md_smem() { return sizeof(MultiSmem<MT>) + 128; }
+static_assert(md_smem<MT_MAX>() <= 232448, "decode_multi shared memory");
 
 // Loads unit u (u = (2 m + h) * MD_UNITS + part) of this CTA into slot u % MD_SLOTS.
 // Caller: the producer thread; the unit's item exists.
-__device__ __forceinline__ void multi_issue_load(MultiSmem &sm, const MultiArgs &a, int u)
+template <int MT>
+__device__ __forceinline__ void multi_issue_load(MultiSmem<MT> &sm, const MultiArgs &a, int u)
 {
     const int item = blockIdx.x + (u / (2 * MD_UNITS)) * gridDim.x;
     const int h = (u / MD_UNITS) & 1, part = u % MD_UNITS;
@@ -96,7 +101,7 @@ __device__ __forceinline__ int multi_channel(int kh, int tid)
 // its channel's conv_state rows, its T inputs and taps; for tid < 256 the z of
 // output column (V-head kh + 16 (tid >> 7), j = tid & 127) of every token; for
 // tid < 2T the gate inputs of token tid >> 1 and V-head kh + 16 (tid & 1).
-template <typename TA> struct MultiIn {
+template <typename TA, int MT> struct MultiIn {
     TA s[KC - 1];
     TA x[MT];
     TA zc[MT];
@@ -105,10 +110,10 @@ template <typename TA> struct MultiIn {
     float A_log, dt_bias;
 };
 
-template <typename TA>
-__device__ __forceinline__ MultiIn<TA> multi_load(const MultiArgs &a, int item, int tid)
+template <typename TA, int MT>
+__device__ __forceinline__ MultiIn<TA, MT> multi_load(const MultiArgs &a, int item, int tid)
 {
-    MultiIn<TA> p;
+    MultiIn<TA, MT> p;
     const size_t b = item / HK;
     const int kh = item % HK, T = a.T;
     const int c = multi_channel(kh, tid);
@@ -137,11 +142,11 @@ __device__ __forceinline__ MultiIn<TA> multi_load(const MultiArgs &a, int item, 
 // Barrier among the 16 compute warps only (the producer warp never joins it).
 __device__ __forceinline__ void multi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(MD_COMPUTE) : "memory"); }
 
-template <typename TA, typename TO>
+template <typename TA, typename TO, int MT>
 __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const MultiArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
-    MultiSmem &sm = *reinterpret_cast<MultiSmem *>(smem_aligned128(smem_raw));
+    MultiSmem<MT> &sm = *reinterpret_cast<MultiSmem<MT> *>(smem_aligned128(smem_raw));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T;
     const volatile int &aborted = sm.abort;
@@ -184,8 +189,8 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
 
     // ---- compute warps
     const float scale = rsqrtf((float)DK);
-    MultiIn<TA> pin;
-    if ((int)blockIdx.x < a.n_items) pin = multi_load<TA>(a, blockIdx.x, tid);
+    MultiIn<TA, MT> pin;
+    if ((int)blockIdx.x < a.n_items) pin = multi_load<TA, MT>(a, blockIdx.x, tid);
     for (int m = 0;; ++m) {
         const int item = blockIdx.x + m * gridDim.x;
         if (item >= a.n_items) break;
@@ -248,7 +253,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
         TA zcur[MT];
 #pragma unroll
         for (int t = 0; t < MT; ++t) zcur[t] = pin.zc[t];
-        if (item + (int)gridDim.x < a.n_items) pin = multi_load<TA>(a, item + gridDim.x, tid);
+        if (item + (int)gridDim.x < a.n_items) pin = multi_load<TA, MT>(a, item + gridDim.x, tid);
 
         // ---- the two states: each row takes tokens 0..T-1 in order
         const int rr = lane >> 3, g = lane & 7;         // row of the warp's four; float4 group within it
@@ -336,16 +341,22 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
 
 int sm_count();
 
-template <typename TA, typename TO>
-static cudaError_t launch_multi_t(const MultiArgs &a, cudaStream_t s)
+template <typename TA, typename TO, int MT>
+static cudaError_t launch_multi_mt(const MultiArgs &a, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<TA, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)MD_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel<TA, TO, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)md_smem<MT>());
     if (e != cudaSuccess) return e;
     const int n_sm = sm_count();
     if (n_sm <= 0) return cudaErrorInvalidDevice;
     const int grid = a.n_items < n_sm ? a.n_items : n_sm;
-    return launch_pdl(decode_multi_kernel<TA, TO>, dim3(grid), dim3(MD_THREADS), MD_SMEM, s, a);
+    return launch_pdl(decode_multi_kernel<TA, TO, MT>, dim3(grid), dim3(MD_THREADS), md_smem<MT>(), s, a);
+}
+
+template <typename TA, typename TO>
+static cudaError_t launch_multi_t(const MultiArgs &a, cudaStream_t s)
+{
+    return a.T <= 4 ? launch_multi_mt<TA, TO, 4>(a, s) : launch_multi_mt<TA, TO, MT_MAX>(a, s);
 }
 
 cudaError_t launch_decode_multi(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
