@@ -10,16 +10,19 @@
 // updates in registers and is written once, so the state bytes per token fall
 // by a factor of T.
 //
-// Structure. It is the decode kernel's: one persistent CTA per SM with 16
-// compute warps and a producer warp, which streams the states through six
-// 32 KiB shared-memory slots with TMA bulk copies (full/empty mbarriers). An
-// item is (sequence b, K-head kh) with both V-heads kh and kh + 16. In an
+// Structure. One persistent CTA per SM with 16 warps streams the states
+// through six 32 KiB shared-memory slots with TMA bulk copies, a full mbarrier
+// per slot. There is no producer warp: the last warp to release a slot (a
+// shared counter per slot) issues the copy of the unit that goes there next,
+// which keeps the CTA at 512 threads and so 128 registers a thread. An item is
+// (sequence b, K-head kh) with both V-heads kh and kh + 16. In an
 // item's prologue each thread convolves one channel over the window
 // [conv_state (3 rows), x_0 .. x_{T-1}] and shifts T rows into conv_state. The
 // q and k rows are L2-normalised per token, and the gates come per token and
 // V-head. In the sweep, lanes 8r..8r+7 of a warp hold state row r (16 keys
-// each), and the warp's four rows apply tokens 0..T-1 in order: decay, pred,
-// delta, write, read. The output stage applies the gated RMSNorm per token.
+// each) of both halves of a state (rows r' and 64 + r' of the two slots of
+// one head), so that each k and q load of a token serves two rows. The warp's
+// rows apply tokens 0..T-1 in order: decay, pred, delta, write, read. The output stage applies the gated RMSNorm per token.
 #include "gdn_async.cuh"
 #include "gdn_common.cuh"
 
@@ -30,9 +33,8 @@ __device__ unsigned int g_multi_error;   // GDN_ERR_TIMEOUT if a bounded wait ga
 constexpr int MT_MAX = GDN_DECODE_MAX_T;                    // tokens per sequence, at most
 // The kernel is instantiated for a token capacity MT of 4 or 8: a call with
 // T <= 4 takes the smaller one, whose per-token arrays use fewer registers.
-constexpr int MD_WARPS = 16;                                // compute warps
-constexpr int MD_COMPUTE = 32 * MD_WARPS;
-constexpr int MD_THREADS = MD_COMPUTE + 32;                 // + the producer warp
+constexpr int MD_WARPS = 16;
+constexpr int MD_THREADS = 32 * MD_WARPS;
 constexpr int MD_SLOT_ROWS = 64;                            // rows j of S^T per staging slot
 constexpr int MD_UNITS = DV / MD_SLOT_ROWS;                 // slots per state (2)
 constexpr int MD_SLOTS = 6;
@@ -58,7 +60,7 @@ struct MultiSmem {
     alignas(16) float v[MT][2][DV];
     alignas(16) float y[MT][2][DV];
     alignas(8) uint64_t full[MD_SLOTS];
-    uint64_t empty[MD_SLOTS];
+    int released[MD_SLOTS];                          // warps done with the slot's current unit
     float red[MT][8];                                // per token: q sums (warps 0..3), k sums (4..7)
     float ored[MT][8];                               // per token: y^2 sums of head 0 (warps 0..3), head 1 (4..7)
     float gate[MT][2][2];                            // per token and V-head: decay exp(g), beta
@@ -70,7 +72,7 @@ constexpr size_t md_smem() { return sizeof(MultiSmem<MT>) + 128; }
 static_assert(md_smem<MT_MAX>() <= 232448, "decode_multi shared memory");
 
 // Loads unit u (u = (2 m + h) * MD_UNITS + part) of this CTA into slot u % MD_SLOTS.
-// Caller: the producer thread; the unit's item exists.
+// Caller: one thread; the unit's item exists and the slot is free.
 template <int MT>
 __device__ __forceinline__ void multi_issue_load(MultiSmem<MT> &sm, const MultiArgs &a, int u)
 {
@@ -139,8 +141,32 @@ __device__ __forceinline__ MultiIn<TA, MT> multi_load(const MultiArgs &a, int it
     return p;
 }
 
-// Barrier among the 16 compute warps only (the producer warp never joins it).
-__device__ __forceinline__ void multi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(MD_COMPUTE) : "memory"); }
+__device__ __forceinline__ void multi_sync() { __syncthreads(); }
+
+template <int MT>
+__device__ __forceinline__ bool multi_unit_exists(const MultiArgs &a, int u)
+{
+    return blockIdx.x + (u / (2 * MD_UNITS)) * (int)gridDim.x < a.n_items;
+}
+
+// Lane 0 of a warp that has finished reading unit u in slot u % MD_SLOTS. The
+// sixteenth warp to get here frees the slot and loads unit u + MD_SLOTS into it.
+// The fences order every warp's reads of the slot before the counter updates,
+// and the last update before the copy, which the proxy fence hands to TMA.
+template <int MT>
+__device__ __forceinline__ void multi_release(MultiSmem<MT> &sm, const MultiArgs &a, int u)
+{
+    const int slot = u % MD_SLOTS;
+    __threadfence_block();
+    if (atomicAdd(&sm.released[slot], 1) != MD_WARPS - 1) return;
+    __threadfence_block();
+    sm.released[slot] = 0;
+    sm.pending[slot] = -1;
+    const int nu = u + MD_SLOTS;
+    if (sm.abort || !multi_unit_exists<MT>(a, nu)) return;
+    fence_proxy_async_smem();
+    multi_issue_load(sm, a, nu);
+}
 
 template <typename TA, typename TO, int MT>
 __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const MultiArgs a)
@@ -154,7 +180,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
     if (tid == 0) {
         for (int i = 0; i < MD_SLOTS; ++i) {
             mbar_init(smem_u32(&sm.full[i]), 1);
-            mbar_init(smem_u32(&sm.empty[i]), MD_WARPS);
+            sm.released[i] = 0;
             sm.pending[i] = -1;
         }
         sm.abort = 0;
@@ -164,30 +190,9 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
     grid_dep_wait();                                   // inputs and states may come from the kernel ahead
     grid_dep_launch();
 
-    if (warp == MD_WARPS) {
-        // ---- producer: unit u goes into slot u % MD_SLOTS once the compute warps
-        //      have released that slot's previous unit, u - MD_SLOTS
-        if (lane == 0) {
-            for (int u = 0;; ++u) {
-                if (blockIdx.x + (u / (2 * MD_UNITS)) * (int)gridDim.x >= a.n_items) break;
-                const int slot = u % MD_SLOTS;
-                if (u >= MD_SLOTS) {
-                    if (!mbar_wait_bounded(smem_u32(&sm.empty[slot]), (uint32_t)((u / MD_SLOTS - 1) & 1))) sm.abort = 1;
-                    sm.pending[slot] = -1;
-                }
-                if (aborted) break;
-                fence_proxy_async_smem();
-                multi_issue_load(sm, a, u);
-            }
-            if (aborted)   // let the copies still in flight land before shared memory is released
-                for (int i = 0; i < MD_SLOTS; ++i)
-                    if (sm.pending[i] >= 0)
-                        mbar_wait_bounded(smem_u32(&sm.full[i]), (uint32_t)((sm.pending[i] / MD_SLOTS) & 1));
-        }
-        return;
-    }
+    if (tid == 0)                                      // the first MD_SLOTS units
+        for (int u = 0; u < MD_SLOTS && multi_unit_exists<MT>(a, u); ++u) multi_issue_load(sm, a, u);
 
-    // ---- compute warps
     const float scale = rsqrtf((float)DK);
     MultiIn<TA, MT> pin;
     if ((int)blockIdx.x < a.n_items) pin = multi_load<TA, MT>(a, blockIdx.x, tid);
@@ -256,56 +261,80 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
         if (item + (int)gridDim.x < a.n_items) pin = multi_load<TA, MT>(a, item + gridDim.x, tid);
 
         // ---- the two states: each row takes tokens 0..T-1 in order
+        // Each lane group holds two rows of one head, row jl of part 0 and of
+        // part 1, so that every k and q load of a token serves both.
         const int rr = lane >> 3, g = lane & 7;         // row of the warp's four; float4 group within it
-        for (int hp = 0; hp < 2 * MD_UNITS; ++hp) {
-            const int h = hp / MD_UNITS, part = hp % MD_UNITS;
-            const int u = 2 * MD_UNITS * m + hp;
-            const int slot = u % MD_SLOTS;
+        static_assert(MD_UNITS == 2, "a head is two slots");
+        for (int h = 0; h < 2; ++h) {
+            const int u0 = 2 * MD_UNITS * m + MD_UNITS * h;   // units u0 (rows 0..63), u0 + 1 (rows 64..127)
+            const int s0 = u0 % MD_SLOTS, s1 = (u0 + 1) % MD_SLOTS;
             if (aborted) continue;                       // skip the work, keep the barriers in step
-            if (!mbar_wait_bounded(smem_u32(&sm.full[slot]), (uint32_t)((u / MD_SLOTS) & 1))) {
+            if (!mbar_wait_bounded(smem_u32(&sm.full[s0]), (uint32_t)((u0 / MD_SLOTS) & 1)) ||
+                !mbar_wait_bounded(smem_u32(&sm.full[s1]), (uint32_t)(((u0 + 1) / MD_SLOTS) & 1))) {
                 sm.abort = 1;
                 continue;
             }
             const int vh = kh + HK * h;
             float *Sg = a.ssm_state + (b * HV + vh) * (size_t)(DV * DK);
-            const int jl = warp * 4 + rr;                // row within the slot
-            const int j = part * MD_SLOT_ROWS + jl;
-            const float4 *src = reinterpret_cast<const float4 *>(sm.slot[slot]) + jl * (DK / 4) + g;
-            float4 st[4];
+            const int jl = warp * 4 + rr;                // row within each slot
+            const int j0 = jl, j1 = MD_SLOT_ROWS + jl;
+            const float4 *src0 = reinterpret_cast<const float4 *>(sm.slot[s0]) + jl * (DK / 4) + g;
+            const float4 *src1 = reinterpret_cast<const float4 *>(sm.slot[s1]) + jl * (DK / 4) + g;
+            float4 st0[4], st1[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) st[c] = src[8 * c];
+            for (int c = 0; c < 4; ++c) {
+                st0[c] = src0[8 * c];
+                st1[c] = src1[8 * c];
+            }
             for (int t = 0; t < T; ++t) {
                 const float dec = sm.gate[t][h][0], beta = sm.gate[t][h][1];
                 const float4 *k4 = reinterpret_cast<const float4 *>(sm.k[t]) + g;
-                float pa = 0.0f, pb = 0.0f;
+                float pa0 = 0.0f, pb0 = 0.0f, pa1 = 0.0f, pb1 = 0.0f;
                 float4 kk[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     kk[c] = k4[8 * c];
-                    st[c].x *= dec; st[c].y *= dec; st[c].z *= dec; st[c].w *= dec;                 // (a)
-                    pa = fmaf(st[c].x, kk[c].x, fmaf(st[c].y, kk[c].y, pa));
-                    pb = fmaf(st[c].z, kk[c].z, fmaf(st[c].w, kk[c].w, pb));
+                    st0[c].x *= dec; st0[c].y *= dec; st0[c].z *= dec; st0[c].w *= dec;             // (a)
+                    st1[c].x *= dec; st1[c].y *= dec; st1[c].z *= dec; st1[c].w *= dec;
+                    pa0 = fmaf(st0[c].x, kk[c].x, fmaf(st0[c].y, kk[c].y, pa0));
+                    pb0 = fmaf(st0[c].z, kk[c].z, fmaf(st0[c].w, kk[c].w, pb0));
+                    pa1 = fmaf(st1[c].x, kk[c].x, fmaf(st1[c].y, kk[c].y, pa1));
+                    pb1 = fmaf(st1[c].z, kk[c].z, fmaf(st1[c].w, kk[c].w, pb1));
                 }
-                const float pred = group_sum<8>(pa + pb);                                             // (b)
-                const float delta = (sm.v[t][h][j] - pred) * beta;
+                const float pred0 = group_sum<8>(pa0 + pb0), pred1 = group_sum<8>(pa1 + pb1);         // (b)
+                const float d0 = (sm.v[t][h][j0] - pred0) * beta, d1 = (sm.v[t][h][j1] - pred1) * beta;
                 const float4 *q4 = reinterpret_cast<const float4 *>(sm.q[t]) + g;
-                float ya = 0.0f, yb = 0.0f;
+                float ya0 = 0.0f, yb0 = 0.0f, ya1 = 0.0f, yb1 = 0.0f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const float4 qq = q4[8 * c];
-                    st[c].x = fmaf(kk[c].x, delta, st[c].x); st[c].y = fmaf(kk[c].y, delta, st[c].y); // (c)
-                    st[c].z = fmaf(kk[c].z, delta, st[c].z); st[c].w = fmaf(kk[c].w, delta, st[c].w);
-                    ya = fmaf(st[c].x, qq.x, fmaf(st[c].y, qq.y, ya));
-                    yb = fmaf(st[c].z, qq.z, fmaf(st[c].w, qq.w, yb));
+                    st0[c].x = fmaf(kk[c].x, d0, st0[c].x); st0[c].y = fmaf(kk[c].y, d0, st0[c].y);   // (c)
+                    st0[c].z = fmaf(kk[c].z, d0, st0[c].z); st0[c].w = fmaf(kk[c].w, d0, st0[c].w);
+                    st1[c].x = fmaf(kk[c].x, d1, st1[c].x); st1[c].y = fmaf(kk[c].y, d1, st1[c].y);
+                    st1[c].z = fmaf(kk[c].z, d1, st1[c].z); st1[c].w = fmaf(kk[c].w, d1, st1[c].w);
+                    ya0 = fmaf(st0[c].x, qq.x, fmaf(st0[c].y, qq.y, ya0));
+                    yb0 = fmaf(st0[c].z, qq.z, fmaf(st0[c].w, qq.w, yb0));
+                    ya1 = fmaf(st1[c].x, qq.x, fmaf(st1[c].y, qq.y, ya1));
+                    yb1 = fmaf(st1[c].z, qq.z, fmaf(st1[c].w, qq.w, yb1));
                 }
-                const float yq = group_sum<8>(ya + yb);                                               // (d)
-                if (g == 0) sm.y[t][h][j] = yq * scale;
+                const float y0 = group_sum<8>(ya0 + yb0), y1 = group_sum<8>(ya1 + yb1);                 // (d)
+                if (g == 0) {
+                    sm.y[t][h][j0] = y0 * scale;
+                    sm.y[t][h][j1] = y1 * scale;
+                }
             }
-            float4 *dst = reinterpret_cast<float4 *>(Sg + (size_t)j * DK) + g;
+            float4 *dst0 = reinterpret_cast<float4 *>(Sg + (size_t)j0 * DK) + g;
+            float4 *dst1 = reinterpret_cast<float4 *>(Sg + (size_t)j1 * DK) + g;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) __stcs(dst + 8 * c, st[c]);
-            __syncwarp();                                // this warp's reads of the slot are done
-            if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
+            for (int c = 0; c < 4; ++c) {
+                __stcs(dst0 + 8 * c, st0[c]);
+                __stcs(dst1 + 8 * c, st1[c]);
+            }
+            __syncwarp();                                // this warp's reads of both slots are done
+            if (lane == 0) {
+                multi_release(sm, a, u0);
+                multi_release(sm, a, u0 + 1);
+            }
         }
         multi_sync();                                    // all rows of y are in, and the abort flag agrees
         if (aborted) break;
@@ -337,6 +366,10 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
         // the next prologue writes q/k/v/red/gate, none of which the lines above read
     }
     if (aborted && tid == 0) atomicExch(&g_multi_error, (unsigned int)GDN_ERR_TIMEOUT);
+    multi_sync();                                        // no release is still running
+    if (aborted && tid == 0)   // let the copies still in flight land before shared memory is released
+        for (int i = 0; i < MD_SLOTS; ++i)
+            if (sm.pending[i] >= 0) mbar_wait_bounded(smem_u32(&sm.full[i]), (uint32_t)((sm.pending[i] / MD_SLOTS) & 1));
 }
 
 int sm_count();
