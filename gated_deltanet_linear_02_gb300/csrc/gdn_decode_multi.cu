@@ -218,15 +218,21 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
                 if (t >= T) break;
                 xh[t] = silu_f(pin.w.x * win[t] + pin.w.y * win[t + 1] + pin.w.z * win[t + 2] + pin.w.w * win[t + 3]);
             }
-            // new conv_state: the last three raw inputs, rows T .. T+2 of the window
+            // new conv_state: the last three raw inputs, rows T .. T+2 of the window,
+            // shifted in token by token (static indices keep the inputs in registers)
+            TA ns[KC - 1];
 #pragma unroll
-            for (int r = 0; r < KC - 1; ++r) {
-                TA nv = pin.s[r];
+            for (int r = 0; r < KC - 1; ++r) ns[r] = pin.s[r];
 #pragma unroll
-                for (int t = 0; t < MT + KC - 1; ++t)
-                    if (t == T + r) nv = t < KC - 1 ? pin.s[t] : pin.x[t - (KC - 1)];
-                cs[(size_t)r * CC + c] = nv;                 // this CTA owns channel c of sequence b
+            for (int t = 0; t < MT; ++t) {
+                if (t < T) {
+#pragma unroll
+                    for (int r = 0; r < KC - 2; ++r) ns[r] = ns[r + 1];
+                    ns[KC - 2] = pin.x[t];
+                }
             }
+#pragma unroll
+            for (int r = 0; r < KC - 1; ++r) cs[(size_t)r * CC + c] = ns[r];   // this CTA owns channel c of sequence b
             if (tid < 256) {
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
@@ -286,6 +292,11 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
                 st0[c] = src0[8 * c];
                 st1[c] = src1[8 * c];
             }
+            __syncwarp();                                // the rows are in registers: free both slots
+            if (lane == 0) {
+                multi_release(sm, a, u0);
+                multi_release(sm, a, u0 + 1);
+            }
             for (int t = 0; t < T; ++t) {
                 const float dec = sm.gate[t][h][0], beta = sm.gate[t][h][1];
                 const float4 *k4 = reinterpret_cast<const float4 *>(sm.k[t]) + g;
@@ -329,11 +340,6 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
             for (int c = 0; c < 4; ++c) {
                 __stcs(dst0 + 8 * c, st0[c]);
                 __stcs(dst1 + 8 * c, st1[c]);
-            }
-            __syncwarp();                                // this warp's reads of both slots are done
-            if (lane == 0) {
-                multi_release(sm, a, u0);
-                multi_release(sm, a, u0 + 1);
             }
         }
         multi_sync();                                    // all rows of y are in, and the abort flag agrees
