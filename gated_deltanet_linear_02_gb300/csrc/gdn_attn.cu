@@ -398,7 +398,10 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_block_kernel(const __grid_
                     po[h * AT_D + 128 + r] = acc1[h];
                 }
                 if (r < AT_G) {
-                    pml[2 * r] = m[r];
+                    float mr = m[0];                   // m[r], picked with static indices
+#pragma unroll
+                    for (int h = 1; h < AT_G; ++h) mr = r == h ? m[h] : mr;
+                    pml[2 * r] = mr;
                     pml[2 * r + 1] = ss.lred[0][r] + ss.lred[1][r] + ss.lred[2][r] + ss.lred[3][r];
                 }
             }

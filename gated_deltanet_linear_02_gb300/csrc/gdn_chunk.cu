@@ -245,7 +245,10 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     const int t0 = seq0 + CH * lc;
     const int nv = ci.w;                               // valid tokens in this chunk (1..64)
     const int nit = next_valid(item + (int)gridDim.x);
-    const int chan0[4] = {Q_OFF + kh * DK, K_OFF + kh * DK, V_OFF + kh * DV, V_OFF + (kh + HK) * DV};
+    // first channel of segment sg: q, k of K-head kh, v of V-heads kh and kh + 16
+    auto chan0 = [kh](int sg) {
+        return sg == 0 ? Q_OFF + kh * DK : sg == 1 ? K_OFF + kh * DK : V_OFF + (kh + (sg - 2) * HK) * DV;
+    };
     // gates of both V-heads; padded tokens get g = 0, beta = 0. After the first
     // item the logits were loaded ahead, during the previous item's stores.
     if (tid < 2 * CH) {
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
         // (zeros without one), not the rows before the sequence
         const int r = tid >> 6, sg = (tid >> 4) & 3, pc = tid & 15;
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (a.cs_in) x = __ldg(reinterpret_cast<const uint4 *>(a.cs_in + ((size_t)n * (KC - 1) + r) * CC + chan0[sg]) + pc);
+        if (a.cs_in) x = __ldg(reinterpret_cast<const uint4 *>(a.cs_in + ((size_t)n * (KC - 1) + r) * CC + chan0(sg)) + pc);
         *reinterpret_cast<uint4 *>(sm + S1_RAW + sg * RAW_SEG + r * RAW_ROWB + pc * 16) = x;
     }
     __syncthreads();
@@ -407,9 +410,10 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     if (!mbar_wait_bounded(smem_u32(&ss.bar), 0)) ss.abort = 1;
     tc::fence_after_sync();
 
-    unsigned char *blob[2];
-    blob[0] = a.blobs + ((size_t)g * HV + kh) * BLOB_BYTES;
-    blob[1] = a.blobs + ((size_t)g * HV + kh + HK) * BLOB_BYTES;
+    // the blobs of V-heads kh and kh + 16 (a function of h, not an array, so
+    // that a runtime h does not put the pointers in local memory)
+    unsigned char *const blob0 = a.blobs + ((size_t)g * HV + kh) * BLOB_BYTES;
+    auto blob = [&](int h) { return blob0 + (size_t)h * HK * BLOB_BYTES; };
 
     // ---- E. P = Mask o QK^T and beta * L from the M=64 accumulators (row t in
     //      TMEM lane 32*(t/16) + t%16), then Q~ and gamma_n. Warp w reads
@@ -444,7 +448,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
                         Lb[lb_at(t, s)] = s < t ? bt * dec * kk[cc] : 0.0f;
                         pv[e] = dec * qk[cc];
                     }
-                    *reinterpret_cast<float4 *>(blob[h] + BLOB_P + km<4>(t, cbase + c4 * 4, CH)) =
+                    *reinterpret_cast<float4 *>(blob(h) + BLOB_P + km<4>(t, cbase + c4 * 4, CH)) =
                         tc::tf32_rn(make_float4(pv[0], pv[1], pv[2], pv[3]));
                 }
             }
@@ -456,12 +460,14 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
         const float gm = ss.gam[h][t];
         const float4 x0 = *reinterpret_cast<const float4 *>(sm + S1_QS + km<4>(t, i8 * 8, DK));
         const float4 x1 = *reinterpret_cast<const float4 *>(sm + S1_QS + km<4>(t, i8 * 8 + 4, DK));
-        __align__(16) bf16 o[8] = {from_f<bf16>(x0.x * gm), from_f<bf16>(x0.y * gm), from_f<bf16>(x0.z * gm),
-                                   from_f<bf16>(x0.w * gm), from_f<bf16>(x1.x * gm), from_f<bf16>(x1.y * gm),
-                                   from_f<bf16>(x1.z * gm), from_f<bf16>(x1.w * gm)};
-        *reinterpret_cast<uint4 *>(blob[h] + BLOB_Q + km<2>(t, i8 * 8, DK)) = *reinterpret_cast<const uint4 *>(o);
+        auto pk = [gm](float lo, float hi) {            // two bf16 in one word, lo first
+            const __nv_bfloat162 v = __floats2bfloat162_rn(lo * gm, hi * gm);
+            return *reinterpret_cast<const uint32_t *>(&v);
+        };
+        *reinterpret_cast<uint4 *>(blob(h) + BLOB_Q + km<2>(t, i8 * 8, DK)) =
+            make_uint4(pk(x0.x, x0.y), pk(x0.z, x0.w), pk(x1.x, x1.y), pk(x1.z, x1.w));
     }
-    if (tid < 2) *reinterpret_cast<float *>(blob[tid] + BLOB_G) = ss.gam[tid][CH - 1];
+    if (tid < 2) *reinterpret_cast<float *>(blob(tid) + BLOB_G) = ss.gam[tid][CH - 1];
     tc::fence_before_sync();
     __syncthreads();
 
@@ -605,7 +611,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
             const int t = t4 * 4 + e;
             v[e] = ss.ktf[h][t] * *reinterpret_cast<const float *>(sm + S1_KS + km<4>(t, i, DK));
         }
-        *reinterpret_cast<float4 *>(blob[h] + BLOB_KT + km<4>(i, t4 * 4, CH)) =
+        *reinterpret_cast<float4 *>(blob(h) + BLOB_KT + km<4>(i, t4 * 4, CH)) =
             tc::tf32_rn(make_float4(v[0], v[1], v[2], v[3]));
     }
     if (!ss.abort && !mbar_wait_bounded(smem_u32(&ss.bar), 1)) ss.abort = 1;
@@ -637,12 +643,12 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
             tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_W + 64 * h + 16 * hf), wv);
             tc::wait_ld();
             if (!ss.abort) {
-                float *U = reinterpret_cast<float *>(blob[h] + BLOB_U);
+                float *U = reinterpret_cast<float *>(blob(h) + BLOB_U);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int t = 16 * hf + e;
                     U[t * DV + j] = u[e];
-                    *reinterpret_cast<bf16 *>(blob[h] + BLOB_W + km<2>(t, j, DK)) = from_f<bf16>(wv[e]);
+                    *reinterpret_cast<bf16 *>(blob(h) + BLOB_W + km<2>(t, j, DK)) = from_f<bf16>(wv[e]);
                 }
             }
         }

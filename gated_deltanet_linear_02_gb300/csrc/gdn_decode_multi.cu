@@ -11,18 +11,20 @@
 // by a factor of T.
 //
 // Structure. One persistent CTA per SM with 16 warps streams the states
-// through six 32 KiB shared-memory slots with TMA bulk copies, a full mbarrier
-// per slot. There is no producer warp: the last warp to release a slot (a
-// shared counter per slot) issues the copy of the unit that goes there next,
-// which keeps the CTA at 512 threads and so 128 registers a thread. An item is
-// (sequence b, K-head kh) with both V-heads kh and kh + 16. In an
-// item's prologue each thread convolves one channel over the window
-// [conv_state (3 rows), x_0 .. x_{T-1}] and shifts T rows into conv_state. The
-// q and k rows are L2-normalised per token, and the gates come per token and
-// V-head. In the sweep, lanes 8r..8r+7 of a warp hold state row r (16 keys
-// each) of both halves of a state (rows r' and 64 + r' of the two slots of
-// one head), so that each k and q load of a token serves two rows. The warp's
-// rows apply tokens 0..T-1 in order: decay, pred, delta, write, read. The output stage applies the gated RMSNorm per token.
+// through six 32 KiB shared-memory slots, a full mbarrier per slot. There is
+// no producer warp: the last warp to finish with a slot (a shared counter per
+// slot) issues its copies, which keeps the CTA at 512 threads and so 128
+// registers a thread. An item is (sequence b, K-head kh) with both V-heads kh
+// and kh + 16. In an item's prologue each thread convolves one channel over the
+// window [conv_state (3 rows), x_0 .. x_{T-1}] and shifts T rows into
+// conv_state; then warp w L2-normalises q or k of one token, and the gates come
+// per token and V-head. In the sweep, head h is one pass over its two slots:
+// a group of 16 lanes holds four of its rows (8 keys a lane), so each k and q
+// load of a token serves four rows, and applies tokens 0..T-1 in order: decay,
+// pred, delta, write, read. The new rows go back into their slot, and a TMA
+// bulk store drains the slot to HBM while the warps go on; once it has read
+// the slot, the next unit is loaded there. The output stage gives warp w the
+// gated RMSNorm of one (token, head) row.
 #include "gdn_async.cuh"
 #include "gdn_common.cuh"
 
@@ -61,9 +63,8 @@ struct MultiSmem {
     alignas(16) float y[MT][2][DV];
     alignas(8) uint64_t full[MD_SLOTS];
     int released[MD_SLOTS];                          // warps done with the slot's current unit
-    float red[MT][8];                                // per token: q sums (warps 0..3), k sums (4..7)
-    float ored[MT][8];                               // per token: y^2 sums of head 0 (warps 0..3), head 1 (4..7)
-    float gate[MT][2][2];                            // per token and V-head: decay exp(g), beta
+    int owed[MD_WARPS][2];                           // loads a warp owes (multi_release), -1 for none
+    float gate[MT][2][3];                            // per token and V-head: decay exp(g), beta, 1 / exp(g)
     int pending[MD_SLOTS];
     int abort;
 };
@@ -73,14 +74,19 @@ static_assert(md_smem<MT_MAX>() <= 232448, "decode_multi shared memory");
 
 // Loads unit u (u = (2 m + h) * MD_UNITS + part) of this CTA into slot u % MD_SLOTS.
 // Caller: one thread; the unit's item exists and the slot is free.
-template <int MT>
-__device__ __forceinline__ void multi_issue_load(MultiSmem<MT> &sm, const MultiArgs &a, int u)
+// Rows [64 part, 64 part + 64) of the state of unit u.
+__device__ __forceinline__ char *multi_unit_ptr(const MultiArgs &a, int u)
 {
     const int item = blockIdx.x + (u / (2 * MD_UNITS)) * gridDim.x;
     const int h = (u / MD_UNITS) & 1, part = u % MD_UNITS;
     const int b = item / HK, kh = item % HK, vh = kh + HK * h;
-    const char *src = reinterpret_cast<const char *>(a.ssm_state + ((size_t)b * HV + vh) * (DV * DK)) +
-                      (size_t)part * MD_SLOT_BYTES;
+    return reinterpret_cast<char *>(a.ssm_state + ((size_t)b * HV + vh) * (DV * DK)) + (size_t)part * MD_SLOT_BYTES;
+}
+
+template <int MT>
+__device__ __forceinline__ void multi_issue_load(MultiSmem<MT> &sm, const MultiArgs &a, int u)
+{
+    const char *src = multi_unit_ptr(a, u);
     const int slot = u % MD_SLOTS;
     sm.pending[slot] = u;
     const uint32_t bar = smem_u32(&sm.full[slot]);
@@ -99,14 +105,22 @@ __device__ __forceinline__ int multi_channel(int kh, int tid)
     return V_OFF + (kh + HK) * DV + (tid - 384);
 }
 
+// Four consecutive activations as loaded (converted only when used, so that a
+// prefetch does not wait for its data).
+template <typename TA> struct Raw4;
+template <> struct Raw4<float> { using type = float4; };
+template <> struct Raw4<bf16> { using type = uint2; };
+__device__ __forceinline__ float4 raw4_f(float4 v) { return v; }
+__device__ __forceinline__ float4 raw4_f(uint2 u) { return load4(reinterpret_cast<const bf16 *>(&u)); }
+
 // An item's global prologue inputs held by thread tid, loaded one item ahead:
-// its channel's conv_state rows, its T inputs and taps; for tid < 256 the z of
-// output column (V-head kh + 16 (tid >> 7), j = tid & 127) of every token; for
+// its channel's conv_state rows, its T inputs and taps; for warp w < 2T the z
+// of token w >> 1, V-head kh + 16 (w & 1), columns 4 lane .. 4 lane + 3; for
 // tid < 2T the gate inputs of token tid >> 1 and V-head kh + 16 (tid & 1).
 template <typename TA, int MT> struct MultiIn {
     TA s[KC - 1];
     TA x[MT];
-    TA zc[MT];
+    typename Raw4<TA>::type z;
     TA al, be;
     float4 w;
     float A_log, dt_bias;
@@ -126,9 +140,11 @@ __device__ __forceinline__ MultiIn<TA, MT> multi_load(const MultiArgs &a, int it
     for (int r = 0; r < KC - 1; ++r) p.s[r] = cs[(size_t)r * CC + c];
 #pragma unroll
     for (int t = 0; t < MT; ++t) p.x[t] = t < T ? x[(size_t)t * CC + c] : from_f<TA>(0.0f);
-    const TA *zb = static_cast<const TA *>(a.z) + b * (size_t)T * DI + (size_t)(kh + HK * (tid >> 7)) * DV + (tid & 127);
-#pragma unroll
-    for (int t = 0; t < MT; ++t) p.zc[t] = (tid < 2 * DV && t < T) ? zb[(size_t)t * DI] : from_f<TA>(0.0f);
+    const int w = tid >> 5;
+    p.z = typename Raw4<TA>::type{};
+    if (w < 2 * T)
+        p.z = *reinterpret_cast<const typename Raw4<TA>::type *>(
+            static_cast<const TA *>(a.z) + (b * T + (w >> 1)) * (size_t)DI + (size_t)(kh + HK * (w & 1)) * DV + 4 * (tid & 31));
     p.al = p.be = from_f<TA>(0.0f);
     p.A_log = p.dt_bias = 0.0f;
     if (tid < 2 * T) {
@@ -143,28 +159,73 @@ __device__ __forceinline__ MultiIn<TA, MT> multi_load(const MultiArgs &a, int it
 
 __device__ __forceinline__ void multi_sync() { __syncthreads(); }
 
+// Gamma below this is folded into S^: 1/Gamma stays far inside the fp32 range.
+constexpr float MD_RENORM = 0x1p-60f;
+
+__device__ __forceinline__ void scale4(float4 &v, float s)
+{
+    v.x *= s; v.y *= s; v.z *= s; v.w *= s;
+}
+__device__ __forceinline__ void axpy4(float4 &v, const float4 &x, float s)
+{
+    v.x = fmaf(x.x, s, v.x); v.y = fmaf(x.y, s, v.y); v.z = fmaf(x.z, s, v.z); v.w = fmaf(x.w, s, v.w);
+}
+__device__ __forceinline__ float dot4(const float4 &v, const float4 &x, float acc)
+{
+    return fmaf(v.w, x.w, fmaf(v.z, x.z, fmaf(v.y, x.y, fmaf(v.x, x.x, acc))));
+}
+
+// Sums four values p[0..3] over the 16 lanes of a half-warp (g = lane & 15)
+// in five shuffles, halving the set at each step: lanes whose bit 3 is clear
+// keep p[0], p[1] and send p[2], p[3] to their partner, and so on. Returns the
+// total of p[g >> 2] (each total lands in four lanes).
+__device__ __forceinline__ float group16_reduce4(const float (&p)[4], int g)
+{
+    const bool hi3 = g & 8, hi2 = g & 4;
+    const float a0 = (hi3 ? p[2] : p[0]) + __shfl_xor_sync(0xffffffffu, hi3 ? p[0] : p[2], 8);
+    const float a1 = (hi3 ? p[3] : p[1]) + __shfl_xor_sync(0xffffffffu, hi3 ? p[1] : p[3], 8);
+    float b = (hi2 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, hi2 ? a0 : a1, 4);
+    b += __shfl_xor_sync(0xffffffffu, b, 2);
+    return b + __shfl_xor_sync(0xffffffffu, b, 1);
+}
+
 template <int MT>
 __device__ __forceinline__ bool multi_unit_exists(const MultiArgs &a, int u)
 {
     return blockIdx.x + (u / (2 * MD_UNITS)) * (int)gridDim.x < a.n_items;
 }
 
-// Lane 0 of a warp that has finished reading unit u in slot u % MD_SLOTS. The
-// sixteenth warp to get here frees the slot and loads unit u + MD_SLOTS into it.
-// The fences order every warp's reads of the slot before the counter updates,
-// and the last update before the copy, which the proxy fence hands to TMA.
+// Lane 0 of a warp whose lanes have written their rows of unit u's new state
+// back into slot u % MD_SLOTS and fenced them for the async proxy. The
+// sixteenth warp to get here stores the slot to the unit's state with a bulk
+// copy and returns unit u + MD_SLOTS, which it loads into the slot later
+// (multi_refill), once the copy has surely read the slot; other warps, or
+// when there is no such unit, get -1. The block fences order every warp's
+// writes before the counter updates, and the last update before the copies.
 template <int MT>
-__device__ __forceinline__ void multi_release(MultiSmem<MT> &sm, const MultiArgs &a, int u)
+__device__ __forceinline__ int multi_release(MultiSmem<MT> &sm, const MultiArgs &a, int u)
 {
     const int slot = u % MD_SLOTS;
     __threadfence_block();
-    if (atomicAdd(&sm.released[slot], 1) != MD_WARPS - 1) return;
+    if (atomicAdd(&sm.released[slot], 1) != MD_WARPS - 1) return -1;
     __threadfence_block();
     sm.released[slot] = 0;
     sm.pending[slot] = -1;
+    const uint32_t src = smem_u32(sm.slot[slot]);
+    char *dst = multi_unit_ptr(a, u);
+    bulk_s2g(dst, src, MD_SLOT_BYTES / 2);
+    bulk_s2g(dst + MD_SLOT_BYTES / 2, src + MD_SLOT_BYTES / 2, MD_SLOT_BYTES / 2);
+    bulk_commit();
     const int nu = u + MD_SLOTS;
-    if (sm.abort || !multi_unit_exists<MT>(a, nu)) return;
-    fence_proxy_async_smem();
+    return sm.abort || !multi_unit_exists<MT>(a, nu) ? -1 : nu;
+}
+
+// The load multi_release returned, issued by the same thread one pass later:
+// its own bulk stores have read the slot by then (the wait is a formality).
+template <int MT>
+__device__ __forceinline__ void multi_refill(MultiSmem<MT> &sm, const MultiArgs &a, int nu)
+{
+    bulk_wait_read();
     multi_issue_load(sm, a, nu);
 }
 
@@ -183,6 +244,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
             sm.released[i] = 0;
             sm.pending[i] = -1;
         }
+        for (int w = 0; w < MD_WARPS; ++w) sm.owed[w][0] = sm.owed[w][1] = -1;
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -194,6 +256,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
         for (int u = 0; u < MD_SLOTS && multi_unit_exists<MT>(a, u); ++u) multi_issue_load(sm, a, u);
 
     const float scale = rsqrtf((float)DK);
+    const float4 nw = load4(a.norm_w + 4 * lane);      // norm weights of columns 4 lane .. 4 lane + 3
     MultiIn<TA, MT> pin;
     if ((int)blockIdx.x < a.n_items) pin = multi_load<TA, MT>(a, blockIdx.x, tid);
     for (int m = 0;; ++m) {
@@ -212,12 +275,10 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
             for (int r = 0; r < KC - 1; ++r) win[r] = to_f(pin.s[r]);
 #pragma unroll
             for (int t = 0; t < MT; ++t) win[KC - 1 + t] = to_f(pin.x[t]);
-            float xh[MT];
+            float xh[MT];                                // every slot computed, so tokens interleave
 #pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                if (t >= T) break;
+            for (int t = 0; t < MT; ++t)
                 xh[t] = silu_f(pin.w.x * win[t] + pin.w.y * win[t + 1] + pin.w.z * win[t + 2] + pin.w.w * win[t + 3]);
-            }
             // new conv_state: the last three raw inputs, rows T .. T+2 of the window,
             // shifted in token by token (static indices keep the inputs in registers)
             TA ns[KC - 1];
@@ -233,145 +294,141 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
             }
 #pragma unroll
             for (int r = 0; r < KC - 1; ++r) cs[(size_t)r * CC + c] = ns[r];   // this CTA owns channel c of sequence b
-            if (tid < 256) {
+            float *dst = tid < 128 ? &sm.q[0][tid] : tid < 256 ? &sm.k[0][tid - 128] : &sm.v[0][(tid - 256) >> 7][tid & 127];
+            const int tstride = tid < 256 ? DK : 2 * DV;
 #pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    if (t >= T) break;
-                    const float ss = warp_sum(xh[t] * xh[t]);
-                    if (lane == 0) sm.red[t][warp] = ss;
-                }
-            }
+            for (int t = 0; t < MT; ++t)
+                if (t < T) dst[t * tstride] = xh[t];
             if (tid < 2 * T) {
                 float ga, gb;
                 gates_f(pin.A_log, pin.dt_bias, to_f(pin.al), to_f(pin.be), ga, gb);
                 sm.gate[tid >> 1][tid & 1][0] = ga;
                 sm.gate[tid >> 1][tid & 1][1] = gb;
+                sm.gate[tid >> 1][tid & 1][2] = 1.0f / ga;   // inf for a decay of 0: then Gamma is renormalised
             }
             multi_sync();
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                if (t >= T) break;
-                if (tid < 128)
-                    sm.q[t][tid] = xh[t] * rsqrtf(sm.red[t][0] + sm.red[t][1] + sm.red[t][2] + sm.red[t][3] + a.l2_eps);
-                else if (tid < 256)
-                    sm.k[t][tid - 128] =
-                        xh[t] * rsqrtf(sm.red[t][4] + sm.red[t][5] + sm.red[t][6] + sm.red[t][7] + a.l2_eps);
-                else
-                    sm.v[t][(tid - 256) >> 7][tid & 127] = xh[t];
+            if (warp < 2 * T) {                          // L2 norm of q_t (w even) or k_t (w odd), t = w >> 1
+                float4 *vec = reinterpret_cast<float4 *>((warp & 1) ? sm.k[warp >> 1] : sm.q[warp >> 1]) + lane;
+                float4 v4 = *vec;
+                const float r = rsqrtf(warp_sum(dot4(v4, v4, 0.0f)) + a.l2_eps);
+                scale4(v4, r);
+                *vec = v4;
             }
             multi_sync();
         }
-        TA zcur[MT];
-#pragma unroll
-        for (int t = 0; t < MT; ++t) zcur[t] = pin.zc[t];
+        const typename Raw4<TA>::type zcur = pin.z;
         if (item + (int)gridDim.x < a.n_items) pin = multi_load<TA, MT>(a, item + gridDim.x, tid);
 
-        // ---- the two states: each row takes tokens 0..T-1 in order
-        // Each lane group holds two rows of one head, row jl of part 0 and of
-        // part 1, so that every k and q load of a token serves both.
-        const int rr = lane >> 3, g = lane & 7;         // row of the warp's four; float4 group within it
-        static_assert(MD_UNITS == 2, "a head is two slots");
+        // ---- the two states: each row takes tokens 0..T-1 in order.
+        // Head h is one pass over its two slots. A group of 16 lanes holds four
+        // of its rows, jl and jl + 32 of each slot, 8 keys a lane, so every k
+        // and q load of a token serves four rows. The state is kept as
+        // Gamma * S^ with Gamma the running product of the head's decays: the
+        // decay costs one multiply per token instead of one per element, and
+        // S^ is rescaled only when Gamma falls below MD_RENORM (and at the
+        // end). In this form, with Gamma_t = Gamma_{t-1} exp(g_t),
+        //   pred = Gamma_t (S^ k),  S^ += k (beta (v - pred) / Gamma_t),
+        //   y = Gamma_t (S^ q) / sqrt(d_k).
+        static_assert(MD_UNITS == 2 && MD_SLOT_ROWS == 2 * 32 && MD_WARPS * 2 == 32, "row mapping");
+        const int g = lane & 15;                         // float4 columns g and g + 16 of each row
+        const int jl = warp * 2 + (lane >> 4);           // rows jl, jl + 32 of each slot
+        const int qown = g >> 2;                         // the row this lane reduces (see row_of)
+        auto row_of = [&](int q) { return (q >> 1) * MD_SLOT_ROWS + jl + 32 * (q & 1); };   // row j of the head
+        const int jown = row_of(qown);
         for (int h = 0; h < 2; ++h) {
             const int u0 = 2 * MD_UNITS * m + MD_UNITS * h;   // units u0 (rows 0..63), u0 + 1 (rows 64..127)
-            const int s0 = u0 % MD_SLOTS, s1 = (u0 + 1) % MD_SLOTS;
+            if (lane == 0) {                             // units of later passes, owed since the last one
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    if (sm.owed[warp][i] >= 0 && !aborted) multi_refill(sm, a, sm.owed[warp][i]);
+                    sm.owed[warp][i] = -1;
+                }
+            }
             if (aborted) continue;                       // skip the work, keep the barriers in step
-            if (!mbar_wait_bounded(smem_u32(&sm.full[s0]), (uint32_t)((u0 / MD_SLOTS) & 1)) ||
-                !mbar_wait_bounded(smem_u32(&sm.full[s1]), (uint32_t)(((u0 + 1) / MD_SLOTS) & 1))) {
+            if (!mbar_wait_bounded(smem_u32(&sm.full[u0 % MD_SLOTS]), (uint32_t)((u0 / MD_SLOTS) & 1)) ||
+                !mbar_wait_bounded(smem_u32(&sm.full[(u0 + 1) % MD_SLOTS]), (uint32_t)(((u0 + 1) / MD_SLOTS) & 1))) {
                 sm.abort = 1;
                 continue;
             }
-            const int vh = kh + HK * h;
-            float *Sg = a.ssm_state + (b * HV + vh) * (size_t)(DV * DK);
-            const int jl = warp * 4 + rr;                // row within each slot
-            const int j0 = jl, j1 = MD_SLOT_ROWS + jl;
-            const float4 *src0 = reinterpret_cast<const float4 *>(sm.slot[s0]) + jl * (DK / 4) + g;
-            const float4 *src1 = reinterpret_cast<const float4 *>(sm.slot[s1]) + jl * (DK / 4) + g;
-            float4 st0[4], st1[4];
+            float4 st[4][2];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                st0[c] = src0[8 * c];
-                st1[c] = src1[8 * c];
+            for (int q = 0; q < 4; ++q) {
+                const float4 *src = reinterpret_cast<const float4 *>(sm.slot[(u0 + (q >> 1)) % MD_SLOTS]) +
+                                    (jl + 32 * (q & 1)) * (DK / 4) + g;
+                st[q][0] = src[0];
+                st[q][1] = src[16];
             }
-            __syncwarp();                                // the rows are in registers: free both slots
-            if (lane == 0) {
-                multi_release(sm, a, u0);
-                multi_release(sm, a, u0 + 1);
-            }
+            float gam = 1.0f, igam = 1.0f;               // Gamma and 1 / Gamma
             for (int t = 0; t < T; ++t) {
-                const float dec = sm.gate[t][h][0], beta = sm.gate[t][h][1];
+                float G = gam * sm.gate[t][h][0], iG = igam * sm.gate[t][h][2];
+                if (G < MD_RENORM) {                     // fold Gamma into S^ (warp-uniform)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        scale4(st[q][0], G);
+                        scale4(st[q][1], G);
+                    }
+                    G = iG = 1.0f;
+                }
+                gam = G;
+                igam = iG;
                 const float4 *k4 = reinterpret_cast<const float4 *>(sm.k[t]) + g;
-                float pa0 = 0.0f, pb0 = 0.0f, pa1 = 0.0f, pb1 = 0.0f;
-                float4 kk[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    kk[c] = k4[8 * c];
-                    st0[c].x *= dec; st0[c].y *= dec; st0[c].z *= dec; st0[c].w *= dec;             // (a)
-                    st1[c].x *= dec; st1[c].y *= dec; st1[c].z *= dec; st1[c].w *= dec;
-                    pa0 = fmaf(st0[c].x, kk[c].x, fmaf(st0[c].y, kk[c].y, pa0));
-                    pb0 = fmaf(st0[c].z, kk[c].z, fmaf(st0[c].w, kk[c].w, pb0));
-                    pa1 = fmaf(st1[c].x, kk[c].x, fmaf(st1[c].y, kk[c].y, pa1));
-                    pb1 = fmaf(st1[c].z, kk[c].z, fmaf(st1[c].w, kk[c].w, pb1));
-                }
-                const float pred0 = group_sum<8>(pa0 + pb0), pred1 = group_sum<8>(pa1 + pb1);         // (b)
-                const float d0 = (sm.v[t][h][j0] - pred0) * beta, d1 = (sm.v[t][h][j1] - pred1) * beta;
                 const float4 *q4 = reinterpret_cast<const float4 *>(sm.q[t]) + g;
-                float ya0 = 0.0f, yb0 = 0.0f, ya1 = 0.0f, yb1 = 0.0f;
+                const float4 k0 = k4[0], k1 = k4[16];
+                float p[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float4 qq = q4[8 * c];
-                    st0[c].x = fmaf(kk[c].x, d0, st0[c].x); st0[c].y = fmaf(kk[c].y, d0, st0[c].y);   // (c)
-                    st0[c].z = fmaf(kk[c].z, d0, st0[c].z); st0[c].w = fmaf(kk[c].w, d0, st0[c].w);
-                    st1[c].x = fmaf(kk[c].x, d1, st1[c].x); st1[c].y = fmaf(kk[c].y, d1, st1[c].y);
-                    st1[c].z = fmaf(kk[c].z, d1, st1[c].z); st1[c].w = fmaf(kk[c].w, d1, st1[c].w);
-                    ya0 = fmaf(st0[c].x, qq.x, fmaf(st0[c].y, qq.y, ya0));
-                    yb0 = fmaf(st0[c].z, qq.z, fmaf(st0[c].w, qq.w, yb0));
-                    ya1 = fmaf(st1[c].x, qq.x, fmaf(st1[c].y, qq.y, ya1));
-                    yb1 = fmaf(st1[c].z, qq.z, fmaf(st1[c].w, qq.w, yb1));
+                for (int q = 0; q < 4; ++q) p[q] = dot4(st[q][1], k1, dot4(st[q][0], k0, 0.0f));
+                const float pred = G * group16_reduce4(p, g);
+                const float dn = (sm.v[t][h][jown] - pred) * sm.gate[t][h][1] * iG;
+                float d[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) d[q] = __shfl_sync(0xffffffffu, dn, (lane & 16) | (q << 2));
+                const float4 q0 = q4[0], q1 = q4[16];
+                float y[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    axpy4(st[q][0], k0, d[q]);
+                    axpy4(st[q][1], k1, d[q]);
+                    y[q] = dot4(st[q][1], q1, dot4(st[q][0], q0, 0.0f));
                 }
-                const float y0 = group_sum<8>(ya0 + yb0), y1 = group_sum<8>(ya1 + yb1);                 // (d)
-                if (g == 0) {
-                    sm.y[t][h][j0] = y0 * scale;
-                    sm.y[t][h][j1] = y1 * scale;
-                }
+                const float yo = group16_reduce4(y, g);
+                if ((g & 3) == 0) sm.y[t][h][jown] = yo * G * scale;
             }
-            float4 *dst0 = reinterpret_cast<float4 *>(Sg + (size_t)j0 * DK) + g;
-            float4 *dst1 = reinterpret_cast<float4 *>(Sg + (size_t)j1 * DK) + g;
+            // the new rows go back where they came from; the slots' bulk stores
+            // then drain them to HBM while the warps go on
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                __stcs(dst0 + 8 * c, st0[c]);
-                __stcs(dst1 + 8 * c, st1[c]);
+            for (int q = 0; q < 4; ++q) {
+                float4 *dst = reinterpret_cast<float4 *>(sm.slot[(u0 + (q >> 1)) % MD_SLOTS]) +
+                              (jl + 32 * (q & 1)) * (DK / 4) + g;
+                scale4(st[q][0], gam);
+                scale4(st[q][1], gam);
+                dst[0] = st[q][0];
+                dst[16] = st[q][1];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                sm.owed[warp][0] = multi_release(sm, a, u0);
+                sm.owed[warp][1] = multi_release(sm, a, u0 + 1);
             }
         }
         multi_sync();                                    // all rows of y are in, and the abort flag agrees
         if (aborted) break;
 
-        // ---- gated RMSNorm of both heads for every token, times silu(z) ("Output path")
-        if (tid < 256) {
-            const int h = tid >> 7, j = tid & 127;
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                if (t >= T) break;
-                const float yv = sm.y[t][h][j];
-                const float ss = warp_sum(yv * yv);
-                if (lane == 0) sm.ored[t][warp] = ss;
-            }
+        // ---- gated RMSNorm times silu(z) ("Output path"): warp w < 2T takes
+        //      token w >> 1 of V-head kh + 16 (w & 1), columns 4 lane .. 4 lane + 3
+        if (warp < 2 * T) {
+            const int t = warp >> 1, h = warp & 1;
+            const float4 y4 = reinterpret_cast<const float4 *>(sm.y[t][h])[lane];
+            const float rr2 = rsqrtf(warp_sum(dot4(y4, y4, 0.0f)) * (1.0f / DV) + a.norm_eps);
+            const float4 zf = raw4_f(zcur);
+            const float4 o = make_float4(y4.x * rr2 * nw.x * silu_f(zf.x), y4.y * rr2 * nw.y * silu_f(zf.y),
+                                         y4.z * rr2 * nw.z * silu_f(zf.z), y4.w * rr2 * nw.w * silu_f(zf.w));
+            store4(static_cast<TO *>(a.out) + (b * T + t) * (size_t)DI + (size_t)(kh + HK * h) * DV + 4 * lane, o);
         }
-        multi_sync();
-        if (tid < 256) {
-            const int h = tid >> 7, j = tid & 127;
-            const float nw = a.norm_w[j];
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                if (t >= T) break;
-                const float *r4 = sm.ored[t] + 4 * h;
-                const float rr2 = rsqrtf((r4[0] + r4[1] + r4[2] + r4[3]) * (1.0f / DV) + a.norm_eps);
-                const size_t o = (b * T + t) * (size_t)DI + (size_t)(kh + HK * h) * DV + j;
-                static_cast<TO *>(a.out)[o] = from_f<TO>(sm.y[t][h][j] * rr2 * nw * silu_f(to_f(zcur[t])));
-            }
-        }
-        // the next prologue writes q/k/v/red/gate, none of which the lines above read
+        // the next prologue writes q/k/v/gate and the next sweep y only after a barrier
     }
     if (aborted && tid == 0) atomicExch(&g_multi_error, (unsigned int)GDN_ERR_TIMEOUT);
+    if (lane == 0) bulk_wait_all();                      // the state stores this lane issued are done
     multi_sync();                                        // no release is still running
     if (aborted && tid == 0)   // let the copies still in flight land before shared memory is released
         for (int i = 0; i < MD_SLOTS; ++i)

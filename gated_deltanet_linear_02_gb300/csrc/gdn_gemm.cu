@@ -72,6 +72,24 @@ struct ProjOut {
     int nseg;
 };
 
+// Address of output element (m, n): the segment holding column n is picked by
+// a compare chain with static indices, so the kernel parameter stays in the
+// constant bank (a runtime index would copy the struct to local memory).
+template <typename TO>
+__device__ __forceinline__ TO *proj_out_addr(const ProjOut &out, int m, int n)
+{
+    void *p = out.ptr[0];
+    int ld = out.ld[0], c0 = out.c0[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i)
+        if (i < out.nseg && n >= out.c0[i]) {
+            p = out.ptr[i];
+            ld = out.ld[i];
+            c0 = out.c0[i];
+        }
+    return static_cast<TO *>(p) + (size_t)m * ld + (n - c0);
+}
+
 template <int BN>
 struct GemmSmem {
     static constexpr int STAGES = GemmCfg<BN>::STAGES;
@@ -219,9 +237,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_consta
                               *reinterpret_cast<float(*)[16]>(v + 16));
                 tc::wait_ld();
                 const int n = nt * GM_BN + c;          // first output column of this chunk
-                int sg = 0;
-                while (sg + 1 < out.nseg && n >= out.c0[sg + 1]) ++sg;
-                TO *dst = static_cast<TO *>(out.ptr[sg]) + (size_t)m * out.ld[sg] + (n - out.c0[sg]);
+                TO *dst = proj_out_addr<TO>(out, m, n);
                 if (m < M && n < N) {
                     if (sizeof(TO) == 4) {
                         float4 *d4 = reinterpret_cast<float4 *>(dst);
@@ -265,9 +281,7 @@ __global__ void __launch_bounds__(GM_THREADS, 1) proj_kernel(const __grid_consta
                     }
                 const int m = mt * GM_BM + rr, n = nt * GM_BN + col;
                 if (m < M && n < N) {
-                    int sg = 0;
-                    while (sg + 1 < out.nseg && n >= out.c0[sg + 1]) ++sg;
-                    TO *dst = static_cast<TO *>(out.ptr[sg]) + (size_t)m * out.ld[sg] + (n - out.c0[sg]);
+                    TO *dst = proj_out_addr<TO>(out, m, n);
                     if (sizeof(TO) == 4) {
                         *reinterpret_cast<float4 *>(dst) = acc;
                     } else {
