@@ -125,3 +125,24 @@ def test_multi_empty_batch_is_noop(ops):
                      torch.zeros(0, I.HV, I.DV, I.DK, dtype=torch.float32, device=DEV),
                      torch.zeros(0, 2, I.D_INNER, dtype=torch.float32, device=DEV), cparams=cp)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("act", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [3, 8])
+def test_multi_strong_decays(ops, act, T):
+    # Large alpha gives g = -exp(A_log) softplus(alpha + dt_bias) from about -7
+    # down to below -100, where exp(g) is 0 in fp32: the kernel's running decay
+    # product crosses its renormalisation threshold after one or two tokens, or
+    # meets a decay of exactly 0. Heads vh % 3 == 2 and every third token keep
+    # the ordinary gates, so strong and weak decays alternate within a state.
+    lp, st, conv0, S0 = case(I.seed_of(7, 200 + T), 5, T, act)
+    al = st.alpha.float().clone()
+    vh = torch.arange(I.HV)
+    for t in range(T):
+        if t % 3 == 2:
+            continue
+        al[:, t, vh % 3 == 0] = 8.0
+        al[:, t, vh % 3 == 1] = 30.0
+    st.alpha = al.to(act)
+    out, conv, S = run_multi(ops, lp, st, conv0, S0, torch.float32)
+    check(out, conv, S, oracle_multi(lp, st, conv0, S0), act, f"decode_multi strong decays T={T} {act}")
