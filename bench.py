@@ -65,13 +65,13 @@ ATTN_BYTES_PER_CALL = BATCH * 2 * ATTN_CTX * 256 * 2 * 2 + 3 * BATCH * 16 * 256 
 # DRAM traffic of one attn_block_kernel launch at B=256 (ncu capture in
 # profiles/attn_decode_B256_ctx4096.md). None once the kernel or its launch
 # shape changes without a new capture.
-ATTN_TRAFFIC_PER_CALL = 2_149_658_880 + 19_715_840
+ATTN_TRAFFIC_PER_CALL = 2_149_655_040 + 18_066_688
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch at B=256
 # (one layer, cold L2), from the ncu capture in
 # profiles/decode_step_kernel_B256.md. Set to None whenever the kernel changes
 # without a new capture.
-DECODE_TRAFFIC_PER_LAUNCH = 555_954_944 + 490_157_056
+DECODE_TRAFFIC_PER_LAUNCH = 555_980_032 + 490_060_544
 
 
 def load_peaks():
