@@ -146,3 +146,22 @@ def test_multi_strong_decays(ops, act, T):
     st.alpha = al.to(act)
     out, conv, S = run_multi(ops, lp, st, conv0, S0, torch.float32)
     check(out, conv, S, oracle_multi(lp, st, conv0, S0), act, f"decode_multi strong decays T={T} {act}")
+
+
+def test_multi_bench_launch_B256_T4_sampled(ops):
+    # The benchmarked launch: B=256 sequences, T=4 tokens each, bf16 in and out
+    # (27 items per persistent CTA). Every output and state is checked finite;
+    # eight seeded sequences against the oracle.
+    B, T = 256, 4
+    lp, st, conv0, S0 = case(I.seed_of(3, 100), B, T, torch.bfloat16)
+    out, conv, S = run_multi(ops, lp, st, conv0, S0, torch.bfloat16)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(S).all()
+    seqs = sorted(set(int(x) for x in np.random.default_rng(41).choice(B, 8, replace=False)) | {0, B - 1})
+    sel = torch.tensor(seqs)
+    sub = I.Streams(st.qkv[sel], st.z[sel], st.alpha[sel], st.beta[sel])
+    ref = oracle_multi(lp, sub, conv0[sel], S0[sel])
+    ro, rc, rS = ref
+    e_o, e_S = tl.max_rel(out[sel].float(), ro), tl.max_rel(S[sel], rS)
+    print(f"decode_multi B=256 T=4 sampled {seqs}: out {e_o:.2e} state {e_S:.2e}")
+    assert e_o < tl.TOL_BF16_OUT + tl.BF16_ROUND and e_S < tl.TOL_BF16_STATE
+    assert tl.max_rel(conv[sel], rc) == 0.0
