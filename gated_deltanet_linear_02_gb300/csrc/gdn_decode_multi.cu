@@ -359,6 +359,9 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
                 st[q][1] = src[16];
             }
             float gam = 1.0f, igam = 1.0f;               // Gamma and 1 / Gamma
+            // y of each token is stored during the next one, so that the next
+            // token's work need not wait for the reduction behind it
+            float y_prev = 0.0f, yscale_prev = 0.0f;
             for (int t = 0; t < T; ++t) {
                 float G = gam * sm.gate[t][h][0], iG = igam * sm.gate[t][h][2];
                 if (G < MD_RENORM) {                     // fold Gamma into S^ (warp-uniform)
@@ -390,9 +393,11 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
                     axpy4(st[q][1], k1, d[q]);
                     y[q] = dot4(st[q][1], q1, dot4(st[q][0], q0, 0.0f));
                 }
-                const float yo = group16_reduce4(y, g);
-                if ((g & 3) == 0) sm.y[t][h][jown] = yo * G * scale;
+                if (t > 0 && (g & 3) == 0) sm.y[t - 1][h][jown] = y_prev * yscale_prev;
+                y_prev = group16_reduce4(y, g);
+                yscale_prev = G * scale;
             }
+            if ((g & 3) == 0) sm.y[T - 1][h][jown] = y_prev * yscale_prev;
             // the new rows go back where they came from; the slots' bulk stores
             // then drain them to HBM while the warps go on
 #pragma unroll
