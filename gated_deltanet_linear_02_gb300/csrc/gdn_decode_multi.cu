@@ -22,8 +22,8 @@
 // a group of 16 lanes holds four of its rows (8 keys a lane), so each k and q
 // load of a token serves four rows, and applies tokens 0..T-1 in order: decay,
 // pred, delta, write, read. The new rows go back into their slot, and a TMA
-// bulk store drains the slot to HBM while the warps go on; once it has read
-// the slot, the next unit is loaded there. The output stage gives warp w the
+// bulk store drains the slot to HBM while the warps go on; one pass later,
+// when the store has read the slot, the next unit is loaded there. The output stage gives warp w the
 // gated RMSNorm of one (token, head) row.
 #include "gdn_async.cuh"
 #include "gdn_common.cuh"
@@ -41,7 +41,7 @@ constexpr int MD_SLOT_ROWS = 64;                            // rows j of S^T per
 constexpr int MD_UNITS = DV / MD_SLOT_ROWS;                 // slots per state (2)
 constexpr int MD_SLOTS = 6;
 constexpr uint32_t MD_SLOT_BYTES = MD_SLOT_ROWS * DK * sizeof(float);   // 32 KiB
-static_assert(MD_SLOT_ROWS / MD_WARPS == 4, "a warp computes 4 rows of a slot at once, 8 lanes per row");
+static_assert(MD_SLOT_ROWS / MD_WARPS == 4, "a warp holds 4 rows of each slot, 16 lanes per row");
 
 struct MultiArgs {
     const float *conv_w, *A_log, *dt_bias, *norm_w;
