@@ -41,7 +41,7 @@ def rows(M, seed):
     return torch.randn(M, I.D_INNER, generator=g).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("M", [1, 100, 128, 129, 300, 1000])
+@pytest.mark.parametrize("M", [1, 100, 128, 129, 256, 300, 1000])
 def test_out_proj_matches_oracle(ops, weight, M):
     # one tile row, partial tiles, exact multiples and several tile rows
     x = rows(M, 900 + M)
