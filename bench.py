@@ -80,7 +80,7 @@ def load_peaks():
         with open(p) as f:
             d = json.load(f)
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
-    except Exception:
+    except (OSError, ValueError, KeyError, TypeError):     # absent or malformed: the recipe's fallback
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
@@ -102,7 +102,7 @@ class ClockSampler:
                                           "-lms", "200", "-i", str(self.idx)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
-        except Exception:
+        except OSError:                                    # no nvidia-smi: no clock record
             self.proc = None
 
     def _read(self):
@@ -117,7 +117,7 @@ class ClockSampler:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
-            except Exception:
+            except subprocess.TimeoutExpired:
                 self.proc.kill()
         rows = []
         for ts, line in self.lines:
@@ -567,7 +567,7 @@ def oracle_decode_sample(n_seq: int, threads: int):
 def host_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
-    except Exception:
+    except (AttributeError, OSError):                      # no affinity call on this platform
         return os.cpu_count() or 1
 
 
