@@ -634,9 +634,18 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
 
     // ---- H. U -> blob as [t][j] fp32; W -> blob as bf16 K-major [t][i]. Warp w
     //      reads token columns [16 (w / 4), +16) of its lane quarter w % 4.
+    //      Its W values fill two runs of 512 bytes of the K-major layout (rows
+    //      t >> 3 = 2 hf, 2 hf + 1; columns [32 q, 32 q + 32)), so the warp stages
+    //      them in shared memory (the v^T tile, which the U products have read)
+    //      and copies its own runs out in 16-byte stores. In the staging copy the
+    //      16-byte units of a run are XOR-swizzled (row t & 7 ^ 2 g for column
+    //      group g), which puts the lanes' 2-byte stores for one token in four
+    //      different bank groups.
     {
         const int q = warp & 3, hf = warp >> 2;
         const int j = 32 * q + lane;
+        unsigned char *wst = sm + S1_VT0;                // 16 KiB per head
+        auto wst_unit = [](int r8, int g) { return g * 8 + (r8 ^ (2 * g)); };   // staged unit of (t & 7, g)
         for (int h = 0; h < 2; ++h) {
             float u[16], wv[16];
             tc::tmem_ld16(tc::tmem_addr(tm, 32 * q, T1_U + 64 * h + 16 * hf), u);
@@ -648,9 +657,22 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
                 for (int e = 0; e < 16; ++e) {
                     const int t = 16 * hf + e;
                     U[t * DV + j] = u[e];
-                    *reinterpret_cast<bf16 *>(blob(h) + BLOB_W + km<2>(t, j, DK)) = from_f<bf16>(wv[e]);
+                    *reinterpret_cast<bf16 *>(wst + h * 16384 + (t >> 3) * 2048 + q * 512 +
+                                              wst_unit(t & 7, (j >> 3) & 3) * 16 + (j & 7) * 2) = from_f<bf16>(wv[e]);
                 }
             }
+        }
+        __syncwarp();
+        if (!ss.abort) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {            // run r (row block 2 hf + r), unit lane of 32
+                    const uint32_t run = (uint32_t)((2 * hf + r) * 2048 + q * 512);
+                    const int g = lane >> 3, r8 = lane & 7;
+                    *reinterpret_cast<uint4 *>(blob(h) + BLOB_W + run + lane * 16) =
+                        *reinterpret_cast<const uint4 *>(wst + h * 16384 + run + wst_unit(r8, g) * 16);
+                }
         }
     }
     tc::fence_before_sync();
