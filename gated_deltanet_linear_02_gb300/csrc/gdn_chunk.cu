@@ -283,25 +283,25 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     const unsigned char *raw = sm + S1_RAW;
     // Each pass loads the inputs of four iterations before it stores anything,
     // so the loads of later iterations need not wait behind earlier stores.
+    static_assert(NW1 == 16, "a pass's four iterations it0 + 16 k share the tile (it >> 6) and k-group (it & 7)");
+#pragma unroll 1
     for (int it0 = warp; it0 < 128; it0 += 4 * NW1) {                // q, k: (tile, row octet, k-group)
+        const int tile = it0 >> 6, kgh = it0 & 7;
+        const int d = 4 * (kgh * 4 + (lane >> 3));                    // 4 consecutive channels d..d+3
+        float4 w4[4];                                                 // their taps, the same for the whole pass
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w4[e] = reinterpret_cast<const float4 *>(sm + S1_CW + tile * 2048)[d + e];
         uint2 pr[4][4];
-        float4 w4[4][4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int it = it0 + k * NW1, tile = it >> 6, po = (it >> 3) & 7, kgh = it & 7;
-            const int p = po * 8 + (lane & 7);
-            const int d = 4 * (kgh * 4 + (lane >> 3));                // 4 consecutive channels d..d+3
+            const int p = (((it0 + k * NW1) >> 3) & 7) * 8 + (lane & 7);
 #pragma unroll
             for (int m = 0; m < 4; ++m)                               // positions p-3+m = rows p+m
                 pr[k][m] = *reinterpret_cast<const uint2 *>(raw + tile * RAW_SEG + (p + m) * RAW_ROWB + d * 2);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) w4[k][e] = reinterpret_cast<const float4 *>(sm + S1_CW + tile * 2048)[d + e];
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int it = it0 + k * NW1, tile = it >> 6, po = (it >> 3) & 7, kgh = it & 7;
-            const int p = po * 8 + (lane & 7);
-            const int d = 4 * (kgh * 4 + (lane >> 3));
+            const int p = (((it0 + k * NW1) >> 3) & 7) * 8 + (lane & 7);
             float x[4][4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
             float o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float4 w = w4[k][e];
+                const float4 w = w4[e];
                 const float u = w.x * x[0][e] + w.y * x[1][e] + w.z * x[2][e] + w.w * x[3][e];
                 o[e] = p < nv ? silu_fast(u) : 0.0f;
             }
