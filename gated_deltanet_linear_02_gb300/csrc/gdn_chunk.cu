@@ -375,35 +375,48 @@ __global__ void __launch_bounds__(P1_THREADS, 1) chunk_prep_kernel(const __grid_
     }
     // The value stream's conv runs while the tensor core computes K K^T and Q K^T:
     // v^T of both heads goes straight into its tiles.
-    for (int it0 = warp; it0 < 128; it0 += 4 * NW1) {                // v^T: (head, row octet of j, token group)
-        bf16 xr[4][7];
-        float4 w4[4];
+    // Iteration it = (V-head hv, half of the channels, block of 8 tokens): lane
+    // (group g = lane >> 3, pair c = lane & 7) convolves channels d, d + 1
+    // (d = 64 half + 16 g + 2 c) over tokens p0 .. p0 + 7, from 4-byte loads of
+    // 11 staged rows; a warp's load covers 128 contiguous bytes of one row. For
+    // the stores, lanes c >= 4 write their odd channel first, so that each
+    // quarter-warp's 16-byte stores fill rows 0..7 of two core matrices.
+    static_assert(CH == 64 && DV == 128, "v^T tiling of the conv");
+#pragma unroll 1
+    for (int it = warp; it < 32; it += NW1) {
+        const int hv = it >> 4, half = (it >> 3) & 1, p0 = 8 * (it & 7);
+        const int c = lane & 7, d = 64 * half + 16 * (lane >> 3) + 2 * c;
+        const float4 *cw = reinterpret_cast<const float4 *>(sm + S1_CW + (2 + hv) * 2048);
+        const float4 wa = cw[d], wb = cw[d + 1];
+        uint32_t xr[11];                                              // positions p0-3 .. p0+7, channels d, d+1
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int it = it0 + k * NW1, hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
-            const int d = dob * 8 + (lane & 7);
-            const int p0 = 4 * (pgh * 4 + (lane >> 3));              // tokens p0..p0+3
-            w4[k] = reinterpret_cast<const float4 *>(sm + S1_CW + (2 + hv) * 2048)[d];
+        for (int m = 0; m < 11; ++m)
+            xr[m] = *reinterpret_cast<const uint32_t *>(raw + (2 + hv) * RAW_SEG + (p0 + m) * RAW_ROWB + d * 2);
+        float oa[8], ob[8];
 #pragma unroll
-            for (int m = 0; m < 7; ++m)                               // positions p0-3 .. p0+3
-                xr[k][m] = *reinterpret_cast<const bf16 *>(raw + (2 + hv) * RAW_SEG + (p0 + m) * RAW_ROWB + d * 2);
-        }
+        for (int e = 0; e < 8; ++e) {
+            float xa[4], xb[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int it = it0 + k * NW1, hv = it >> 6, dob = (it >> 2) & 15, pgh = it & 3;
-            const int d = dob * 8 + (lane & 7);
-            const int p0 = 4 * (pgh * 4 + (lane >> 3));
-            const float4 w = w4[k];
-            float x[7];
-#pragma unroll
-            for (int m = 0; m < 7; ++m) x[m] = to_f(xr[k][m]);
-            float o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float u = w.x * x[e] + w.y * x[e + 1] + w.z * x[e + 2] + w.w * x[e + 3];
-                o[e] = (p0 + e) < nv ? tc::tf32_rn(silu_fast(u)) : 0.0f;
+            for (int m = 0; m < 4; ++m) {
+                xa[m] = __uint_as_float(xr[e + m] << 16);             // channel d: the low half
+                xb[m] = __uint_as_float(xr[e + m] & 0xFFFF0000u);     // channel d + 1
             }
-            *reinterpret_cast<float4 *>(sm + (hv ? S1_VT1 : S1_VT0) + km<4>(d, p0, CH)) = make_float4(o[0], o[1], o[2], o[3]);
+            const float ua = wa.x * xa[0] + wa.y * xa[1] + wa.z * xa[2] + wa.w * xa[3];
+            const float ub = wb.x * xb[0] + wb.y * xb[1] + wb.z * xb[2] + wb.w * xb[3];
+            const bool ok = (p0 + e) < nv;
+            oa[e] = ok ? tc::tf32_rn(silu_fast(ua)) : 0.0f;
+            ob[e] = ok ? tc::tf32_rn(silu_fast(ub)) : 0.0f;
+        }
+        unsigned char *vt = sm + (hv ? S1_VT1 : S1_VT0);
+        const bool odd_first = c >= 4;
+#pragma unroll
+        for (int sidx = 0; sidx < 2; ++sidx) {
+            const bool odd = odd_first != (sidx == 1);
+            const float *o = odd ? ob : oa;
+#pragma unroll
+            for (int tq = 0; tq < 2; ++tq)
+                *reinterpret_cast<float4 *>(vt + km<4>(d + (odd ? 1 : 0), p0 + 4 * tq, CH)) =
+                    make_float4(o[4 * tq], o[4 * tq + 1], o[4 * tq + 2], o[4 * tq + 3]);
         }
     }
     __syncthreads();                                   // every read of the staged rows is done
