@@ -65,7 +65,7 @@ extern "C" {
 typedef enum {
     GDN_OK = 0,
     GDN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad enum     */
-    GDN_ERR_UNSUPPORTED = 2,   /* well-formed request this build does not serve   */
+    GDN_ERR_UNSUPPORTED = 2,   /* well-formed request the library does not serve  */
     GDN_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required      */
     GDN_ERR_CUDA = 4,          /* the CUDA runtime rejected a launch              */
     GDN_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up              */
