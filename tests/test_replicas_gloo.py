@@ -32,7 +32,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks_take_the_slowest_time():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:       # no fork from this multi-threaded process
         out = m.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
