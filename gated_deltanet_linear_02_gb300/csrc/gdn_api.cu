@@ -4,18 +4,20 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "gdn_common.cuh"
 
 namespace gdn {
-cudaError_t take_decode_error(unsigned int *word, cudaStream_t s);
+void *decode_error_word();
 cudaError_t launch_conv_step(const float *, const void *, void *, void *, int, gdn_dtype, cudaStream_t);
 cudaError_t launch_decode_step(const gdn_params *, const void *, const void *, const void *, const void *,
                                void *, float *, void *, int, gdn_dtype, gdn_dtype, cudaStream_t);
 cudaError_t launch_decode_multi(const gdn_params *, const void *, const void *, const void *, const void *,
                                 void *, float *, void *, int, int, gdn_dtype, gdn_dtype, cudaStream_t);
-cudaError_t take_multi_error(unsigned int *word, cudaStream_t s);
+void *multi_error_word();
 cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s);
-cudaError_t take_gemm_error(unsigned int *word, cudaStream_t s);
+void *gemm_error_word();
 cudaError_t launch_in_proj(const void *h, const void *w_in, void *qkv, void *z, void *alpha, void *beta, int M,
                            gdn_dtype act, cudaStream_t s);
 size_t scan_workspace_bytes(int T_total);
@@ -23,17 +25,18 @@ cudaError_t launch_prefill_scan(const gdn_params *, const void *, const void *, 
                                 const int32_t *, int, int, const void *, void *, const float *, float *,
                                 void *, gdn_dtype, gdn_dtype, void *, cudaStream_t);
 size_t chunk_workspace_bytes(int N, int T_total);
+size_t chunk_min_workspace_bytes(int N);
 cudaError_t launch_prefill_chunked(const gdn_params *, const void *, const void *, const void *, const void *,
                                    const int32_t *, int, int, const void *, void *, const float *, float *, void *,
-                                   gdn_dtype, void *, cudaStream_t);
-cudaError_t take_chunk_error(unsigned int *word, cudaStream_t s);
+                                   gdn_dtype, void *, size_t, cudaStream_t);
+void *chunk_error_word();
 size_t attn_workspace_bytes(int B, int Lmax);
 cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
                                const void *z, void *out, int B, int Lmax, void *ws, gdn_dtype out_dt,
                                cudaStream_t s);
-cudaError_t take_attn_error(unsigned int *word, cudaStream_t s);
+void *attn_error_word();
 cudaError_t launch_wait_timeout(cudaStream_t s);
-cudaError_t take_selftest_error(unsigned int *word, cudaStream_t s);
+void *selftest_error_word();
 }  // namespace gdn
 
 using namespace gdn;
@@ -85,6 +88,51 @@ int resolve_chunk(int chunk_size, gdn_dtype act)
 }  // namespace
 
 namespace gdn {
+
+// Every kernel file keeps its own device error word. gdn_device_error reads and
+// clears all of them with one small kernel (an atomic exchange each, so a word
+// set while the call runs is either reported now or kept for the next call)
+// and one copy of the OR back to the host.
+constexpr int N_ERROR_WORDS = 6;
+struct ErrorWords {
+    unsigned int *p[N_ERROR_WORDS];
+};
+__device__ unsigned int g_error_any;
+
+__global__ void error_gather_kernel(const ErrorWords w)
+{
+    if (threadIdx.x != 0) return;
+    unsigned int v = 0;
+#pragma unroll
+    for (int i = 0; i < N_ERROR_WORDS; ++i)
+        if (w.p[i]) v |= atomicExch(w.p[i], 0u);
+    g_error_any = v;
+}
+
+// The words' device addresses, looked up once per device with that device
+// current (a host-side symbol is not a device address).
+static bool error_words(ErrorWords *out)
+{
+    constexpr int MAX_DEV = 64;
+    static std::mutex mu;
+    static ErrorWords cache[MAX_DEV];
+    static bool have[MAX_DEV] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        void *(*const fns[N_ERROR_WORDS])() = {decode_error_word, chunk_error_word, multi_error_word,
+                                               gemm_error_word,   attn_error_word,  selftest_error_word};
+        for (int i = 0; i < N_ERROR_WORDS; ++i) {
+            cache[dev].p[i] = static_cast<unsigned int *>(fns[i]());
+            if (cache[dev].p[i] == nullptr) return false;
+        }
+        have[dev] = true;
+    }
+    *out = cache[dev];
+    return true;
+}
+
 // Lets other translation units of the library set the gdn_last_error() text.
 void record_error(const char *msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
 }  // namespace gdn
@@ -242,9 +290,16 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
     if (!ok_opt_ptr(conv_state_in) || !ok_opt_ptr(conv_state_out) || !ok_opt_ptr(ssm_state_in) ||
         !ok_opt_ptr(ssm_state_out))
         return fail(GDN_ERR_INVALID_ARG, "a state pointer is not 16-byte aligned");
-    const size_t need = gdn_prefill_workspace_size(N, T_total, act, ch);
-    if (workspace == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return fail(GDN_ERR_WORKSPACE, "workspace missing, misaligned (256 B) or too small");
+    // The exact scan needs its whole workspace. The chunked form runs in windows
+    // of the packed tokens sized to the workspace it is given, so any workspace
+    // that holds one 64-token window will do.
+    const size_t need = ch == 1 ? gdn_prefill_workspace_size(N, T_total, act, ch)
+                                : WS_HEADER + ((chunk_min_workspace_bytes(N) + 255) & ~(size_t)255);
+    if (workspace == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+        snprintf(g_last_error, sizeof(g_last_error),
+                 "workspace missing, misaligned (256 B) or too small: %zu bytes given, %zu needed", ws_bytes, need);
+        return GDN_ERR_WORKSPACE;
+    }
     void *body = static_cast<char *>(workspace) + WS_HEADER;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
@@ -253,27 +308,23 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
                                 ssm_state_in, ssm_state_out, out, act, out_dt, body, s);
     else
         e = launch_prefill_chunked(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
-                                   ssm_state_in, ssm_state_out, out, out_dt, body, s);
+                                   ssm_state_in, ssm_state_out, out, out_dt, body, ws_bytes - WS_HEADER, s);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_prefill");
 }
 
 gdn_status gdn_device_error(void *stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
-    unsigned int word = 0;
-    unsigned int word2 = 0;
-    unsigned int word3 = 0;
-    unsigned int word4 = 0;
-    unsigned int word5 = 0;
-    unsigned int word6 = 0;
-    cudaError_t e = take_decode_error(&word, s);
-    if (e == cudaSuccess) e = take_chunk_error(&word2, s);
-    if (e == cudaSuccess) e = take_multi_error(&word3, s);
-    if (e == cudaSuccess) e = take_gemm_error(&word4, s);
-    if (e == cudaSuccess) e = take_attn_error(&word5, s);
-    if (e == cudaSuccess) e = take_selftest_error(&word6, s);
+    ErrorWords w;
+    if (!error_words(&w)) return cuda_fail(cudaGetLastError(), "gdn_device_error: error word lookup");
+    unsigned int any = 0;
+    error_gather_kernel<<<1, 32, 0, s>>>(w);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&any, g_error_any, sizeof(unsigned int), 0,
+                                                        cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "gdn_device_error");
-    return (word | word2 | word3 | word4 | word5 | word6) == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
+    return any == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
 }
 
 gdn_status gdn_selftest_wait_timeout(void *stream)

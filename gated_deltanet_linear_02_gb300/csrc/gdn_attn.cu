@@ -563,15 +563,12 @@ cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v
 }
 
 // Reads and clears this file's device error word (synchronous on `s`).
-cudaError_t take_attn_error(unsigned int *word, cudaStream_t s)
+// Device address of this file's error word, for gdn_device_error, which reads
+// and clears every word of the library in one kernel (NULL if the lookup fails).
+void *attn_error_word()
 {
-    unsigned int zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_attn_error, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e == cudaSuccess && *word != 0)
-        e = cudaMemcpyToSymbolAsync(g_attn_error, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    return e;
+    void *p = nullptr;
+    return cudaGetSymbolAddress(&p, g_attn_error) == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace gdn

@@ -477,15 +477,12 @@ cudaError_t launch_decode_multi(const gdn_params *p, const void *qkv, const void
 }
 
 // Reads and clears this file's device error word (synchronous on `s`).
-cudaError_t take_multi_error(unsigned int *word, cudaStream_t s)
+// Device address of this file's error word, for gdn_device_error, which reads
+// and clears every word of the library in one kernel (NULL if the lookup fails).
+void *multi_error_word()
 {
-    unsigned int zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_multi_error, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e == cudaSuccess && *word != 0)
-        e = cudaMemcpyToSymbolAsync(g_multi_error, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    return e;
+    void *p = nullptr;
+    return cudaGetSymbolAddress(&p, g_multi_error) == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace gdn

@@ -40,22 +40,23 @@ extern "C" gdn_status gdn_prefill_static(const gdn_params *p, const void *qkv, c
                                          gdn_dtype act, gdn_dtype out_dt, int chunk_size, void *stream)
 {
     const size_t need = gdn_prefill_workspace_size(N, T_total, act, chunk_size);
-    if (N == 0 || need == 0)   // nothing to run, or invalid sizes: gdn_prefill reports it without touching CUDA
+    // Nothing to run, or arguments gdn_prefill rejects on their own: it reports
+    // them (with the same status and message as a direct call) without touching
+    // CUDA. So does a call with a null or misaligned pointer, which gdn_prefill
+    // checks before it looks at the workspace below.
+    if (N == 0 || need == 0)
         return gdn_prefill(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
                            ssm_state_in, ssm_state_out, out, act, out_dt, chunk_size, nullptr, 0, stream);
-    if (need > (size_t)GDN_STATIC_SCRATCH_BYTES) {
-        char msg[256];
-        snprintf(msg, sizeof(msg),
-                 "gdn_prefill_static: this call needs %zu bytes of scratch but the static scratch holds %zu; "
-                 "use gdn_prefill with a caller-provided workspace",
-                 need, (size_t)GDN_STATIC_SCRATCH_BYTES);
-        gdn::record_error(msg);
-        return GDN_ERR_WORKSPACE;
-    }
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return GDN_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        gdn::record_error("gdn_prefill_static: no current CUDA device");
+        return GDN_ERR_CUDA;
+    }
     void *scratch = nullptr;
     {
+        // The address is looked up once per device and kept for the life of the
+        // process. It assumes the device's primary context is never reset
+        // (cudaDeviceReset): after a reset the array has a new address.
         std::lock_guard<std::mutex> lock(g_mu);
         if (g_scratch_dev[dev] == nullptr) {
             void *ptr = nullptr;
@@ -70,8 +71,10 @@ extern "C" gdn_status gdn_prefill_static(const gdn_params *p, const void *qkv, c
         }
         scratch = g_scratch_dev[dev];
     }
-    // The kernels write every scratch byte they later read, so stale contents
-    // from the previous call need no clearing.
+    // gdn_prefill validates every argument first, then the scratch size: the
+    // chunked form runs in windows sized to the scratch, the exact scan needs
+    // room for all of its tokens. The kernels write every scratch byte they
+    // later read, so stale contents from the previous call need no clearing.
     return gdn_prefill(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out, ssm_state_in,
                        ssm_state_out, out, act, out_dt, chunk_size, scratch, (size_t)GDN_STATIC_SCRATCH_BYTES,
                        stream);

@@ -158,10 +158,19 @@ gdn_status gdn_decode_multi(const gdn_params *p, const void *qkv, const void *z,
  *                   be GDN_BF16). The chunked form is an exact re-association
  *                   of the same recurrence; the two differ only by rounding.
  *                   Library choice: GDN_F32 -> 1, GDN_BF16 -> 64.
- *   workspace       DEVICE scratch of at least gdn_prefill_workspace_size(...)
- *                   bytes, 256-byte aligned; contents need no initialisation
- *                   and are clobbered. Calls that share a workspace must be
- *                   ordered on one stream.
+ *   workspace       DEVICE scratch, 256-byte aligned; contents need no
+ *                   initialisation and are clobbered. Calls that share a
+ *                   workspace must be ordered on one stream. Size:
+ *                   - chunk_size 1: at least gdn_prefill_workspace_size(...).
+ *                   - chunk_size 64: the packed tokens run in windows sized
+ *                     to the workspace given, with the state carried from
+ *                     window to window, so the scratch does not grow with the
+ *                     prompt. gdn_prefill_workspace_size(...) is the size for
+ *                     one window of up to 4096 tokens (the same for any
+ *                     T_total >= 4096); any size down to
+ *                     gdn_prefill_workspace_size(N, 64, act, 64) (one 64-token
+ *                     window) is accepted, and a larger one gives longer
+ *                     windows.
  * 0 <= N <= 65535, 0 <= T_total <= 2^24. cu_seqlens is read on the device only;
  * a cu_seqlens that breaks the rules above gives unspecified results for the
  * offending sequences but never touches memory outside the stated extents.
@@ -189,15 +198,18 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
  *
  * Scratch: a file-scope device array of GDN_STATIC_SCRATCH_BYTES (64 MiB) in
  * libgdn. Every GPU that loads the library holds it until the process exits.
- * A call whose gdn_prefill_workspace_size(N, T_total, act, chunk_size) exceeds
- * it returns GDN_ERR_WORKSPACE without launching anything, and gdn_last_error()
- * states the size it would need. As a guide, one bf16 sequence of up to 895
- * tokens fits with the chunked form, and up to about 1,300 tokens with the
- * exact scan.
+ * The chunked form (bf16) runs in windows that fit the array, about 1,600
+ * tokens each for one sequence, so a prompt of any length fits; only a call
+ * with so many sequences that one 64-token window does not fit is refused.
+ * The exact scan needs room for all of its tokens: up to about 1,300 tokens
+ * per call. A call that does not fit returns GDN_ERR_WORKSPACE without
+ * launching anything, after the same argument checks as gdn_prefill.
  *
  * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it. Make that
- * first call before any stream capture on the device.
+ * (cudaGetSymbolAddress, with that device current) and caches it for the life
+ * of the process, so the device's primary context must not be reset
+ * (cudaDeviceReset) afterwards. Make that first call before any stream
+ * capture on the device.
  *
  * Sharing: every call on a device uses the same scratch, and the scratch keeps
  * the previous call's contents (the kernels need none of it cleared). Calls

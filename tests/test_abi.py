@@ -72,6 +72,23 @@ def test_workspace_size_arithmetic(ops):
     assert L.gdn_prefill_workspace_size(70000, 10, ops.GDN_F32, 1) == 0
 
 
+def test_chunked_workspace_is_bounded(ops):
+    """The chunked form runs the packed tokens in windows, so its default
+    workspace stops growing with the prompt: one sequence of 4096 tokens, of
+    32768 tokens and of 2^24 tokens all get the size of one 4096-token window.
+    Shorter prompts get less, and the size grows with N only through the
+    per-sequence tables (at most one 4096-token window's worth of sequences)."""
+    L = ops.lib()
+    a = L.gdn_prefill_workspace_size(1, 4096, ops.GDN_BF16, 64)
+    assert a == L.gdn_prefill_workspace_size(1, 32768, ops.GDN_BF16, 64)
+    assert a == L.gdn_prefill_workspace_size(1, 1 << 24, ops.GDN_BF16, 64)
+    assert L.gdn_prefill_workspace_size(1, 64, ops.GDN_BF16, 64) < L.gdn_prefill_workspace_size(1, 1000, ops.GDN_BF16, 64) < a
+    assert L.gdn_prefill_workspace_size(8, 70264, ops.GDN_BF16, 64) == L.gdn_prefill_workspace_size(8, 4096, ops.GDN_BF16, 64)
+    assert L.gdn_prefill_workspace_size(65535, 1 << 20, ops.GDN_BF16, 64) == \
+        L.gdn_prefill_workspace_size(4096, 1 << 20, ops.GDN_BF16, 64)
+    assert a < 160 << 20
+
+
 FAKE = 0x10000          # 16-byte aligned, never dereferenced: every case fails a host check first
 MIS = 0x10004           # misaligned
 

@@ -21,7 +21,7 @@ def ops():
     return ops
 
 
-def gpu_prefill(ops, lp, st, lengths, conv0, S0, out_dtype, chunk, pass_states=True, alias=False):
+def gpu_prefill(ops, lp, st, lengths, conv0, S0, out_dtype, chunk, pass_states=True, alias=False, ws_tokens=None):
     cu = I.cu_seqlens(lengths).to(DEV)
     N, T = len(lengths), int(sum(lengths))
     s = st.to(DEV)
@@ -33,8 +33,11 @@ def gpu_prefill(ops, lp, st, lengths, conv0, S0, out_dtype, chunk, pass_states=T
     else:
         cout = torch.full((N, I.KCONV - 1, I.C_CONV), float("nan"), dtype=st.qkv.dtype, device=DEV)
         sout = torch.full((N, I.HV, I.DV, I.DK), float("nan"), dtype=torch.float32, device=DEV)
+    ws = None
+    if ws_tokens is not None:   # a workspace sized for windows of ws_tokens tokens
+        ws = torch.empty(ops.prefill_workspace_size(N, ws_tokens, st.qkv.dtype, chunk), dtype=torch.uint8, device=DEV)
     ws = ops.prefill(lp.to(DEV), s.qkv, s.z, s.alpha, s.beta, cu, out, conv_state_in=cin, conv_state_out=cout,
-                     ssm_state_in=sin, ssm_state_out=sout, chunk_size=chunk)
+                     ssm_state_in=sin, ssm_state_out=sout, chunk_size=chunk, workspace=ws)
     assert ops.device_error() == ops.GDN_OK
     return out.cpu(), cout.cpu(), sout.cpu()
 
@@ -210,3 +213,17 @@ def test_prefill_bitwise_repeatable(ops):
     b = gpu_prefill(ops, lp, st, lengths, conv0, S0, torch.bfloat16, 64)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("ws_tokens,alias", [(64, False), (128, True), (192, False)])
+def test_prefill_windows_small_workspace(ops, ws_tokens, alias):
+    """The chunked form given a workspace for windows of 64, 128 or 192 tokens:
+    the packed tokens run as many windows, sequences cross window edges with
+    their state carried between windows, and the result still matches the
+    oracle (also with the states updated in place)."""
+    lengths = [300, 77, 1, 0, 200, 64, 130]
+    lp, st, conv0, S0 = varlen_case(905, lengths, torch.bfloat16)
+    got = gpu_prefill(ops, lp, st, lengths, conv0, S0, torch.float32, chunk=64, alias=alias, ws_tokens=ws_tokens)
+    ref = oracle_varlen(lp, st, lengths, conv0, S0)
+    check(f"windows of {ws_tokens}", got, ref, torch.bfloat16, torch.float32)
+

@@ -9,8 +9,10 @@ library's fixed 64 MiB device scratch instead.
 These tests call it through the C ABI and check that it gives the same results
 as gdn_prefill with a caller-provided workspace, within the parity tolerances
 of the other tests, on two calls in a row. The second call runs on the first
-call's leftover scratch contents. The tests also check that an oversized
-request is refused with a clear error, and that a call allocates nothing.
+call's leftover scratch contents. The tests also check that a prompt too long
+for one window of the scratch runs in several windows, that a request the
+scratch cannot hold is refused with a clear error after the argument checks,
+and that a call allocates nothing.
 
 The file is named so that pytest collects it last.
 """
@@ -89,15 +91,42 @@ def test_static_allocates_nothing(ops):
     assert torch.isfinite(out).all()
 
 
-def test_static_refuses_oversized_request(ops):
-    # one bf16 sequence of 4096 tokens needs about 239 MB of scratch with the chunked form
-    need = ops.prefill_workspace_size(1, 4096, torch.bfloat16, 0)
-    assert need > ops.STATIC_SCRATCH_BYTES
+def test_static_long_prompt_runs_in_windows(ops):
+    # One bf16 sequence of 4096 tokens does not fit the 64 MiB scratch in one
+    # window; the chunked form runs it as several windows with the state
+    # carried, and gives what gdn_prefill gives with a full-size workspace.
+    full = ops.prefill_workspace_size(1, 4096, torch.bfloat16, 0)
+    assert full > ops.STATIC_SCRATCH_BYTES
     lp, st, cu, conv0, S0 = _case(4104, [4096], torch.bfloat16)
-    out, cs, S = _outputs(4096, 1, torch.bfloat16)
+    ref = _run(ops, ops.prefill, lp, st, cu, conv0, S0, 0)
+    got = _run(ops, ops.prefill_static, lp, st, cu, conv0, S0, 0)
+    torch.cuda.synchronize()
+    _compare(ref, got, torch.bfloat16)
+
+
+def test_static_refuses_oversized_request(ops):
+    # the exact scan keeps all of its tokens in scratch: 4096 fp32 tokens need
+    # about 200 MB, more than the static scratch holds
+    need = ops.prefill_workspace_size(1, 4096, torch.float32, 1)
+    assert need > ops.STATIC_SCRATCH_BYTES
+    lp, st, cu, conv0, S0 = _case(4105, [4096], torch.float32)
+    out, cs, S = _outputs(4096, 1, torch.float32)
     with pytest.raises(ops.GdnError) as err:
-        ops.prefill_static(lp, st.qkv, st.z, st.alpha, st.beta, cu, out, ssm_state_out=S)
+        ops.prefill_static(lp, st.qkv, st.z, st.alpha, st.beta, cu, out, ssm_state_out=S, chunk_size=1)
     assert err.value.status == ops.GDN_ERR_WORKSPACE
-    assert "static scratch" in str(err.value) and str(need) in str(err.value)
+    assert str(need) in str(err.value)
     torch.cuda.synchronize()
     assert torch.isnan(out).all()           # nothing was launched
+
+
+def test_static_checks_arguments_before_scratch_size(ops):
+    # A request that would not fit AND has a null tensor pointer reports the
+    # invalid argument, as gdn_prefill does, not the scratch size.
+    import ctypes
+    lp, st, cu, conv0, S0 = _case(4106, [4096], torch.float32)
+    out, cs, S = _outputs(4096, 1, torch.float32)
+    cp = ops.make_params(lp)
+    rc = ops.lib().gdn_prefill_static(ctypes.byref(cp), None, st.z.data_ptr(), st.alpha.data_ptr(),
+                                      st.beta.data_ptr(), cu.data_ptr(), 1, 4096, None, None, None,
+                                      S.data_ptr(), out.data_ptr(), ops.GDN_F32, ops.GDN_F32, 1, None)
+    assert rc == ops.GDN_ERR_INVALID_ARG
