@@ -72,7 +72,7 @@ struct WyCount {
     int n_frag, n_chunks;
 };
 
-// Per (chunk, V-head) operand blob, 73 KiB. The tiles are stored exactly as
+// Per (chunk, V-head) operand blob, 72 KiB. The tiles are stored exactly as
 // the carry kernel's shared-memory operands, so one bulk copy moves the blob.
 constexpr uint32_t BL_WT = 0;          // W^T, fp16, MN-major (N = token t, K = key i),       16 KiB
 constexpr uint32_t BL_UT = 16384;      // U^T, fp16, same layout (t, value j),                 16 KiB
@@ -80,9 +80,13 @@ constexpr uint32_t BL_P = 32768;       // P = Mask o Q K^T, fp16 K-major [t][s] 
 constexpr uint32_t BL_KT = 40960;      // K~ = diag(exp(G_n - G_t)) k^, fp16, two 64-column boxes
                                        // [t][i] in the 128-byte swizzle (as TMA writes x^)  16 KiB
 constexpr uint32_t BL_QT = 57344;      // Q~ = diag(gamma_t) q^, fp16, same layout             16 KiB
-constexpr uint32_t BL_GN = 73728;      // gamma_n = exp(G_n), fp32
-constexpr uint32_t BLOB_BYTES = 74752;
+constexpr uint32_t BLOB_BYTES = 73728;
 static_assert(BLOB_BYTES % 1024 == 0, "blobs stay 1 KiB aligned");
+
+// Gate record of one (chunk, V-head), fp32: the chunk-local cumulative
+// log-decay G_t, beta_t, gamma_t = exp(G_t), and exp(G_n - G_t) (0 past the
+// chunk's tokens); gamma_n = exp(G_n) is gamma_63 (g is 0 past the tokens).
+constexpr int GR_G = 0, GR_B = CH, GR_GAM = 2 * CH, GR_KTF = 3 * CH, GATE_FLOATS = 4 * CH;
 
 // (t, c) of a [t][c] fp16 tile stored MN-major with t as the contiguous (N)
 // index and c as K: 8-token groups 2 KiB apart, 8-row c groups 128 B apart.
@@ -119,6 +123,7 @@ struct WyArgs {
     WyChunk *chunks;
     __half *xhat;                // [wlen][8192]
     __half *ybuf;                // [wlen][4096]: y (scale applied) before the gated norm
+    float *gates;                // [c_cap][32][4][64]: per (chunk, V-head) G, beta, gamma_t, exp(G_n - G_t)
     unsigned char *blobs;        // [c_cap][32] x BLOB_BYTES
     float *slot_in, *slot_out;   // [32][128][128]: the state of a sequence that crosses a window edge
 };
@@ -211,12 +216,50 @@ __global__ void __launch_bounds__(1024) wy_plan_kernel(const WyArgs a)
 constexpr int ACT_THREADS = 256;
 __global__ void __launch_bounds__(ACT_THREADS) wy_act_kernel(const WyArgs a)
 {
+    __shared__ float gs[2][2][CH];                     // g (then G) and beta of V-heads y, y + 16
     grid_dep_wait();
     grid_dep_launch();
     const int g = blockIdx.x;
     if (g >= a.count->n_chunks) return;
     const WyChunk ck = a.chunks[g];
     const int tid = threadIdx.x, lane = tid & 31, tg = tid >> 5;
+    if (blockIdx.y < HK) {
+        // the gates of V-heads y and y + 16 over this chunk (section "Decay gate"):
+        // g = -exp(A_log) softplus(alpha + dt_bias), beta = sigmoid(beta); tokens
+        // past the chunk get g = 0, beta = 0. Then G = the chunk-local prefix sum.
+        const int h = tid >> 6, p = tid & 63, vh = blockIdx.y + HK * h;
+        if (tid < 2 * CH) {
+            float gg = 0.0f, bb = 0.0f;
+            if (p < ck.nv) {
+                const size_t r = (size_t)(ck.row0 + p) * HV + vh;
+                gg = -expf(__ldg(a.A_log + vh)) * softplus_f(to_f(a.alpha[r]) + __ldg(a.dt_bias + vh));
+                bb = 1.0f / (1.0f + expf(-to_f(a.beta[r])));
+            }
+            gs[h][0][p] = gg;
+            gs[h][1][p] = bb;
+        }
+        __syncthreads();
+        if (tg < 2) {                                  // warp h: inclusive scan of head h's log-decays
+            const float g0 = gs[tg][0][2 * lane], g1 = gs[tg][0][2 * lane + 1];
+            float run = g0 + g1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float up = __shfl_up_sync(0xffffffffu, run, o);
+                if (lane >= o) run += up;
+            }
+            gs[tg][0][2 * lane] = run - g1;
+            gs[tg][0][2 * lane + 1] = run;
+        }
+        __syncthreads();
+        if (tid < 2 * CH) {
+            const float Gp = gs[h][0][p], Gn = gs[h][0][CH - 1];
+            float *rec = a.gates + ((size_t)g * HV + vh) * GATE_FLOATS;
+            rec[GR_G + p] = Gp;
+            rec[GR_B + p] = gs[h][1][p];
+            rec[GR_GAM + p] = expf(Gp);
+            rec[GR_KTF + p] = p < ck.nv ? __expf(Gn - Gp) : 0.0f;
+        }
+    }
     const int c0 = blockIdx.y * DK + 4 * lane;
     const int tb = 8 * tg;                             // first token (uniform over the warp)
     if (tb >= ck.nv) return;
@@ -286,11 +329,8 @@ constexpr uint32_t PR_M = 198656;      // per head: block products, fp32 [32][36
 constexpr int MLD = 36;
 constexpr uint32_t PR_SMALL = 207872;
 struct PrSmall {
-    float G[2][CH];                    // cumulative log-decay (chunk-local) per V-head
-    float B[2][CH];                    // beta
-    float gam[2][CH];                  // exp(G)
-    float ktf[2][CH];                  // exp(G_n - G_t), 0 past the chunk's tokens
-    uint64_t bar_x[2];                 // the x^ tiles, per buffer
+    float gr[2][2][GATE_FLOATS];       // gate records [buffer][V-head of the pair], loaded with the tiles
+    uint64_t bar_x[2];                 // the x^ tiles and gate records, per buffer
     uint64_t bar_qk, bar_uw;           // tensor-core completions
     uint32_t tmem;
     int abort;
@@ -332,7 +372,11 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
         const int kh = it % HK, y = ck.row0 - a.w0;
         const uint32_t xb = sb + (uint32_t)buf * PR_X_BYTES;
         const uint32_t bx = smem_u32(&ss.bar_x[buf]);
-        mbar_arrive_expect_tx(bx, PR_X_BYTES);
+        mbar_arrive_expect_tx(bx, PR_X_BYTES + 2 * GATE_FLOATS * 4);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            bulk_g2s(smem_u32(&ss.gr[buf][h][0]), a.gates + ((size_t)(it / HK) * HV + kh + HK * h) * GATE_FLOATS,
+                     GATE_FLOATS * 4, bx);
         tma_load_2d(xb + PR_Q0, &xmap, Q_OFF + kh * DK, y, bx);
         tma_load_2d(xb + PR_Q1, &xmap, Q_OFF + kh * DK + 64, y, bx);
         tma_load_2d(xb + PR_K0, &xmap, K_OFF + kh * DK, y, bx);
@@ -368,20 +412,6 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
     int pend_buf = -1;                                 // thread 0: buffer of a copy not yet waited for
     uint32_t pend_par = 0;
     if (tid == 0 && item < n_items) pend_buf = 0;
-    // threads < 128: (V-head, token) tid >> 6, tid & 63 of the item about to run:
-    // its gate logits and its head's parameters, loaded one item ahead
-    float al_next = 0.0f, be_next = 0.0f, A_h = 0.0f, dtb_h = 0.0f;
-    if (tid < 2 * CH && item < n_items) {
-        const WyChunk c0 = a.chunks[item / HK];
-        const int vh0 = item % HK + HK * (tid >> 6), p0 = tid & 63;
-        A_h = __ldg(a.A_log + vh0);
-        dtb_h = __ldg(a.dt_bias + vh0);
-        if (p0 < c0.nv) {
-            const size_t r = (size_t)(c0.row0 + p0) * HV + vh0;
-            al_next = to_f(a.alpha[r]);
-            be_next = to_f(a.beta[r]);
-        }
-    }
 
     for (; item < n_items; item += stride, ++n) {
         const int g = item / HK, kh = item % HK;
@@ -413,75 +443,12 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
                 pend_par = (uint32_t)(((n + 1) >> 1) & 1);
             }
         }
-        // ---- gates of both V-heads; tokens past the chunk get g = 0, beta = 0. The
-        //      logits were loaded during the previous item (al_next, be_next).
-        if (tid < 2 * CH) {
-            const int h = tid >> 6, p = tid & 63;
-            float gg = 0.0f, bb = 0.0f;
-            if (p < nv) {
-                gg = -expf(A_h) * softplus_f(al_next + dtb_h);
-                bb = 1.0f / (1.0f + expf(-be_next));
-            }
-            ss.G[h][p] = gg;
-            ss.B[h][p] = bb;
-            // the next item's logits, if any (same thread, same (head, token) slot)
-            const int nit = item + stride;
-            if (nit < n_items) {
-                const WyChunk cn = a.chunks[nit / HK];
-                const int vn = nit % HK + HK * h;
-                A_h = __ldg(a.A_log + vn);
-                dtb_h = __ldg(a.dt_bias + vn);
-                if (p < cn.nv) {
-                    const size_t r = (size_t)(cn.row0 + p) * HV + vn;
-                    al_next = to_f(a.alpha[r]);
-                    be_next = to_f(a.beta[r]);
-                }
-            }
-        }
-        __syncthreads();
-        if (warp < 2) {                                // warp h: inclusive scan of head h's log-decays
-            const float g0 = ss.G[warp][2 * lane], g1 = ss.G[warp][2 * lane + 1];
-            float run = g0 + g1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float up = __shfl_up_sync(0xffffffffu, run, o);
-                if (lane >= o) run += up;
-            }
-            ss.G[warp][2 * lane] = run - g1;
-            ss.G[warp][2 * lane + 1] = run;
-        }
-        __syncthreads();
-        if (tid < 2 * CH) {                            // decays: to shared memory and to both blobs
-            const int h = tid >> 6, p = tid & 63;
-            const float Gp = ss.G[h][p], Gn = ss.G[h][CH - 1];
-            const float gm = expf(Gp);
-            ss.gam[h][p] = gm;
-            ss.ktf[h][p] = p < nv ? __expf(Gn - Gp) : 0.0f;
-            if (p == CH - 1) *reinterpret_cast<float *>(blob(h) + BL_GN) = expf(Gn);
-        }
+        // the gate records of both V-heads (loaded with the tiles; thread 0 waited)
+        const float (*gr)[GATE_FLOATS] = ss.gr[buf];
+        auto Gof = [&](int h, int t) { return gr[h][GR_G + t]; };
         if (!mbar_wait_sleep(smem_u32(&ss.bar_qk), (uint32_t)(n & 1))) ss.abort = 1;
         tc::fence_after_sync();
-        __syncthreads();                               // gam, ktf visible to every thread
-        // K~ = diag(exp(G_n - G_t)) k^ and Q~ = diag(gamma_t) q^ of both heads to the
-        // blobs, in the swizzled layout of the x^ tiles (16-byte unit w of a box
-        // holds row w / 8)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int u = tid + PR_THREADS * e;        // 0..4095: q or k, head, box, 16-byte unit
-            const int isq = u >> 11, h = (u >> 10) & 1, b = (u >> 9) & 1, w = u & 511, t = w >> 3;
-            const uint32_t src = isq ? (b ? PR_Q1 : PR_Q0) : (b ? PR_K1 : PR_K0);
-            const uint4 kv = *reinterpret_cast<const uint4 *>(sm + (uint32_t)buf * PR_X_BYTES + src + 16 * w);
-            const float f = isq ? ss.gam[h][t] : ss.ktf[h][t];
-            const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 x2 = __half22float2(*reinterpret_cast<const __half2 *>(&kk[i]));
-                o[i] = tc::pack_half2(x2.x * f, x2.y * f);
-            }
-            *reinterpret_cast<uint4 *>(blob(h) + (isq ? BL_QT : BL_KT) + 8192 * b + 16 * w) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-
+        __syncthreads();                               // the records are visible to every thread
         // ---- P (rows 0-63 of the product) to the blobs; beta L (rows 64-127) to shared
         //      memory. Thread: one row, 16 columns [16 cq, 16 cq + 16), both heads.
         {
@@ -493,7 +460,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
             const int s0 = 16 * cq;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const float Gt = ss.G[h][t];
+                const float Gt = Gof(h, t);
                 if (q < 2) {
                     uint32_t wd[8];
 #pragma unroll
@@ -502,7 +469,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int s = s0 + 2 * e2 + e;
-                            pv[e] = (s <= t && t < nv) ? __expf(Gt - ss.G[h][s]) * qk[2 * e2 + e] : 0.0f;
+                            pv[e] = (s <= t && t < nv) ? __expf(Gt - Gof(h, s)) * qk[2 * e2 + e] : 0.0f;
                         }
                         wd[e2] = tc::pack_half2(pv[0], pv[1]);
                     }
@@ -510,7 +477,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
                     *reinterpret_cast<uint4 *>(P + km64(t, s0)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
                     *reinterpret_cast<uint4 *>(P + km64(t, s0 + 8)) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
                 } else {
-                    const float bt = ss.B[h][t];
+                    const float bt = gr[h][GR_B + t];
                     float *L = Lf(h);
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
@@ -518,7 +485,7 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int s = s0 + 4 * c4 + e;
-                            lv[e] = (s < t && t < nv) ? bt * __expf(Gt - ss.G[h][s]) * qk[4 * c4 + e] : 0.0f;
+                            lv[e] = (s < t && t < nv) ? bt * __expf(Gt - Gof(h, s)) * qk[4 * c4 + e] : 0.0f;
                         }
                         *reinterpret_cast<float4 *>(L + lb_at(t, s0 + 4 * c4)) = make_float4(lv[0], lv[1], lv[2], lv[3]);
                     }
@@ -552,6 +519,25 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) X[(16 * I + r) * XLD + 16 * I + c] = x[r];
+        } else {
+            // meanwhile: K~ = diag(exp(G_n - G_t)) k^ and Q~ = diag(gamma_t) q^ of both
+            // heads to the blobs, in the swizzled layout of the x^ tiles (16-byte
+            // unit w of a box holds row w / 8)
+            for (int u = tid - 128; u < 4096; u += PR_THREADS - 128) {
+                const int isq = u >> 11, h = (u >> 10) & 1, b = (u >> 9) & 1, w = u & 511, t = w >> 3;
+                const uint32_t src = isq ? (b ? PR_Q1 : PR_Q0) : (b ? PR_K1 : PR_K0);
+                const uint4 kv = *reinterpret_cast<const uint4 *>(sm + (uint32_t)buf * PR_X_BYTES + src + 16 * w);
+                const float fsc = gr[h][(isq ? GR_GAM : GR_KTF) + t];
+                const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 x2 = __half22float2(*reinterpret_cast<const __half2 *>(&kk[i]));
+                    o[i] = tc::pack_half2(x2.x * fsc, x2.y * fsc);
+                }
+                *reinterpret_cast<uint4 *>(blob(h) + (isq ? BL_QT : BL_KT) + 8192 * b + 16 * w) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            }
         }
         __syncthreads();
         {                                              // level 2a: M = A_BA X_AA for 16-row pairs
@@ -591,45 +577,59 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
             *reinterpret_cast<float2 *>(X + (rA + r) * XLD + rB + c) = make_float2(0.0f, 0.0f);
         }
         __syncthreads();
-        {                                              // level 3a: M = A_BA X_AA for the 32-row halves
-            const int h = tid >> 8, r = (tid >> 3) & 31, c = 4 * (tid & 7);
+        // level 3 (32-row halves) on 128 threads, each a 4 x 4 block of its head's
+        // 32 x 32 product: 8 vector loads per 64 multiply-adds
+        if (tid < 128) {                               // level 3a: M = A_BA X_AA
+            const int h = tid >> 6, r0 = 4 * ((tid >> 3) & 7), c0 = 4 * (tid & 7);
             const float *L = Lf(h), *X = Xi(h);
-            float m[4] = {};
-#pragma unroll
+            float m[4][4] = {};
+#pragma unroll 2
             for (int k4 = 0; k4 < 8; ++k4) {
-                const float4 l4 = *reinterpret_cast<const float4 *>(L + lb_at(32 + r, 4 * k4));
-                const float lk[4] = {l4.x, l4.y, l4.z, l4.w};
+                float av[4][4], xv[4][4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 x4 = *reinterpret_cast<const float4 *>(X + (4 * k4 + e) * XLD + c);
-                    m[0] = fmaf(lk[e], x4.x, m[0]);
-                    m[1] = fmaf(lk[e], x4.y, m[1]);
-                    m[2] = fmaf(lk[e], x4.z, m[2]);
-                    m[3] = fmaf(lk[e], x4.w, m[3]);
+                for (int i = 0; i < 4; ++i) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(L + lb_at(32 + r0 + i, 4 * k4));
+                    av[i][0] = l4.x; av[i][1] = l4.y; av[i][2] = l4.z; av[i][3] = l4.w;
+                    const float4 x4 = *reinterpret_cast<const float4 *>(X + (4 * k4 + i) * XLD + c0);
+                    xv[i][0] = x4.x; xv[i][1] = x4.y; xv[i][2] = x4.z; xv[i][3] = x4.w;
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) m[i][jj] = fmaf(av[i][e], xv[e][jj], m[i][jj]);
             }
-            *reinterpret_cast<float4 *>(Mm(h) + r * MLD + c) = make_float4(m[0], m[1], m[2], m[3]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4 *>(Mm(h) + (r0 + i) * MLD + c0) = make_float4(m[i][0], m[i][1], m[i][2], m[i][3]);
         }
         __syncthreads();
-        {                                              // level 3b: X_BA = -X_BB M
-            const int h = tid >> 8, r = (tid >> 3) & 31, c = 4 * (tid & 7);
+        if (tid < 128) {                               // level 3b: X_BA = -X_BB M
+            const int h = tid >> 6, r0 = 4 * ((tid >> 3) & 7), c0 = 4 * (tid & 7);
             float *X = Xi(h);
             const float *M = Mm(h);
-            float x[4] = {};
-#pragma unroll
+            float x[4][4] = {};
+#pragma unroll 2
             for (int k4 = 0; k4 < 8; ++k4) {
-                const float4 xb4 = *reinterpret_cast<const float4 *>(X + (32 + r) * XLD + 32 + 4 * k4);
-                const float xb[4] = {xb4.x, xb4.y, xb4.z, xb4.w};
+                float bv[4][4], mv[4][4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 m4 = *reinterpret_cast<const float4 *>(M + (4 * k4 + e) * MLD + c);
-                    x[0] = fmaf(xb[e], m4.x, x[0]);
-                    x[1] = fmaf(xb[e], m4.y, x[1]);
-                    x[2] = fmaf(xb[e], m4.z, x[2]);
-                    x[3] = fmaf(xb[e], m4.w, x[3]);
+                for (int i = 0; i < 4; ++i) {
+                    const float4 b4 = *reinterpret_cast<const float4 *>(X + (32 + r0 + i) * XLD + 32 + 4 * k4);
+                    bv[i][0] = b4.x; bv[i][1] = b4.y; bv[i][2] = b4.z; bv[i][3] = b4.w;
+                    const float4 m4 = *reinterpret_cast<const float4 *>(M + (4 * k4 + i) * MLD + c0);
+                    mv[i][0] = m4.x; mv[i][1] = m4.y; mv[i][2] = m4.z; mv[i][3] = m4.w;
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) x[i][jj] = fmaf(bv[i][e], mv[e][jj], x[i][jj]);
             }
-            *reinterpret_cast<float4 *>(X + (32 + r) * XLD + c) = make_float4(-x[0], -x[1], -x[2], -x[3]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4 *>(X + (32 + r0 + i) * XLD + c0) = make_float4(-x[i][0], -x[i][1], -x[i][2], -x[i][3]);
         }
         __syncthreads();
         {                                              // T = X diag(beta), T' = T diag(gamma): fp16, K-major
@@ -645,8 +645,8 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
 #pragma unroll
                 for (int e4 = 0; e4 < 2; ++e4) {
                     const float4 x4 = *reinterpret_cast<const float4 *>(X + t * XLD + s0 + 4 * e4);
-                    const float4 b4 = *reinterpret_cast<const float4 *>(&ss.B[h][s0 + 4 * e4]);
-                    const float4 m4 = *reinterpret_cast<const float4 *>(&ss.gam[h][s0 + 4 * e4]);
+                    const float4 b4 = *reinterpret_cast<const float4 *>(&gr[h][GR_B + s0 + 4 * e4]);
+                    const float4 m4 = *reinterpret_cast<const float4 *>(&gr[h][GR_GAM + s0 + 4 * e4]);
                     xv[4 * e4] = x4.x; xv[4 * e4 + 1] = x4.y; xv[4 * e4 + 2] = x4.z; xv[4 * e4 + 3] = x4.w;
                     bv[4 * e4] = b4.x; bv[4 * e4 + 1] = b4.y; bv[4 * e4 + 2] = b4.z; bv[4 * e4 + 3] = b4.w;
                     gv[4 * e4] = m4.x; gv[4 * e4 + 1] = m4.y; gv[4 * e4 + 2] = m4.z; gv[4 * e4 + 3] = m4.w;
@@ -810,6 +810,8 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
     float *S_dst = (fr.flags & 2) ? (a.S_out ? a.S_out + ((size_t)fr.seq * HV + vh) * (DV * DK) : nullptr)
                                   : a.slot_out + (size_t)vh * (DV * DK);
     auto blob_of = [&](int c) { return a.blobs + ((size_t)(fr.chunk0 + c) * HV + vh) * BLOB_BYTES; };
+    // gamma_n of chunk c: gamma_t of its last row (g is 0 past the chunk's tokens)
+    auto gamma_n = [&](int c) { return __ldg(a.gates + ((size_t)(fr.chunk0 + c) * HV + vh) * GATE_FLOATS + GR_GAM + CH - 1); };
     auto nv_of = [&](int c) { return min(CH, fr.row_b - fr.row_a - CH * c); };
     auto s16_of = [&](int c) { return TC_S16 + 64u * (uint32_t)(c & 1); };   // fp16 state the chunk's products read
 
@@ -930,7 +932,7 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
                     s[p][e] = v.x; s[p][e + 1] = v.y; s[p][e + 2] = v.z; s[p][e + 3] = v.w;
                 }
-            const float g0 = *reinterpret_cast<const float *>(blob_of(0) + BL_GN);
+            const float g0 = gamma_n(0);
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
                 uint32_t wd[16];
@@ -950,7 +952,7 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
             const int st = c & 1;
             const uint32_t par = (uint32_t)(c & 1), spar = (uint32_t)((c >> 1) & 1);
             const unsigned char *stg = sm + st * STAGE_BYTES + ST_BLOB;
-            const float g_next = c + 1 < nc ? *reinterpret_cast<const float *>(blob_of(c + 1) + BL_GN) : 0.0f;
+            const float g_next = c + 1 < nc ? gamma_n(c + 1) : 0.0f;
             // ---- E1: Vnew^T for tokens [32 hh, 32 hh + 32). Tokens past the chunk need
             //      no mask: their rows of U and W are zero, so Vnew is zero there.
             if (!wait(ss.full[st], spar) || !wait(ss.m1a, par) || !wait(ss.m1b, par)) break;
@@ -1126,12 +1128,13 @@ static size_t rnd256(size_t x) { return (x + 255) & ~(size_t)255; }
 static size_t rnd1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
 struct WyLayout {
-    size_t count, frags, chunks, xhat, ybuf, blobs, slots, total;
+    size_t count, frags, chunks, gates, xhat, ybuf, blobs, slots, total;
     int W, f_cap, c_cap;
 };
 
 // Workspace of the chunked path for windows of W tokens (W a multiple of 64):
-// counts | fragments | chunks | x^ [W][8192] fp16 | y [W][4096] fp16 | blobs [c_cap][32] | two state slots.
+// counts | fragments | chunks | gate records [c_cap][32] | x^ [W][8192] fp16 | y [W][4096] fp16 |
+// blobs [c_cap][32] | two state slots.
 static WyLayout wy_layout(int N, int W)
 {
     WyLayout L;
@@ -1142,6 +1145,7 @@ static WyLayout wy_layout(int N, int W)
     L.count = o;  o = rnd256(o + sizeof(WyCount));
     L.frags = o;  o = rnd256(o + (size_t)L.f_cap * sizeof(WyFrag));
     L.chunks = o; o = rnd1024(o + (size_t)L.c_cap * sizeof(WyChunk));
+    L.gates = o;  o = rnd1024(o + (size_t)L.c_cap * HV * GATE_FLOATS * sizeof(float));
     L.xhat = o;   o = rnd1024(o + (size_t)W * CC * sizeof(__half));
     L.ybuf = o;   o = rnd1024(o + (size_t)W * DI * sizeof(__half));
     L.blobs = o;  o = rnd1024(o + (size_t)L.c_cap * HV * BLOB_BYTES);
@@ -1209,6 +1213,7 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
         a.count = reinterpret_cast<WyCount *>(ws + L.count);
         a.frags = reinterpret_cast<WyFrag *>(ws + L.frags);
         a.chunks = reinterpret_cast<WyChunk *>(ws + L.chunks);
+        a.gates = reinterpret_cast<float *>(ws + L.gates);
         a.xhat = reinterpret_cast<__half *>(ws + L.xhat);
         a.ybuf = reinterpret_cast<__half *>(ws + L.ybuf);
         a.blobs = ws + L.blobs;
