@@ -327,6 +327,12 @@ gdn_status gdn_device_error(void *stream)
     return any == 0 ? GDN_OK : GDN_ERR_TIMEOUT;
 }
 
+gdn_status gdn_get_device_error(void *workspace, void *stream)
+{
+    (void)workspace;
+    return gdn_device_error(stream);
+}
+
 gdn_status gdn_selftest_wait_timeout(void *stream)
 {
     cudaError_t e = launch_wait_timeout((cudaStream_t)stream);

@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_selftest_wait_timeout.argtypes = [_vp]
         L.gdn_device_error.restype = _int
         L.gdn_device_error.argtypes = [_vp]
+        L.gdn_get_device_error.restype = _int
+        L.gdn_get_device_error.argtypes = [_vp, _vp]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_status_string.argtypes = [_int]
         L.gdn_last_error.restype = ctypes.c_char_p

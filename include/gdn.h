@@ -309,6 +309,13 @@ size_t gdn_prefill_workspace_size(int N, int T_total, gdn_dtype act, int chunk_s
  * current device gave up since the word was last cleared. */
 gdn_status gdn_device_error(void *stream);
 
+/* The same query under the name and argument list that the mixer's boundary
+ * is specified with: `workspace` is accepted for that signature and not read
+ * (the error word is per device, not per workspace, so a timeout in any call
+ * is seen whichever workspace is named; NULL is fine). Same result and
+ * synchronisation as gdn_device_error(stream). */
+gdn_status gdn_get_device_error(void *workspace, void *stream);
+
 /* Diagnostic of the failure path above: enqueues one small kernel that waits
  * on an mbarrier nothing ever completes, through the library's bounded wait.
  * After the limit (2 s) the kernel records GDN_ERR_TIMEOUT and returns

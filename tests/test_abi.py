@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     for n in ("gdn_conv_step", "gdn_decode_step", "gdn_decode_multi", "gdn_prefill", "gdn_prefill_workspace_size",
               "gdn_in_proj", "gdn_out_proj", "gdn_attn_decode", "gdn_attn_decode_workspace_size",
               "gdn_selftest_wait_timeout",
-              "gdn_device_error", "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
+              "gdn_device_error", "gdn_get_device_error", "gdn_status_string", "gdn_last_error", "gdn_abi_version"):
         assert n in names
 
 
@@ -86,7 +86,10 @@ def test_chunked_workspace_is_bounded(ops):
     assert L.gdn_prefill_workspace_size(8, 70264, ops.GDN_BF16, 64) == L.gdn_prefill_workspace_size(8, 4096, ops.GDN_BF16, 64)
     assert L.gdn_prefill_workspace_size(65535, 1 << 20, ops.GDN_BF16, 64) == \
         L.gdn_prefill_workspace_size(4096, 1 << 20, ops.GDN_BF16, 64)
-    assert a < 160 << 20
+    # one 4096-token window: 64 chunks x 32 V-heads of 72 KiB operand blobs
+    # (144 MiB), 64 MiB of fp16 activations, 32 MiB of fp16 y, the gate records
+    # and the tables
+    assert 240 << 20 < a < 256 << 20
 
 
 FAKE = 0x10000          # 16-byte aligned, never dereferenced: every case fails a host check first

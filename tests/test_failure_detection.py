@@ -35,6 +35,11 @@ def test_bounded_wait_reports_timeout_and_context_survives(ops):
     assert 1.5 < waited < 30.0, f"the bounded wait took {waited:.1f} s"
     assert ops.device_error() == ops.GDN_OK              # the word was cleared
 
+    # the same query under its specified name and arguments (the workspace is not read)
+    ops.selftest_wait_timeout()
+    assert ops.lib().gdn_get_device_error(None, None) == ops.GDN_ERR_TIMEOUT
+    assert ops.lib().gdn_get_device_error(None, None) == ops.GDN_OK
+
     # the context still runs the library's kernels correctly
     a = I.attn_inputs(31, 2, 200, [200, 50])
     d = a.to("cuda")
