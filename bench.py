@@ -50,6 +50,7 @@ DECODE_PARAM_BYTES_PER_LAUNCH = 131_840
 # e.g. a speculative step. The state and conv_state cross HBM once per call, the
 # per-token inputs and outputs once per token.
 MULTI_T = 4
+MULTI_TS = (2, 4, 8)        # the multi-token leg runs each; MULTI_T is the one the roofline object names
 # Algorithmic FLOPs of the chunked prefill per token: the dense contractions
 # K K^T and Q K^T once per K-head; T V, T (Gamma K), W S, Q S, the intra-chunk
 # (M o Q K^T) V_new and the state update K^T V_new per V-head, with C=64.
@@ -62,16 +63,55 @@ PREFILL_FLOP_PER_TOKEN = 5_242_880
 # the bf16 output written once (3 x B x 16 x 256 x 2 B), ctx_len (B x 4 B).
 ATTN_LAYERS, ATTN_CTX = 10, 4096
 ATTN_BYTES_PER_CALL = BATCH * 2 * ATTN_CTX * 256 * 2 * 2 + 3 * BATCH * 16 * 256 * 2 + BATCH * 4
-# DRAM traffic of one attn_block_kernel launch at B=256 (ncu capture in
-# profiles/attn_decode_B256_ctx4096.md). None once the kernel or its launch
-# shape changes without a new capture.
-ATTN_TRAFFIC_PER_CALL = 2_149_655_040 + 18_066_688
+# Algorithmic bytes of one T=4096 bf16 prefill call: the per-token streams
+# (32,896 B per token, as for decode), the final state (32 x 128 x 128 x 4) and
+# conv_state (3 x 8192 x 2) written, the layer's parameters read.
+PREFILL_IO_BYTES_PER_TOKEN = 32_896
+PREFILL_END_STATE_BYTES = 2_097_152 + 49_152
+PREFILL_PARAM_BYTES = 131_840
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode launch at B=256
-# (one layer, cold L2), from the ncu capture in
-# profiles/decode_step_kernel_B256.md. Set to None whenever the kernel changes
-# without a new capture.
-DECODE_TRAFFIC_PER_LAUNCH = 555_980_032 + 490_060_544
+# Measured DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, one ncu
+# capture each, cold L2) per launch or per call, with the source file of the
+# kernels it covers and that file's SHA-256 prefix at capture time. A figure
+# whose source has changed since is reported as null: the counters no longer
+# describe the kernel that ran. The summaries under profiles/ give the
+# commands and the per-kernel split.
+TRAFFIC = {
+    "decode": dict(bytes=555_963_648 + 490_369_536, src="gdn_decode.cu", sha="99381d2bf3475be0", profile="profiles/decode_step_kernel_B256.md",
+                   per="launch of decode_step_kernel at B=256"),
+    "attn": dict(bytes=2_168_676_864 + 18_318_080, src="gdn_attn.cu", sha="c68c58d38f8812f9", profile="profiles/attn_decode_B256_ctx4096.md",
+                 per="call (attn_block_kernel + attn_combine_kernel) at B=256, ctx 4096"),
+    "multi": dict(bytes=574_938_112 + 495_531_520, src="gdn_decode_multi.cu", sha="a78ad87764f2cd50", profile="profiles/decode_multi_kernel_B256_T4.md",
+                  per="launch of decode_multi_kernel at B=256, T=4"),
+    "prefill": dict(bytes=355_513_344 + 124_455_168, src="gdn_chunk.cu", sha="31a2a1c8a298dbf3", profile="profiles/chunk_prefill_T4096.md",
+                    per="gdn_prefill call at T=4096 (all of its kernels)"),
+    "varlen": dict(bytes=6_169_908_224 + 2_179_091_968, src="gdn_chunk.cu", sha="31a2a1c8a298dbf3", profile="profiles/chunk_prefill_varlen8.md",
+                   per="gdn_prefill call on the 8-sequence varlen workload (all of its kernels)"),
+    "in_proj": dict(bytes=109_801_728 + 76_413_184, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
+                    per="gdn_in_proj call at M=4096"),
+    "out_proj": dict(bytes=50_358_016 + 100_096, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
+                     per="gdn_out_proj call at M=4096"),
+    "out_proj_batch": dict(bytes=18_900_224 + 0, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
+                           per="gdn_out_proj call at M=256"),
+}
+
+
+def traffic(key):
+    """(bytes, note) of a TRAFFIC entry: the bytes only while the kernel source
+    is the one the counters were taken on."""
+    import hashlib
+    t = TRAFFIC[key]
+    path = os.path.join(ROOT, "gated_deltanet_linear_02_gb300", "csrc", t["src"])
+    try:
+        with open(path, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        sha = None
+    if t["bytes"] is None:
+        return None, f"not captured for this kernel version ({t['src']} sha {sha})"
+    if sha != t["sha"]:
+        return None, f"{t['src']} changed since the capture in {t['profile']} (sha {t['sha']} -> {sha})"
+    return t["bytes"], f"ncu, per {t['per']}, {t['profile']}"
 
 
 def load_peaks():
@@ -209,33 +249,36 @@ def run_gpu(args, rank, world, dev):
     achieved = bytes_per_launch / per_launch_s / 1e9
     dec_tok_s = job_rate(BATCH * args.steps, world, dec_ms)
 
-    # ---------------- multi-token decode: MULTI_T consecutive tokens per sequence
+    # ---------------- multi-token decode: T consecutive tokens per sequence
     #                  (gdn_decode_multi) through the same 30 layers and states
-    m_streams = [I.streams(I.seed_of(3, 100 + layer), MULTI_T, torch.bfloat16, device=dev, lead=(BATCH,))
-                 for layer in range(LAYERS)]
-    m_out = [torch.empty(BATCH, MULTI_T, I.D_INNER, dtype=torch.bfloat16, device=dev) for _ in range(LAYERS)]
+    mts = {}
+    for MT in MULTI_TS:
+        m_streams = [I.streams(I.seed_of(3, 100 + layer), MT, torch.bfloat16, device=dev, lead=(BATCH,))
+                     for layer in range(LAYERS)]
+        m_out = [torch.empty(BATCH, MT, I.D_INNER, dtype=torch.bfloat16, device=dev) for _ in range(LAYERS)]
 
-    def multi_step():
-        for L, ms, mo in zip(layers, m_streams, m_out):
-            ops.decode_multi(None, ms.qkv, ms.z, ms.alpha, ms.beta, L["conv"], L["S"], mo, cparams=L["cp"])
+        def multi_step():
+            for L, ms, mo in zip(layers, m_streams, m_out):
+                ops.decode_multi(None, ms.qkv, ms.z, ms.alpha, ms.beta, L["conv"], L["S"], mo, cparams=L["cp"])
 
-    for _ in range(args.warmup):
-        multi_step()
-    barrier_sync()
-    t_wall0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        multi_step()
-    ev1.record(stream)
-    barrier_sync()
-    sampler.mark(t_wall0, time.time())
-    mt_ms = max_over_ranks(ev0.elapsed_time(ev1))
-    mt_launch_s = mt_ms / 1e3 / (LAYERS * args.steps)
-    mt_bytes = BATCH * (DECODE_STATE_CONV_BYTES + MULTI_T * DECODE_IO_BYTES_PER_TOKEN) + DECODE_PARAM_BYTES_PER_LAUNCH
-    mt = dict(tok_s=job_rate(BATCH * MULTI_T * args.steps, world, mt_ms), launch_s=mt_launch_s, bytes=mt_bytes,
-              achieved=mt_bytes / mt_launch_s / 1e9)
-    assert ops.device_error() == ops.GDN_OK
-    del m_streams, m_out
+        for _ in range(args.warmup):
+            multi_step()
+        barrier_sync()
+        t_wall0 = time.time()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            multi_step()
+        ev1.record(stream)
+        barrier_sync()
+        sampler.mark(t_wall0, time.time())
+        mt_ms = max_over_ranks(ev0.elapsed_time(ev1))
+        mt_launch_s = mt_ms / 1e3 / (LAYERS * args.steps)
+        mt_bytes = BATCH * (DECODE_STATE_CONV_BYTES + MT * DECODE_IO_BYTES_PER_TOKEN) + DECODE_PARAM_BYTES_PER_LAUNCH
+        mts[MT] = dict(tok_s=job_rate(BATCH * MT * args.steps, world, mt_ms), launch_s=mt_launch_s, bytes=mt_bytes,
+                       achieved=mt_bytes / mt_launch_s / 1e9)
+        assert ops.device_error() == ops.GDN_OK
+        del m_streams, m_out
+    mt = mts[MULTI_T]
 
     # ---------------- e2e: the same decode through the C ABI from pinned host buffers
     host_in = []
@@ -354,8 +397,9 @@ def run_gpu(args, rank, world, dev):
         barrier_sync()
         sampler.mark(t_wall0, time.time())
         ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))
+        ob = I.N_EMBD * I.D_INNER * 2 + M * I.D_INNER * 2 + M * I.N_EMBD * 2
         op[M] = dict(us=ms * 1e3, tflops=2.0 * M * I.D_INNER * I.N_EMBD / (ms / 1e3) / 1e12,
-                     gbs=(I.N_EMBD * I.D_INNER * 2 + M * I.D_INNER * 2 + M * I.N_EMBD * 2) / (ms / 1e3) / 1e9)
+                     bytes=ob, gbs=ob / (ms / 1e3) / 1e9)
         del xo, yo
     # ---------------- input projections (gdn_in_proj) at the prefill size
     w_in = torch.cat(I.in_proj_weights(I.seed_of(2), device=dev), dim=0)
@@ -376,7 +420,9 @@ def run_gpu(args, rank, world, dev):
     barrier_sync()
     sampler.mark(t_wall0, time.time())
     ip_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))
-    ip = dict(us=ip_ms * 1e3, tflops=2.0 * PREFILL_T * w_in.shape[0] * I.N_EMBD / (ip_ms / 1e3) / 1e12)
+    ip_bytes = (PREFILL_T * I.N_EMBD + w_in.shape[0] * I.N_EMBD + PREFILL_T * w_in.shape[0]) * 2
+    ip = dict(us=ip_ms * 1e3, tflops=2.0 * PREFILL_T * w_in.shape[0] * I.N_EMBD / (ip_ms / 1e3) / 1e12,
+              bytes=ip_bytes, gbs=ip_bytes / (ip_ms / 1e3) / 1e9)
     del w_in, h_in, outs_in
     assert ops.device_error() == ops.GDN_OK
     torch.cuda.empty_cache()
@@ -406,16 +452,17 @@ def run_gpu(args, rank, world, dev):
     assert ops.device_error() == ops.GDN_OK
     del att, att_out, att_ws
     torch.cuda.empty_cache()
-    cfgs = other_configs(args, torch, I, ops, dev, stream, flush, barrier_sync, max_over_ranks, sampler)
+    cfgs = other_configs(args, torch, I, ops, dev, stream, flush, barrier_sync, max_over_ranks, sampler,
+                         hbm_peak, tc_peak)
     clocks = sampler.stop()
 
-    return dict(cfgs=cfgs, at=at, ip=ip, op=op, mt=mt, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
+    return dict(cfgs=cfgs, at=at, ip=ip, op=op, mt=mt, mts=mts, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
                 bytes_per_launch=bytes_per_launch, launches=launches, e2e_tok_s=e2e_tok_s, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, pf_ms=pf_ms, pf_tok_s=pf_tok_s, pf_tflops=pf_tflops, hbm_peak=hbm_peak,
                 tc_peak=tc_peak, peak_src=peak_src, clocks=clocks)
 
 
-def other_configs(args, torch, I, ops, dev, stream, flush, barrier_sync, max_over_ranks, sampler):
+def other_configs(args, torch, I, ops, dev, stream, flush, barrier_sync, max_over_ranks, sampler, hbm_peak, tc_peak):
     """The other configurations of the metric, timed beside the headline:
     0) one layer, T=64, fp32, zero states: the prefill (exact scan) and 64
        decode steps; 1) one layer, B=64, 128 sequential decode steps, bf16;
@@ -518,10 +565,20 @@ def other_configs(args, torch, I, ops, dev, stream, flush, barrier_sync, max_ove
     ms = time_calls(lambda: ops.prefill(None, st.qkv, st.z, st.alpha, st.beta, cu, o, conv, cout, S, sout,
                                         workspace=ws, cparams=cp))
     tflops = PREFILL_FLOP_PER_TOKEN * T4 / (ms / 1e3) / 1e12
-    io = T4 * DECODE_IO_BYTES_PER_TOKEN + len(lens) * DECODE_STATE_CONV_BYTES   # streams, states in and out
+    # streams, states in and out, parameters
+    io = T4 * PREFILL_IO_BYTES_PER_TOKEN + len(lens) * DECODE_STATE_CONV_BYTES + PREFILL_PARAM_BYTES
+    tr, tr_note = traffic("varlen")
     out["varlen_prefill_8seq_bf16"] = {"lengths": lens, "tokens": T4, "value": T4 / (ms / 1e3), "unit": "tok/s",
                                        "ms_per_call": ms, "tflops": tflops,
-                                       "io_GBs": io / (ms / 1e3) / 1e9}
+                                       "io_GBs": io / (ms / 1e3) / 1e9,
+                                       "roofline": {"bound": "tensor", "achieved": tflops, "peak": tc_peak,
+                                                    "unit": "TFLOP/s", "frac": tflops / tc_peak,
+                                                    "hbm_achieved_GBs": io / (ms / 1e3) / 1e9,
+                                                    "hbm_frac": io / (ms / 1e3) / 1e9 / hbm_peak,
+                                                    "frac_of_nominal_8TBs": io / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                                                    "algorithmic_flop_per_call": PREFILL_FLOP_PER_TOKEN * T4,
+                                                    "algorithmic_bytes_per_call": io,
+                                                    "traffic": tr, "traffic_source": tr_note}}
     del st, conv, S, o, cout, sout, ws
     assert ops.device_error() == ops.GDN_OK
     return out
@@ -592,10 +649,11 @@ def profile_case(args):
     """A small, self-contained run of one path for profilers: no JSON line, no
     clocks, a few launches on a few GB. ``--case decode``: --layers layers of
     gdn_decode_step on --batch sequences; ``--case multi``: the same with
-    gdn_decode_multi, MULTI_T tokens per sequence; ``--case prefill``: gdn_prefill on one
+    gdn_decode_multi, --mt tokens per sequence; ``--case prefill``: gdn_prefill on one
     sequence of --T tokens; ``--case out_proj`` / ``--case in_proj``: the
     projection GEMMs on --T rows; ``--case attn``: gdn_attn_decode on --batch
-    sequences with a --T position context."""
+    sequences with a --T position context; ``--case varlen``: gdn_prefill on
+    the 8-sequence varlen workload."""
     import torch
 
     from gated_deltanet_linear_02_gb300 import build as gbuild
@@ -629,8 +687,8 @@ def profile_case(args):
             seed = I.seed_of(3, layer)
             lp = I.layer_params(seed).to(dev)
             conv, S = I.initial_states(seed, args.batch, torch.bfloat16, device=dev)
-            st = I.streams(seed, MULTI_T, torch.bfloat16, device=dev, lead=(args.batch,))
-            out = torch.empty(args.batch, MULTI_T, I.D_INNER, dtype=torch.bfloat16, device=dev)
+            st = I.streams(seed, args.mt, torch.bfloat16, device=dev, lead=(args.batch,))
+            out = torch.empty(args.batch, args.mt, I.D_INNER, dtype=torch.bfloat16, device=dev)
             Ls.append((ops.make_params(lp), conv, S, st, out))
         for _ in range(n):
             for cp, conv, S, st, out in Ls:
@@ -648,6 +706,20 @@ def profile_case(args):
         outs = [torch.empty(args.T, m, dtype=torch.bfloat16, device=dev) for m in (I.C_CONV, I.D_INNER, I.HV, I.HV)]
         for _ in range(n):
             ops.in_proj(h, w_in, *outs)
+        assert ops.device_error() == ops.GDN_OK
+    elif args.case == "varlen":
+        seed = I.seed_of(4)
+        lens = I.varlen_lengths(seed)
+        T4 = sum(lens)
+        lp = I.layer_params(seed).to(dev)
+        st = I.streams(seed, T4, torch.bfloat16, device=dev)
+        conv, S = I.initial_states(seed, len(lens), torch.bfloat16, device=dev)
+        cu = I.cu_seqlens(lens).to(dev)
+        out = torch.empty(T4, I.D_INNER, dtype=torch.bfloat16, device=dev)
+        cout, sout = torch.empty_like(conv), torch.empty_like(S)
+        ws = torch.empty(ops.prefill_workspace_size(len(lens), T4, torch.bfloat16, 0), dtype=torch.uint8, device=dev)
+        for _ in range(n):
+            ops.prefill(lp, st.qkv, st.z, st.alpha, st.beta, cu, out, conv, cout, S, sout, workspace=ws)
         assert ops.device_error() == ops.GDN_OK
     else:
         seed = I.seed_of(2)
@@ -673,12 +745,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["decode", "multi", "prefill", "out_proj", "in_proj", "attn"], default=None,
+    ap.add_argument("--case", choices=["decode", "multi", "prefill", "varlen", "out_proj", "in_proj", "attn"],
+                    default=None,
                     help="profiling run of one path (see profile_case); prints no JSON line")
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--layers", type=int, default=1)
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--mt", type=int, default=MULTI_T, help="tokens per sequence of --case multi")
     args = ap.parse_args()
     if args.case is not None:
         profile_case(args)
@@ -736,6 +810,15 @@ def main():
     if rank != 0:
         return
     frac = r["achieved"] / r["hbm_peak"]
+    dec_tr, dec_tr_note = traffic("decode")
+    at_tr, at_tr_note = traffic("attn")
+    mt_tr, mt_tr_note = traffic("multi")
+    pf_tr, pf_tr_note = traffic("prefill")
+    ip_tr, ip_tr_note = traffic("in_proj")
+    op_tr, op_tr_note = traffic("out_proj")
+    opb_tr, opb_tr_note = traffic("out_proj_batch")
+    PREFILL_BYTES = PREFILL_T * PREFILL_IO_BYTES_PER_TOKEN + PREFILL_END_STATE_BYTES + PREFILL_PARAM_BYTES
+    pf_gbs = PREFILL_BYTES / (r["pf_ms"] / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": r["dec_tok_s"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["dec_ms"] / args.steps, "higher_is_better": True,
@@ -744,7 +827,7 @@ def main():
                    "activations": "bf16", "state": "fp32", "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (15 GiB of state touched per step)"},
         "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["hbm_peak"], "unit": "GB/s",
-                     "frac": frac, "traffic": DECODE_TRAFFIC_PER_LAUNCH,
+                     "frac": frac, "traffic": dec_tr, "traffic_source": dec_tr_note,
                      "kernel": "decode_step_kernel<bf16,bf16>",
                      "peak_source": f"{r['peak_src']} (MEASURED_PEAKS.json hbm_gbs)" if r["peak_src"] == "measured"
                      else "fallback 6.8 TB/s",
@@ -760,19 +843,35 @@ def main():
                     "ms_per_call": r["pf_ms"], "l2": "flushed between timed calls",
                     "roofline": {"bound": "tensor", "achieved": r["pf_tflops"], "peak": r["tc_peak"],
                                  "unit": "TFLOP/s", "frac": r["pf_tflops"] / r["tc_peak"],
-                                 "algorithmic_flop_per_call": PREFILL_FLOP_PER_TOKEN * PREFILL_T}},
+                                 "hbm_achieved_GBs": pf_gbs, "hbm_frac": pf_gbs / r["hbm_peak"],
+                                 "frac_of_nominal_8TBs": pf_gbs / NOMINAL_HBM_GBS,
+                                 "algorithmic_flop_per_call": PREFILL_FLOP_PER_TOKEN * PREFILL_T,
+                                 "algorithmic_bytes_per_call": PREFILL_BYTES,
+                                 "traffic": pf_tr, "traffic_source": pf_tr_note,
+                                 "timed": "whole gdn_prefill call (plan, activation, prep, carry, gated norm, "
+                                          "conv_state kernels)"}},
         "in_proj": {"workload": f"input_projections_M{PREFILL_T}_bf16", "op": "qkv|z|alpha|beta = h w_in^T, 2048 -> 12352",
                     "us_per_call": r["ip"]["us"], "l2": "flushed between timed calls",
                     "roofline": {"bound": "tensor", "achieved": r["ip"]["tflops"], "peak": r["tc_peak"],
-                                 "unit": "TFLOP/s", "frac": r["ip"]["tflops"] / r["tc_peak"]}},
+                                 "unit": "TFLOP/s", "frac": r["ip"]["tflops"] / r["tc_peak"],
+                                 "hbm_achieved_GBs": r["ip"]["gbs"], "hbm_frac": r["ip"]["gbs"] / r["hbm_peak"],
+                                 "algorithmic_bytes_per_call": r["ip"]["bytes"],
+                                 "traffic": ip_tr, "traffic_source": ip_tr_note}},
         "out_proj": {"workload": f"ssm_out_projection_M{PREFILL_T}_bf16", "op": "y = x w^T, 4096 -> 2048",
                      "us_per_call": r["op"][PREFILL_T]["us"], "l2": "flushed between timed calls",
                      "roofline": {"bound": "tensor", "achieved": r["op"][PREFILL_T]["tflops"], "peak": r["tc_peak"],
-                                  "unit": "TFLOP/s", "frac": r["op"][PREFILL_T]["tflops"] / r["tc_peak"]},
+                                  "unit": "TFLOP/s", "frac": r["op"][PREFILL_T]["tflops"] / r["tc_peak"],
+                                  "hbm_achieved_GBs": r["op"][PREFILL_T]["gbs"],
+                                  "hbm_frac": r["op"][PREFILL_T]["gbs"] / r["hbm_peak"],
+                                  "algorithmic_bytes_per_call": r["op"][PREFILL_T]["bytes"],
+                                  "traffic": op_tr, "traffic_source": op_tr_note},
                      "decode_batch": {"M": BATCH, "us_per_call": r["op"][BATCH]["us"],
                                       "roofline": {"bound": "hbm", "achieved": r["op"][BATCH]["gbs"],
                                                    "peak": r["hbm_peak"], "unit": "GB/s",
-                                                   "frac": r["op"][BATCH]["gbs"] / r["hbm_peak"]}}},
+                                                   "frac": r["op"][BATCH]["gbs"] / r["hbm_peak"],
+                                                   "tensor_frac": r["op"][BATCH]["tflops"] / r["tc_peak"],
+                                                   "algorithmic_bytes_per_call": r["op"][BATCH]["bytes"],
+                                                   "traffic": opb_tr, "traffic_source": opb_tr_note}}},
         "attn_decode": {"workload": f"attn_decode_{ATTN_LAYERS}L_B{BATCH}_ctx{ATTN_CTX}_bf16",
                         "op": "GQA 16q/2kv, head_dim 256, softmax(q k^T / 16) v * sigmoid(z)",
                         "value": r["at"]["tok_s"], "unit": "tok/s", "us_per_call": r["at"]["call_s"] * 1e6,
@@ -780,7 +879,10 @@ def main():
                         "roofline": {"bound": "hbm", "achieved": r["at"]["achieved"], "peak": r["hbm_peak"],
                                      "unit": "GB/s", "frac": r["at"]["achieved"] / r["hbm_peak"],
                                      "algorithmic_bytes_per_call": ATTN_BYTES_PER_CALL,
-                                     "traffic": ATTN_TRAFFIC_PER_CALL, "kernel": "attn_block_kernel<bf16>",
+                                     "hbm_frac": r["at"]["achieved"] / r["hbm_peak"],
+                                     "frac_of_nominal_8TBs": r["at"]["achieved"] / NOMINAL_HBM_GBS,
+                                     "traffic": at_tr, "traffic_source": at_tr_note,
+                                     "kernel": "attn_block_kernel<bf16>",
                                      "timed": "whole call: attn_block_kernel + attn_combine_kernel"}},
         "other_configs": r["cfgs"],
         "decode_multi": {"workload": f"decode_multi_30L_B{BATCH}_T{MULTI_T}_bf16", "value": r["mt"]["tok_s"],
@@ -788,7 +890,15 @@ def main():
                          "launch_us": r["mt"]["launch_s"] * 1e6,
                          "roofline": {"bound": "hbm", "achieved": r["mt"]["achieved"], "peak": r["hbm_peak"],
                                       "unit": "GB/s", "frac": r["mt"]["achieved"] / r["hbm_peak"],
-                                      "algorithmic_bytes_per_launch": r["mt"]["bytes"]}},
+                                      "frac_of_nominal_8TBs": r["mt"]["achieved"] / NOMINAL_HBM_GBS,
+                                      "algorithmic_bytes_per_launch": r["mt"]["bytes"],
+                                      "traffic": mt_tr, "traffic_source": mt_tr_note},
+                         "by_tokens_per_sequence": {
+                             str(t): {"value": m["tok_s"], "unit": "tok/s", "launch_us": m["launch_s"] * 1e6,
+                                      "achieved_GBs": m["achieved"], "frac": m["achieved"] / r["hbm_peak"],
+                                      "frac_of_nominal_8TBs": m["achieved"] / NOMINAL_HBM_GBS,
+                                      "algorithmic_bytes_per_launch": m["bytes"]}
+                             for t, m in sorted(r["mts"].items())}},
     }
     print(json.dumps(line))
 
