@@ -18,6 +18,9 @@ cudaError_t launch_decode_multi(const gdn_params *, const void *, const void *, 
 void *multi_error_word();
 cudaError_t launch_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, cudaStream_t s);
 void *gemm_error_word();
+cudaError_t launch_gated_out_proj(const float *norm_w, float eps, const void *y, const void *z, const void *w,
+                                  void *out, int M, gdn_dtype act, gdn_dtype out_dt, cudaStream_t s);
+void *gproj_error_word();
 cudaError_t launch_in_proj(const void *h, const void *w_in, void *qkv, void *z, void *alpha, void *beta, int M,
                            gdn_dtype act, cudaStream_t s);
 size_t scan_workspace_bytes(int T_total);
@@ -65,7 +68,7 @@ bool ok_dtype(gdn_dtype d) { return d == GDN_F32 || d == GDN_BF16; }
 gdn_status check_params(const gdn_params *p)
 {
     if (p == nullptr) return fail(GDN_ERR_INVALID_ARG, "params is NULL");
-    if (!ok_ptr(p->conv_w) || !ok_ptr(p->A_log) || !ok_ptr(p->dt_bias) || !ok_ptr(p->norm_w))
+    if (!ok_ptr(p->conv_w) || !ok_ptr(p->A_log) || !ok_ptr(p->dt_bias) || !ok_opt_ptr(p->norm_w))
         return fail(GDN_ERR_INVALID_ARG, "a parameter pointer is NULL or not 16-byte aligned");
     if (!(p->norm_eps >= 0.0f) || !(p->l2_eps >= 0.0f))
         return fail(GDN_ERR_INVALID_ARG, "epsilons must be >= 0");
@@ -93,7 +96,7 @@ namespace gdn {
 // clears all of them with one small kernel (an atomic exchange each, so a word
 // set while the call runs is either reported now or kept for the next call)
 // and one copy of the OR back to the host.
-constexpr int N_ERROR_WORDS = 6;
+constexpr int N_ERROR_WORDS = 7;
 struct ErrorWords {
     unsigned int *p[N_ERROR_WORDS];
 };
@@ -121,8 +124,9 @@ static bool error_words(ErrorWords *out)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return false;
     std::lock_guard<std::mutex> lock(mu);
     if (!have[dev]) {
-        void *(*const fns[N_ERROR_WORDS])() = {decode_error_word, chunk_error_word, multi_error_word,
-                                               gemm_error_word,   attn_error_word,  selftest_error_word};
+        void *(*const fns[N_ERROR_WORDS])() = {decode_error_word, chunk_error_word,    multi_error_word,
+                                               gemm_error_word,   attn_error_word,     selftest_error_word,
+                                               gproj_error_word};
         for (int i = 0; i < N_ERROR_WORDS; ++i) {
             cache[dev].p[i] = static_cast<unsigned int *>(fns[i]());
             if (cache[dev].p[i] == nullptr) return false;
@@ -225,6 +229,19 @@ gdn_status gdn_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype 
         return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
     cudaError_t e = launch_out_proj(x, w, y, M, out_dt, (cudaStream_t)stream);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_out_proj");
+}
+
+gdn_status gdn_gated_out_proj(const float *norm_w, float norm_eps, const void *y, const void *z, const void *w,
+                              void *out, int M, gdn_dtype act, gdn_dtype out_dt, void *stream)
+{
+    if (!ok_dtype(act) || !ok_dtype(out_dt)) return fail(GDN_ERR_INVALID_ARG, "unknown activation or output dtype");
+    if (M < 0 || M > (1 << 24)) return fail(GDN_ERR_INVALID_ARG, "M out of range [0, 2^24]");
+    if (M == 0) return GDN_OK;
+    if (!ok_ptr(norm_w) || !ok_ptr(y) || !ok_ptr(z) || !ok_ptr(w) || !ok_ptr(out))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    if (!(norm_eps >= 0.0f)) return fail(GDN_ERR_INVALID_ARG, "norm_eps must be >= 0");
+    cudaError_t e = launch_gated_out_proj(norm_w, norm_eps, y, z, w, out, M, act, out_dt, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_gated_out_proj");
 }
 
 size_t gdn_attn_decode_workspace_size(int B, int Lmax)

@@ -1087,6 +1087,17 @@ __global__ void __launch_bounds__(256) wy_norm_kernel(const WyArgs a)
     const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (row >= a.wlen) return;
     const size_t g = (size_t)(a.w0 + row);
+    if (a.norm_w == nullptr) {                         // no norm weights: out is y itself
+#pragma unroll
+        for (int hh = 0; hh < HV / 8; ++hh) {
+            const int vh = warp * (HV / 8) + hh;
+            const uint2 yv = *reinterpret_cast<const uint2 *>(a.ybuf + (size_t)row * DI + (size_t)vh * DV + 4 * lane);
+            const float2 y01 = __half22float2(*reinterpret_cast<const __half2 *>(&yv.x));
+            const float2 y23 = __half22float2(*reinterpret_cast<const __half2 *>(&yv.y));
+            store_out4<TO>(static_cast<TO *>(a.out) + g * DI + (size_t)vh * DV + 4 * lane, y01.x, y01.y, y23.x, y23.y);
+        }
+        return;
+    }
     const float4 w = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane);
 #pragma unroll
     for (int hh = 0; hh < HV / 8; ++hh) {

@@ -322,8 +322,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_step_kernel(const Decod
             const float *rr4 = sm.red + 16 + 4 * h;
             const float rr = rsqrtf((rr4[0] + rr4[1] + rr4[2] + rr4[3]) * (1.0f / DV) + a.norm_eps);
             const size_t o = b * DI + (size_t)(kh + HK * h) * DV + j;
-            const float zz = to_f(zcur);
-            static_cast<TO *>(a.out)[o] = from_f<TO>(sm.y[h][j] * rr * a.norm_w[j] * silu_f(zz));
+            // without norm weights the output is y itself (the norm runs in the
+            // output projection, gdn_gated_out_proj)
+            static_cast<TO *>(a.out)[o] =
+                from_f<TO>(a.norm_w ? sm.y[h][j] * rr * a.norm_w[j] * silu_f(to_f(zcur)) : sm.y[h][j]);
         }
         // the next prologue writes q/k/v/red[0..7]/gate, none of which the lines above read
     }

@@ -256,7 +256,9 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
         for (int u = 0; u < MD_SLOTS && multi_unit_exists<MT>(a, u); ++u) multi_issue_load(sm, a, u);
 
     const float scale = rsqrtf((float)DK);
-    const float4 nw = load4(a.norm_w + 4 * lane);      // norm weights of columns 4 lane .. 4 lane + 3
+    // norm weights of columns 4 lane .. 4 lane + 3 (none: the output is y itself,
+    // and the norm runs in the output projection, gdn_gated_out_proj)
+    const float4 nw = a.norm_w ? load4(a.norm_w + 4 * lane) : make_float4(1.f, 1.f, 1.f, 1.f);
     MultiIn<TA, MT> pin;
     if ((int)blockIdx.x < a.n_items) pin = multi_load<TA, MT>(a, blockIdx.x, tid);
     for (int m = 0;; ++m) {
@@ -426,8 +428,9 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
             const float4 y4 = reinterpret_cast<const float4 *>(sm.y[t][h])[lane];
             const float rr2 = rsqrtf(warp_sum(dot4(y4, y4, 0.0f)) * (1.0f / DV) + a.norm_eps);
             const float4 zf = raw4_f(zcur);
-            const float4 o = make_float4(y4.x * rr2 * nw.x * silu_f(zf.x), y4.y * rr2 * nw.y * silu_f(zf.y),
-                                         y4.z * rr2 * nw.z * silu_f(zf.z), y4.w * rr2 * nw.w * silu_f(zf.w));
+            const float4 o = a.norm_w ? make_float4(y4.x * rr2 * nw.x * silu_f(zf.x), y4.y * rr2 * nw.y * silu_f(zf.y),
+                                                    y4.z * rr2 * nw.z * silu_f(zf.z), y4.w * rr2 * nw.w * silu_f(zf.w))
+                                      : y4;
             store4(static_cast<TO *>(a.out) + (b * T + t) * (size_t)DI + (size_t)(kh + HK * h) * DV + 4 * lane, o);
         }
         // the next prologue writes q/k/v/gate and the next sweep y only after a barrier

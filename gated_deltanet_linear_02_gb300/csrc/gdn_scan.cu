@@ -197,6 +197,14 @@ __global__ void __launch_bounds__(256) scan_norm_kernel(const float *__restrict_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     grid_dep_wait();                                   // y comes from the kernel ahead
     grid_dep_launch();
+    if (norm_w == nullptr) {                           // no norm weights: out is y itself
+#pragma unroll
+        for (int hh = 0; hh < HV / 8; ++hh) {
+            const size_t o = t * DI + (warp * (HV / 8) + hh) * DV + lane * 4;
+            store4(out + o, *reinterpret_cast<const float4 *>(ws.y + o));
+        }
+        return;
+    }
     const float4 w = *reinterpret_cast<const float4 *>(norm_w + lane * 4);
 #pragma unroll
     for (int hh = 0; hh < HV / 8; ++hh) {

@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_in_proj.argtypes = [_vp] * 6 + [_int, _int, _vp]
         L.gdn_out_proj.restype = _int
         L.gdn_out_proj.argtypes = [_vp, _vp, _vp, _int, _int, _vp]
+        L.gdn_gated_out_proj.restype = _int
+        L.gdn_gated_out_proj.argtypes = [_vp, ctypes.c_float, _vp, _vp, _vp, _vp, _int, _int, _int, _vp]
         L.gdn_prefill.restype = _int
         L.gdn_prefill.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 5 + [_int, _int] + [_vp] * 5 + \
             [_int, _int, _int, _vp, _sz, _vp]
@@ -220,6 +222,20 @@ def out_proj(x, w, y, stream=None):
     st = lib().gdn_out_proj(_ptr(x, "x", (M, DI), torch.bfloat16), _ptr(w, "w", (N_EMBD, DI), torch.bfloat16),
                             _ptr(y, "y", (M, N_EMBD)), M, od, _stream(stream))
     _check(st, "gdn_out_proj")
+
+
+def gated_out_proj(norm_w, norm_eps, y, z, w, out, stream=None):
+    """gdn_gated_out_proj: out = (gated RMSNorm(y) . silu(z)) w^T in one
+    tensor-core GEMM. y and z [M][4096] in the same dtype (fp32 or bf16; y is
+    the mixer's output with the norm left out), norm_w [128] fp32, w
+    [2048][4096] bf16, out [M][2048] fp32 or bf16."""
+    M = y.shape[0]
+    act = _act_dtype(y)
+    st = lib().gdn_gated_out_proj(_ptr(norm_w, "norm_w", (DV,), torch.float32), float(norm_eps),
+                                  _ptr(y, "y", (M, DI)), _ptr(z, "z", (M, DI), y.dtype),
+                                  _ptr(w, "w", (N_EMBD, DI), torch.bfloat16), _ptr(out, "out", (M, N_EMBD)),
+                                  M, act, _act_dtype(out), _stream(stream))
+    _check(st, "gdn_gated_out_proj")
 
 
 ATTN_HQ, ATTN_HKV, ATTN_D = 16, 2, 256   # GDN_ATTN_Q_HEADS, GDN_ATTN_KV_HEADS, GDN_ATTN_HEAD_DIM

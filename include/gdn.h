@@ -82,7 +82,11 @@ typedef struct {
     const float *A_log;    /* [32]; the decay uses -exp(A_log) (ssm_a)          */
     const float *dt_bias;  /* [32] (ssm_dt.bias)                                */
     const float *norm_w;   /* [128] (ssm_norm.weight), shared by all V-heads and
-                              applied as w, not 1 + w                          */
+                              applied as w, not 1 + w. NULL: the gated norm is
+                              left out and `out` receives the mixer's raw
+                              output y = scale * S^T q per head (z is not
+                              read), for gdn_gated_out_proj to apply the norm
+                              inside the output projection.                    */
     float norm_eps;        /* RMSNorm epsilon: y * (mean(y^2) + eps)^-1/2       */
     float l2_eps;          /* L2 epsilon: x * (sum(x^2) + eps)^-1/2             */
 } gdn_params;
@@ -261,6 +265,29 @@ gdn_status gdn_in_proj(const void *h, const void *w_in, void *qkv, void *z, void
  * that gives up is reported afterwards by gdn_device_error.
  */
 gdn_status gdn_out_proj(const void *x, const void *w, void *y, int M, gdn_dtype out_dt, void *stream);
+
+/*
+ * gdn_gated_out_proj -- the end of section "Output path" in one tensor-core
+ * GEMM: the gated RMSNorm . silu(z) of the mixer's raw output y, then
+ * cur = ssm_out . gated, 4096 -> GDN_HIDDEN (2048):
+ *   gated[m][h*128 + j] = y[m][h*128 + j] * r * norm_w[j] * silu(z[m][h*128 + j]),
+ *       r = (mean_j y[m][h*128 + j]^2 + norm_eps)^-1/2   (per row m and head h)
+ *   out[m][n] = sum_k gated[m][k] * w[n][k]
+ * The gated rows are formed inside the GEMM, as bf16 tensor-core operands
+ * (fp32 accumulation), and never written to memory.
+ *   norm_w [128] fp32 (ssm_norm.weight, applied as w)
+ *   y      [M][4096] act: the mixer's output with the norm left out, i.e.
+ *          gdn_decode_step / gdn_prefill called with params->norm_w == NULL
+ *   z      [M][4096] act
+ *   w      [2048][4096] bf16: ssm_out.weight, row-major
+ *   out    [M][2048] out_dt
+ * 0 <= M <= 2^24 (M == 0 is a no-op). All pointers 16-byte aligned. Errors:
+ * GDN_ERR_INVALID_ARG, GDN_ERR_CUDA (also when the driver's tensor-map encoder
+ * is unavailable). A bounded device wait that gives up is reported afterwards
+ * by gdn_device_error.
+ */
+gdn_status gdn_gated_out_proj(const float *norm_w, float norm_eps, const void *y, const void *z, const void *w,
+                              void *out, int M, gdn_dtype act, gdn_dtype out_dt, void *stream);
 
 /*
  * gdn_attn_decode -- decode attention of the full-attention layers, steps 5-6

@@ -105,3 +105,32 @@ def oracle_sequence_split_heads(lp, qkv, z, alpha, beta, conv0, S0_lib, groups=8
             S[h] = s[h]
             cs = c
     return out, cs, to_lib(S)
+
+
+def oracle_y_sequence(lp, qkv, alpha, beta, conv_state, S_lib):
+    """The mixer's raw output y = scale S^T q^ of every token and V-head of
+    one sequence (the gated norm left out), composed from the oracle's single
+    steps: conv + SiLU per token, the L2 norms, the gates, then the per-token
+    recurrence of each head over the sequence. S_lib is the library layout
+    [32][j][i]. Returns y [T][4096] in fp64."""
+    qkv, alpha, beta = f64(qkv), f64(alpha), f64(beta)
+    T = qkv.shape[0]
+    conv_w = f64(lp.conv_w)
+    st = f64(conv_state).copy()
+    xh = np.empty((T, qkv.shape[1]))
+    for t in range(T):
+        xh[t], st = oracle.conv_token(qkv[t], conv_w, st)
+    HV, HK, D = 32, 16, 128
+    S_page = to_page(f64(S_lib))
+    y = np.zeros((T, HV * D))
+    A_log, dt_bias = f64(lp.A_log), f64(lp.dt_bias)
+    for vh in range(HV):
+        kh = vh % HK
+        q = np.stack([oracle.l2norm(xh[t, kh * D:(kh + 1) * D], lp.l2_eps) for t in range(T)])
+        k = np.stack([oracle.l2norm(xh[t, 2048 + kh * D:2048 + (kh + 1) * D], lp.l2_eps) for t in range(T)])
+        v = xh[:, 4096 + vh * D:4096 + (vh + 1) * D]
+        gb = [oracle.gates(A_log[vh], dt_bias[vh], alpha[t, vh], beta[t, vh]) for t in range(T)]
+        g = np.array([x[0] for x in gb])
+        b = np.array([x[1] for x in gb])
+        y[:, vh * D:(vh + 1) * D], _ = oracle.delta_rule_scan(q, k, v, g, b, S_page[vh], 1.0 / np.sqrt(D))
+    return y
