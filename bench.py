@@ -91,6 +91,8 @@ TRAFFIC = {
                     per="gdn_in_proj call at M=4096"),
     "out_proj": dict(bytes=50_358_016 + 100_096, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                      per="gdn_out_proj call at M=4096"),
+    "gated_out_proj": dict(bytes=None, src="gdn_gated_proj.cu", sha="", profile="profiles/gated_proj_M4096.md",
+                           per="gdn_gated_out_proj call at M=4096"),
     "out_proj_batch": dict(bytes=18_900_224 + 0, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                            per="gdn_out_proj call at M=256"),
 }
@@ -400,7 +402,28 @@ def run_gpu(args, rank, world, dev):
         ob = I.N_EMBD * I.D_INNER * 2 + M * I.D_INNER * 2 + M * I.N_EMBD * 2
         op[M] = dict(us=ms * 1e3, tflops=2.0 * M * I.D_INNER * I.N_EMBD / (ms / 1e3) / 1e12,
                      bytes=ob, gbs=ob / (ms / 1e3) / 1e9)
-        del xo, yo
+        # the same projection with the gated norm formed inside the GEMM
+        # (gdn_gated_out_proj), from the mixer's y and z
+        zo = torch.randn(M, I.D_INNER, device=dev).to(torch.bfloat16)
+        for _ in range(args.warmup):
+            ops.gated_out_proj(lp.norm_w, lp.norm_eps, xo, zo, w_out, yo)
+        barrier_sync()
+        times = []
+        t_wall0 = time.time()
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ops.gated_out_proj(lp.norm_w, lp.norm_eps, xo, zo, w_out, yo)
+            b.record(stream)
+            times.append((a, b))
+        barrier_sync()
+        sampler.mark(t_wall0, time.time())
+        gms = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times))
+        gb = ob + M * I.D_INNER * 2
+        op[M]["gated"] = dict(us=gms * 1e3, tflops=2.0 * M * I.D_INNER * I.N_EMBD / (gms / 1e3) / 1e12,
+                              bytes=gb, gbs=gb / (gms / 1e3) / 1e9)
+        del xo, yo, zo
     # ---------------- input projections (gdn_in_proj) at the prefill size
     w_in = torch.cat(I.in_proj_weights(I.seed_of(2), device=dev), dim=0)
     h_in = torch.randn(PREFILL_T, I.N_EMBD, device=dev).to(torch.bfloat16)
@@ -817,6 +840,7 @@ def main():
     ip_tr, ip_tr_note = traffic("in_proj")
     op_tr, op_tr_note = traffic("out_proj")
     opb_tr, opb_tr_note = traffic("out_proj_batch")
+    gp_tr, gp_tr_note = traffic("gated_out_proj")
     PREFILL_BYTES = PREFILL_T * PREFILL_IO_BYTES_PER_TOKEN + PREFILL_END_STATE_BYTES + PREFILL_PARAM_BYTES
     pf_gbs = PREFILL_BYTES / (r["pf_ms"] / 1e3) / 1e9
     line = {
@@ -865,6 +889,16 @@ def main():
                                   "hbm_frac": r["op"][PREFILL_T]["gbs"] / r["hbm_peak"],
                                   "algorithmic_bytes_per_call": r["op"][PREFILL_T]["bytes"],
                                   "traffic": op_tr, "traffic_source": op_tr_note},
+                     "gated_out_proj": {
+                         "op": "out = (gated RMSNorm(y) . silu(z)) w^T, the norm formed inside the GEMM",
+                         "us_per_call": {str(m): r["op"][m]["gated"]["us"] for m in (PREFILL_T, BATCH)},
+                         "roofline": {"bound": "tensor", "achieved": r["op"][PREFILL_T]["gated"]["tflops"],
+                                      "peak": r["tc_peak"], "unit": "TFLOP/s",
+                                      "frac": r["op"][PREFILL_T]["gated"]["tflops"] / r["tc_peak"],
+                                      "hbm_achieved_GBs": r["op"][PREFILL_T]["gated"]["gbs"],
+                                      "hbm_frac": r["op"][PREFILL_T]["gated"]["gbs"] / r["hbm_peak"],
+                                      "algorithmic_bytes_per_call": r["op"][PREFILL_T]["gated"]["bytes"],
+                                      "traffic": gp_tr, "traffic_source": gp_tr_note}},
                      "decode_batch": {"M": BATCH, "us_per_call": r["op"][BATCH]["us"],
                                       "roofline": {"bound": "hbm", "achieved": r["op"][BATCH]["gbs"],
                                                    "peak": r["hbm_peak"], "unit": "GB/s",
