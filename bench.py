@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tok/s @T=4096; decode tok/s @B=256; % of HBM/TC roofline"
+I_C_CONV = 8192             # q|k|v conv channels
 LAYERS, BATCH, PREFILL_T, CHUNK = 30, 256, 4096, 64
 NOMINAL_HBM_GBS = 8000.0
 
@@ -446,6 +447,41 @@ def run_gpu(args, rank, world, dev):
     ip_bytes = (PREFILL_T * I.N_EMBD + w_in.shape[0] * I.N_EMBD + PREFILL_T * w_in.shape[0]) * 2
     ip = dict(us=ip_ms * 1e3, tflops=2.0 * PREFILL_T * w_in.shape[0] * I.N_EMBD / (ip_ms / 1e3) / 1e12,
               bytes=ip_bytes, gbs=ip_bytes / (ip_ms / 1e3) / 1e9)
+    # ---------------- projections + mixer at T=4096: gdn_in_proj then gdn_prefill, against
+    #                  gdn_in_proj_conv (conv, SiLU and q/k norms in the GEMM's epilogue)
+    #                  then gdn_prefill_xhat; L2 flushed between calls
+    xh = torch.empty(PREFILL_T, I.C_CONV, dtype=torch.float16, device=dev)
+
+    def unfused():
+        ops.in_proj(h_in, w_in, *outs_in)
+        ops.prefill(None, outs_in[0], outs_in[1], outs_in[2], outs_in[3], cu, out, None, cs_out, None, S_out,
+                    chunk_size=0, workspace=ws, cparams=cp)
+
+    def fused():
+        ops.in_proj_conv(None, h_in, w_in, cu, xh, outs_in[1], outs_in[2], outs_in[3], conv_state_out=cs_out,
+                         cparams=cp)
+        ops.prefill_xhat(None, xh, outs_in[1], outs_in[2], outs_in[3], cu, out, ssm_state_out=S_out, workspace=ws,
+                         cparams=cp)
+
+    f2 = {}
+    for name, fn in (("unfused", unfused), ("fused", fused)):
+        for _ in range(args.warmup):
+            fn()
+        barrier_sync()
+        times = []
+        t_wall0 = time.time()
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            times.append((a, b))
+        barrier_sync()
+        sampler.mark(t_wall0, time.time())
+        f2[name] = max_over_ranks(sum(a.elapsed_time(b) for a, b in times) / len(times)) * 1e3
+    assert ops.device_error() == ops.GDN_OK
+    del xh
     del w_in, h_in, outs_in
     assert ops.device_error() == ops.GDN_OK
     torch.cuda.empty_cache()
@@ -479,7 +515,7 @@ def run_gpu(args, rank, world, dev):
                          hbm_peak, tc_peak)
     clocks = sampler.stop()
 
-    return dict(cfgs=cfgs, at=at, ip=ip, op=op, mt=mt, mts=mts, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
+    return dict(cfgs=cfgs, at=at, ip=ip, op=op, mt=mt, mts=mts, f2=f2, dec_ms=dec_ms, dec_tok_s=dec_tok_s, achieved=achieved, per_launch_s=per_launch_s,
                 bytes_per_launch=bytes_per_launch, launches=launches, e2e_tok_s=e2e_tok_s, e2e_ms=e2e_ms,
                 h2d=h2d, d2h=d2h, pf_ms=pf_ms, pf_tok_s=pf_tok_s, pf_tflops=pf_tflops, hbm_peak=hbm_peak,
                 tc_peak=tc_peak, peak_src=peak_src, clocks=clocks)
@@ -881,6 +917,14 @@ def main():
                                  "hbm_achieved_GBs": r["ip"]["gbs"], "hbm_frac": r["ip"]["gbs"] / r["hbm_peak"],
                                  "algorithmic_bytes_per_call": r["ip"]["bytes"],
                                  "traffic": ip_tr, "traffic_source": ip_tr_note}},
+        "in_proj_conv_prefill": {
+            "workload": f"input_projections_and_prefill_T{PREFILL_T}_bf16",
+            "op": "h -> qkv|z|alpha|beta -> mixer output: gdn_in_proj + gdn_prefill against "
+                  "gdn_in_proj_conv (conv, SiLU, q/k norms in the GEMM epilogue) + gdn_prefill_xhat",
+            "us_per_call_unfused": r["f2"]["unfused"], "us_per_call_fused": r["f2"]["fused"],
+            "hbm_bytes_saved_per_call": 2 * PREFILL_T * I_C_CONV * 2,
+            "bytes_saved": "the raw q|k|v stream [T][8192] bf16, written by the projection and read back "
+                           "by the mixer's conv", "l2": "flushed between timed calls"},
         "out_proj": {"workload": f"ssm_out_projection_M{PREFILL_T}_bf16", "op": "y = x w^T, 4096 -> 2048",
                      "us_per_call": r["op"][PREFILL_T]["us"], "l2": "flushed between timed calls",
                      "roofline": {"bound": "tensor", "achieved": r["op"][PREFILL_T]["tflops"], "peak": r["tc_peak"],

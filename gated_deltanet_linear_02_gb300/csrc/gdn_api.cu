@@ -31,8 +31,12 @@ size_t chunk_workspace_bytes(int N, int T_total);
 size_t chunk_min_workspace_bytes(int N);
 cudaError_t launch_prefill_chunked(const gdn_params *, const void *, const void *, const void *, const void *,
                                    const int32_t *, int, int, const void *, void *, const float *, float *, void *,
-                                   gdn_dtype, void *, size_t, cudaStream_t);
+                                   gdn_dtype, void *, size_t, cudaStream_t, const void *xhat_ext);
 void *chunk_error_word();
+cudaError_t launch_in_proj_conv(const float *conv_w, float l2_eps, const void *h, const void *w_in,
+                                const int32_t *cu, int N, int M, const void *cs_in, void *cs_out, void *xhat,
+                                void *z, void *alpha, void *beta, cudaStream_t s);
+void *inconv_error_word();
 size_t attn_workspace_bytes(int B, int Lmax);
 cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *ctx_len,
                                const void *z, void *out, int B, int Lmax, void *ws, gdn_dtype out_dt,
@@ -96,7 +100,7 @@ namespace gdn {
 // clears all of them with one small kernel (an atomic exchange each, so a word
 // set while the call runs is either reported now or kept for the next call)
 // and one copy of the OR back to the host.
-constexpr int N_ERROR_WORDS = 7;
+constexpr int N_ERROR_WORDS = 8;
 struct ErrorWords {
     unsigned int *p[N_ERROR_WORDS];
 };
@@ -126,7 +130,7 @@ static bool error_words(ErrorWords *out)
     if (!have[dev]) {
         void *(*const fns[N_ERROR_WORDS])() = {decode_error_word, chunk_error_word,    multi_error_word,
                                                gemm_error_word,   attn_error_word,     selftest_error_word,
-                                               gproj_error_word};
+                                               gproj_error_word,  inconv_error_word};
         for (int i = 0; i < N_ERROR_WORDS; ++i) {
             cache[dev].p[i] = static_cast<unsigned int *>(fns[i]());
             if (cache[dev].p[i] == nullptr) return false;
@@ -325,8 +329,68 @@ gdn_status gdn_prefill(const gdn_params *p, const void *qkv, const void *z, cons
                                 ssm_state_in, ssm_state_out, out, act, out_dt, body, s);
     else
         e = launch_prefill_chunked(p, qkv, z, alpha, beta, cu_seqlens, N, T_total, conv_state_in, conv_state_out,
-                                   ssm_state_in, ssm_state_out, out, out_dt, body, ws_bytes - WS_HEADER, s);
+                                   ssm_state_in, ssm_state_out, out, out_dt, body, ws_bytes - WS_HEADER, s, nullptr);
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_prefill");
+}
+
+gdn_status gdn_in_proj_conv(const gdn_params *p, const void *h, const void *w_in, const int32_t *cu_seqlens, int N,
+                            int M, const void *conv_state_in, void *conv_state_out, void *xhat, void *z,
+                            void *alpha, void *beta, void *stream)
+{
+    if (N < 0 || N > MAX_N) return fail(GDN_ERR_INVALID_ARG, "N out of range [0, 65535]");
+    if (M < 0 || M > MAX_T) return fail(GDN_ERR_INVALID_ARG, "M out of range [0, 2^24]");
+    if (N == 0) {
+        if (M != 0) return fail(GDN_ERR_INVALID_ARG, "M > 0 with no sequences");
+        return GDN_OK;
+    }
+    if (p == nullptr || !ok_ptr(p->conv_w) || !(p->l2_eps >= 0.0f))
+        return fail(GDN_ERR_INVALID_ARG, "params NULL, conv_w NULL or misaligned, or l2_eps < 0");
+    if (!ok_ptr(cu_seqlens) || (M > 0 && (!ok_ptr(h) || !ok_ptr(w_in) || !ok_ptr(xhat) || !ok_ptr(z) ||
+                                          !ok_ptr(alpha) || !ok_ptr(beta))))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    if (!ok_opt_ptr(conv_state_in) || !ok_opt_ptr(conv_state_out))
+        return fail(GDN_ERR_INVALID_ARG, "a state pointer is not 16-byte aligned");
+    const size_t cs_bytes = (size_t)N * (GDN_CONV_K - 1) * GDN_CONV_CHANNELS * 2;
+    if (conv_state_in && conv_state_out) {
+        const char *i0 = static_cast<const char *>(conv_state_in), *o0 = static_cast<const char *>(conv_state_out);
+        if (i0 < o0 + cs_bytes && o0 < i0 + cs_bytes)
+            return fail(GDN_ERR_INVALID_ARG, "conv_state_in and conv_state_out overlap");
+    }
+    cudaError_t e = launch_in_proj_conv(p->conv_w, p->l2_eps, h, w_in, cu_seqlens, N, M, conv_state_in,
+                                        conv_state_out, xhat, z, alpha, beta, (cudaStream_t)stream);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_in_proj_conv");
+}
+
+gdn_status gdn_prefill_xhat(const gdn_params *p, const void *xhat, const void *z, const void *alpha,
+                            const void *beta, const int32_t *cu_seqlens, int N, int T_total,
+                            const float *ssm_state_in, float *ssm_state_out, void *out, gdn_dtype out_dt,
+                            void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!ok_dtype(out_dt)) return fail(GDN_ERR_INVALID_ARG, "unknown dtype");
+    if (N < 0 || N > MAX_N) return fail(GDN_ERR_INVALID_ARG, "N out of range [0, 65535]");
+    if (T_total < 0 || T_total > MAX_T) return fail(GDN_ERR_INVALID_ARG, "T_total out of range [0, 2^24]");
+    if (N == 0) {
+        if (T_total != 0) return fail(GDN_ERR_INVALID_ARG, "T_total > 0 with no sequences");
+        return GDN_OK;
+    }
+    gdn_status st = check_params(p);
+    if (st != GDN_OK) return st;
+    if (!ok_ptr(cu_seqlens) || (T_total > 0 && (!ok_ptr(xhat) || !ok_ptr(z) || !ok_ptr(alpha) || !ok_ptr(beta) ||
+                                                !ok_ptr(out))))
+        return fail(GDN_ERR_INVALID_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    if (!ok_opt_ptr(ssm_state_in) || !ok_opt_ptr(ssm_state_out))
+        return fail(GDN_ERR_INVALID_ARG, "a state pointer is not 16-byte aligned");
+    const size_t need = WS_HEADER + ((chunk_min_workspace_bytes(N) + 255) & ~(size_t)255);
+    if (workspace == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+        snprintf(g_last_error, sizeof(g_last_error),
+                 "workspace missing, misaligned (256 B) or too small: %zu bytes given, %zu needed", ws_bytes, need);
+        return GDN_ERR_WORKSPACE;
+    }
+    void *body = static_cast<char *>(workspace) + WS_HEADER;
+    cudaError_t e = launch_prefill_chunked(p, nullptr, z, alpha, beta, cu_seqlens, N, T_total, nullptr, nullptr,
+                                           ssm_state_in, ssm_state_out, out, out_dt, body, ws_bytes - WS_HEADER,
+                                           (cudaStream_t)stream, xhat);
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_prefill_xhat");
 }
 
 gdn_status gdn_device_error(void *stream)

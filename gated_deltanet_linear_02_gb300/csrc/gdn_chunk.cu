@@ -122,6 +122,7 @@ struct WyArgs {
     WyFrag *frags;
     WyChunk *chunks;
     __half *xhat;                // [wlen][8192]
+    int gates_only;              // x^ comes from the caller (gdn_in_proj_conv): act writes the gates only
     __half *ybuf;                // [wlen][4096]: y (scale applied) before the gated norm
     float *gates;                // [c_cap][32][4][64]: per (chunk, V-head) G, beta, gamma_t, exp(G_n - G_t)
     unsigned char *blobs;        // [c_cap][32] x BLOB_BYTES
@@ -260,6 +261,7 @@ __global__ void __launch_bounds__(ACT_THREADS) wy_act_kernel(const WyArgs a)
             rec[GR_KTF + p] = p < ck.nv ? __expf(Gn - Gp) : 0.0f;
         }
     }
+    if (a.gates_only) return;
     const int c0 = blockIdx.y * DK + 4 * lane;
     const int tb = 8 * tg;                             // first token (uniform over the warp)
     if (tb >= ck.nv) return;
@@ -1203,7 +1205,7 @@ static cudaError_t wy_setup()
 cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const void *z, const void *alpha,
                                    const void *beta, const int32_t *cu, int N, int T_total, const void *cs_in,
                                    void *cs_out, const float *S_in, float *S_out, void *out, gdn_dtype out_dt,
-                                   void *ws_body, size_t ws_bytes, cudaStream_t s)
+                                   void *ws_body, size_t ws_bytes, cudaStream_t s, const void *xhat_ext)
 {
     cudaError_t e = wy_setup();
     if (e != cudaSuccess) return e;
@@ -1226,6 +1228,7 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
         a.chunks = reinterpret_cast<WyChunk *>(ws + L.chunks);
         a.gates = reinterpret_cast<float *>(ws + L.gates);
         a.xhat = reinterpret_cast<__half *>(ws + L.xhat);
+        a.gates_only = xhat_ext != nullptr;
         a.ybuf = reinterpret_cast<__half *>(ws + L.ybuf);
         a.blobs = ws + L.blobs;
         float *slots = reinterpret_cast<float *>(ws + L.slots);
@@ -1236,12 +1239,16 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
             a.slot_in = slots + (size_t)((wi + 1) & 1) * HV * DV * DK;
             a.slot_out = slots + (size_t)(wi & 1) * HV * DV * DK;
             CUtensorMap xmap;                          // x^ rows of this window; rows past it read as zero
-            if (!make_bf16_sw128_map(&xmap, a.xhat, a.wlen, CC, CH)) return cudaErrorInvalidValue;
+            const void *xrows = xhat_ext ? static_cast<const void *>(static_cast<const __half *>(xhat_ext) +
+                                                                     (size_t)w0 * CC)
+                                         : static_cast<const void *>(a.xhat);
+            if (!make_bf16_sw128_map(&xmap, xrows, a.wlen, CC, CH)) return cudaErrorInvalidValue;
             // Each kernel is launched with programmatic stream serialization and waits
             // (grid_dep_wait) before it touches what the kernel ahead writes.
             e = launch_pdl(wy_plan_kernel, dim3(1), dim3(1024), 0, s, a);
             if (e == cudaSuccess)
-                e = launch_pdl(wy_act_kernel, dim3((unsigned)L.c_cap, CC / DK), dim3(ACT_THREADS), 0, s, a);
+                e = launch_pdl(wy_act_kernel, dim3((unsigned)L.c_cap, xhat_ext ? HK : CC / DK), dim3(ACT_THREADS), 0,
+                               s, a);
             if (e == cudaSuccess)
                 e = launch_pdl(wy_prep_kernel, dim3((unsigned)std::min(L.c_cap * HK, n_sm)), dim3(PR_THREADS),
                                PR_SMEM, s, xmap, a);

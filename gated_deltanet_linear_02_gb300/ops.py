@@ -60,6 +60,11 @@ def lib() -> ctypes.CDLL:
         L.gdn_in_proj.argtypes = [_vp] * 6 + [_int, _int, _vp]
         L.gdn_out_proj.restype = _int
         L.gdn_out_proj.argtypes = [_vp, _vp, _vp, _int, _int, _vp]
+        L.gdn_in_proj_conv.restype = _int
+        L.gdn_in_proj_conv.argtypes = [ctypes.POINTER(gdn_params), _vp, _vp, _vp, _int, _int] + [_vp] * 6 + [_vp]
+        L.gdn_prefill_xhat.restype = _int
+        L.gdn_prefill_xhat.argtypes = [ctypes.POINTER(gdn_params)] + [_vp] * 5 + [_int, _int] + [_vp] * 3 + \
+            [_int, _vp, _sz, _vp]
         L.gdn_gated_out_proj.restype = _int
         L.gdn_gated_out_proj.argtypes = [_vp, ctypes.c_float, _vp, _vp, _vp, _vp, _int, _int, _int, _vp]
         L.gdn_prefill.restype = _int
@@ -222,6 +227,48 @@ def out_proj(x, w, y, stream=None):
     st = lib().gdn_out_proj(_ptr(x, "x", (M, DI), torch.bfloat16), _ptr(w, "w", (N_EMBD, DI), torch.bfloat16),
                             _ptr(y, "y", (M, N_EMBD)), M, od, _stream(stream))
     _check(st, "gdn_out_proj")
+
+
+def in_proj_conv(params, h, w_in, cu_seqlens, xhat, z, alpha, beta, conv_state_in=None, conv_state_out=None,
+                 stream=None, cparams: gdn_params | None = None):
+    """gdn_in_proj_conv: the input projections with the conv, SiLU and q/k L2
+    norms in the GEMM's epilogue (h [M][2048] bf16, w_in [12352][2048] bf16)
+    into xhat [M][8192] fp16, z [M][4096], alpha/beta [M][32] bf16, and
+    conv_state_out [N][3][8192] bf16."""
+    M = h.shape[0]
+    N = cu_seqlens.shape[0] - 1
+    cp = cparams if cparams is not None else make_params(params)
+    st = lib().gdn_in_proj_conv(ctypes.byref(cp), _ptr(h, "h", (M, N_EMBD), torch.bfloat16),
+                                _ptr(w_in, "w_in", (IN_PROJ_ROWS, N_EMBD), torch.bfloat16),
+                                _ptr(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32), N, M,
+                                _ptr(conv_state_in, "conv_state_in", (N, KC - 1, CC), torch.bfloat16),
+                                _ptr(conv_state_out, "conv_state_out", (N, KC - 1, CC), torch.bfloat16),
+                                _ptr(xhat, "xhat", (M, CC), torch.float16), _ptr(z, "z", (M, DI), torch.bfloat16),
+                                _ptr(alpha, "alpha", (M, HV), torch.bfloat16), _ptr(beta, "beta", (M, HV), torch.bfloat16),
+                                _stream(stream))
+    _check(st, "gdn_in_proj_conv")
+
+
+def prefill_xhat(params, xhat, z, alpha, beta, cu_seqlens, out, ssm_state_in=None, ssm_state_out=None,
+                 workspace=None, stream=None, cparams: gdn_params | None = None):
+    """gdn_prefill_xhat: the chunked prefill from gdn_in_proj_conv's activations.
+    Allocates the workspace through torch when none is given."""
+    T = xhat.shape[0]
+    N = cu_seqlens.shape[0] - 1
+    if workspace is None:
+        workspace = torch.empty(max(prefill_workspace_size(N, T, torch.bfloat16, 64), 256), dtype=torch.uint8,
+                                device=xhat.device)
+    cp = cparams if cparams is not None else make_params(params)
+    st = lib().gdn_prefill_xhat(ctypes.byref(cp), _ptr(xhat, "xhat", (T, CC), torch.float16),
+                                _ptr(z, "z", (T, DI), torch.bfloat16), _ptr(alpha, "alpha", (T, HV), torch.bfloat16),
+                                _ptr(beta, "beta", (T, HV), torch.bfloat16),
+                                _ptr(cu_seqlens, "cu_seqlens", (N + 1,), torch.int32), N, T,
+                                _ptr(ssm_state_in, "ssm_state_in", (N, HV, DV, DK), torch.float32),
+                                _ptr(ssm_state_out, "ssm_state_out", (N, HV, DV, DK), torch.float32),
+                                _ptr(out, "out", (T, DI)), _act_dtype(out), _ptr(workspace, "workspace"),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "gdn_prefill_xhat")
+    return workspace
 
 
 def gated_out_proj(norm_w, norm_eps, y, z, w, out, stream=None):

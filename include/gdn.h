@@ -250,6 +250,45 @@ gdn_status gdn_in_proj(const void *h, const void *w_in, void *qkv, void *z, void
                        gdn_dtype act, void *stream);
 
 /*
+ * gdn_in_proj_conv -- the input projections of gdn_in_proj with the causal
+ * conv1d, SiLU and the q/k L2 norms ("Projections", "Causal conv1d" and the
+ * split of section "SSM block -- Gated-Delta-Net") applied in the GEMM's
+ * epilogue, so the raw q|k|v stream is never written. Over packed sequences
+ * (cu_seqlens as for gdn_prefill):
+ *   qkv = h w_qkv^T (fp32, not stored)
+ *   xhat[m][c] = SiLU(sum_k conv_w[c][k] win_k[c]), win = the three inputs
+ *       before m in its sequence (conv_state_in rows before the sequence's
+ *       start, zeros without it) and qkv[m]; then each q and k head of 128
+ *       channels divided by sqrt(sum of squares + l2_eps)
+ *   z, alpha, beta = the other projections, rounded to bf16
+ *   conv_state_out[n] = the raw inputs at the sequence's last three positions
+ *       (rows of conv_state_in for positions before its start), bf16
+ *   p          conv_w and l2_eps are read (the other fields are not)
+ *   h          [M][2048] bf16;  w_in [12352][2048] bf16 (as gdn_in_proj)
+ *   cu_seqlens device int32 [N+1], 0 = cu[0] <= ... <= cu[N] = M
+ *   conv_state_in, conv_state_out  [N][3][8192] bf16, each may be NULL; they
+ *              must not overlap
+ *   xhat       [M][8192] fp16: the input gdn_prefill_xhat takes
+ *   z [M][4096], alpha [M][32], beta [M][32] bf16
+ * Errors: GDN_ERR_INVALID_ARG, GDN_ERR_CUDA.
+ */
+gdn_status gdn_in_proj_conv(const gdn_params *p, const void *h, const void *w_in, const int32_t *cu_seqlens, int N,
+                            int M, const void *conv_state_in, void *conv_state_out, void *xhat, void *z,
+                            void *alpha, void *beta, void *stream);
+
+/*
+ * gdn_prefill_xhat -- gdn_prefill (chunked tensor-core form, bf16) starting
+ * from the activations gdn_in_proj_conv writes: xhat replaces qkv and its
+ * conv, and conv_state is not touched (gdn_in_proj_conv has advanced it).
+ * Arguments, workspace (gdn_prefill_workspace_size(N, T_total, GDN_BF16, 64)
+ * or any size down to one 64-token window) and errors as gdn_prefill.
+ */
+gdn_status gdn_prefill_xhat(const gdn_params *p, const void *xhat, const void *z, const void *alpha,
+                            const void *beta, const int32_t *cu_seqlens, int N, int T_total,
+                            const float *ssm_state_in, float *ssm_state_out, void *out, gdn_dtype out_dt,
+                            void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * gdn_out_proj -- the projection right after the mixer, section "Output path":
  * cur = ssm_out . gated, 4096 -> GDN_HIDDEN (2048). It computes
  *   y[m][n] = sum_k x[m][k] * w[n][k]
