@@ -61,7 +61,7 @@ def test_attention_and_prefill_replay_from_a_cuda_graph(ops):
     ops.attn_decode(a.q, a.k_cache, a.v_cache, a.ctx_len, a.z, out_e, workspace=ws)
     lp = I.layer_params(I.seed_of(42)).to(DEV)
     cp = ops.make_params(lp)
-    lens = [100, 37]
+    lens = [1500, 837]            # longer than one 1024-token window: two window sets on two streams
     st = I.streams(42, sum(lens), torch.bfloat16, device=DEV)
     cu = I.cu_seqlens(lens).to(DEV)
     pws = torch.empty(ops.prefill_workspace_size(2, sum(lens), torch.bfloat16, 0), dtype=torch.uint8, device=DEV)
