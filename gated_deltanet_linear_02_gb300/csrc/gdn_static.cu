@@ -79,3 +79,5 @@ extern "C" gdn_status gdn_prefill_static(const gdn_params *p, const void *qkv, c
                        ssm_state_out, out, act, out_dt, chunk_size, scratch, (size_t)GDN_STATIC_SCRATCH_BYTES,
                        stream);
 }
+
+extern "C" size_t gdn_static_scratch_bytes(void) { return (size_t)GDN_STATIC_SCRATCH_BYTES; }

@@ -358,7 +358,14 @@ def selftest_wait_timeout(stream=None) -> None:
     _check(lib().gdn_selftest_wait_timeout(_stream(stream)), "gdn_selftest_wait_timeout")
 
 
-STATIC_SCRATCH_BYTES = 64 << 20
+def static_scratch_bytes() -> int:
+    """Bytes of the fixed scratch gdn_prefill_static uses, from the library."""
+    L = lib()
+    L.gdn_static_scratch_bytes.restype = _sz
+    L.gdn_static_scratch_bytes.argtypes = []
+    return int(L.gdn_static_scratch_bytes())
+
+
 DECODE_MAX_T = 8   # GDN_DECODE_MAX_T: tokens per sequence of gdn_decode_multi, at most
 
 

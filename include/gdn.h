@@ -231,6 +231,10 @@ gdn_status gdn_prefill_static(const gdn_params *p, const void *qkv, const void *
                               const float *ssm_state_in, float *ssm_state_out, void *out,
                               gdn_dtype act, gdn_dtype out_dt, int chunk_size, void *stream);
 
+/* Bytes of the fixed scratch gdn_prefill_static uses (GDN_STATIC_SCRATCH_BYTES
+ * of the built library). Pure host arithmetic. */
+size_t gdn_static_scratch_bytes(void);
+
 /*
  * gdn_in_proj -- the four input projections of section "SSM block --
  * Gated-Delta-Net", from the normed hidden state: attn_qkv -> qkv [8192],

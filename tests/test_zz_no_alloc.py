@@ -96,7 +96,7 @@ def test_static_long_prompt_runs_in_windows(ops):
     # window; the chunked form runs it as several windows with the state
     # carried, and gives what gdn_prefill gives with a full-size workspace.
     full = ops.prefill_workspace_size(1, 4096, torch.bfloat16, 0)
-    assert full > ops.STATIC_SCRATCH_BYTES
+    assert full > ops.static_scratch_bytes()
     lp, st, cu, conv0, S0 = _case(4104, [4096], torch.bfloat16)
     ref = _run(ops, ops.prefill, lp, st, cu, conv0, S0, 0)
     got = _run(ops, ops.prefill_static, lp, st, cu, conv0, S0, 0)
@@ -108,7 +108,7 @@ def test_static_refuses_oversized_request(ops):
     # the exact scan keeps all of its tokens in scratch: 4096 fp32 tokens need
     # about 200 MB, more than the static scratch holds
     need = ops.prefill_workspace_size(1, 4096, torch.float32, 1)
-    assert need > ops.STATIC_SCRATCH_BYTES
+    assert need > ops.static_scratch_bytes()
     lp, st, cu, conv0, S0 = _case(4105, [4096], torch.float32)
     out, cs, S = _outputs(4096, 1, torch.float32)
     with pytest.raises(ops.GdnError) as err:
