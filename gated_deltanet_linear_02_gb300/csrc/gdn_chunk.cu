@@ -94,10 +94,11 @@ __host__ __device__ __forceinline__ uint32_t mn_off(int t, int c) { return tc::m
 // (r, s) of a K-major fp16 tile with 64 columns
 __host__ __device__ __forceinline__ uint32_t km64(int r, int s) { return tc::kmajor_offset<2>(r, s, 64); }
 
-// silu(z) = z sigmoid(z) = z (1 + tanh(z / 2)) / 2 for the output gate, with the
-// hardware tanh approximation (one special-function operation instead of an
-// exponential and a reciprocal; absolute error about 5e-4 on tanh, so about
-// 2.5e-4 |z| on silu(z), far below the output tolerance).
+// silu(z) = z sigmoid(z) = z (1 + tanh(z / 2)) / 2, for the conv outputs and the
+// output gate, with the hardware tanh approximation (one special-function
+// operation instead of an exponential and a reciprocal; absolute error about
+// 5e-4 on tanh, so about 2.5e-4 |z| on silu(z), below the fp16 rounding of x^
+// and far below the output tolerance).
 __device__ __forceinline__ float silu_gate(float z)
 {
     float th;
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(ACT_THREADS) wy_act_kernel(const WyArgs a)
         for (int e = 0; e < 4; ++e) {
             const float u = w[e][0] * chan(t, e) + w[e][1] * chan(t + 1, e) + w[e][2] * chan(t + 2, e) +
                             w[e][3] * chan(t + 3, e);
-            o[e] = silu_fast(u);
+            o[e] = silu_gate(u);                       // one special-function operation (tanh)
             s2 += o[e] * o[e];
         }
         if (norm) {
