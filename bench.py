@@ -78,22 +78,26 @@ PREFILL_PARAM_BYTES = 131_840
 # describe the kernel that ran. The summaries under profiles/ give the
 # commands and the per-kernel split.
 TRAFFIC = {
-    "decode": dict(bytes=555_963_648 + 490_369_536, src="gdn_decode.cu", sha="99381d2bf3475be0", profile="profiles/decode_step_kernel_B256.md",
+    "decode": dict(bytes=555_943_936 + 490_274_304, src="gdn_decode.cu", sha="76721eb1da31064e", profile="profiles/decode_step_kernel_B256.md",
                    per="launch of decode_step_kernel at B=256"),
     "attn": dict(bytes=2_168_676_864 + 18_318_080, src="gdn_attn.cu", sha="c68c58d38f8812f9", profile="profiles/attn_decode_B256_ctx4096.md",
                  per="call (attn_block_kernel + attn_combine_kernel) at B=256, ctx 4096"),
-    "multi": dict(bytes=574_938_112 + 495_531_520, src="gdn_decode_multi.cu", sha="a78ad87764f2cd50", profile="profiles/decode_multi_kernel_B256_T4.md",
+    "multi": dict(bytes=574_927_360 + 495_363_328, src="gdn_decode_multi.cu", sha="9724c9ac6f3ea2aa", profile="profiles/decode_multi_kernel_B256_T4.md",
                   per="launch of decode_multi_kernel at B=256, T=4"),
-    "prefill": dict(bytes=355_513_344 + 124_455_168, src="gdn_chunk.cu", sha="31a2a1c8a298dbf3", profile="profiles/chunk_prefill_T4096.md",
+    "prefill": dict(bytes=355_511_296 + 124_768_512, src="gdn_chunk.cu", sha="912edb772ce70df0", profile="profiles/chunk_prefill_T4096.md",
                     per="gdn_prefill call at T=4096 (all of its kernels)"),
-    "varlen": dict(bytes=6_169_908_224 + 2_179_091_968, src="gdn_chunk.cu", sha="31a2a1c8a298dbf3", profile="profiles/chunk_prefill_varlen8.md",
+    "varlen": dict(bytes=6_169_870_080 + 2_176_316_160, src="gdn_chunk.cu", sha="912edb772ce70df0", profile="profiles/chunk_prefill_varlen8.md",
                    per="gdn_prefill call on the 8-sequence varlen workload (all of its kernels)"),
     "in_proj": dict(bytes=109_801_728 + 76_413_184, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                     per="gdn_in_proj call at M=4096"),
     "out_proj": dict(bytes=50_358_016 + 100_096, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                      per="gdn_out_proj call at M=4096"),
-    "gated_out_proj": dict(bytes=None, src="gdn_gated_proj.cu", sha="", profile="profiles/gated_proj_M4096.md",
+    "gated_out_proj": dict(bytes=83_935_232 + 2_999_040, src="gdn_gated_proj.cu", sha="459ac59685a98db4",
+                           profile="profiles/gated_proj_M4096.md",
                            per="gdn_gated_out_proj call at M=4096"),
+    "in_proj_conv_prefill": dict(bytes=404_716_032 + 182_607_616, src=("gdn_in_conv.cu", "gdn_chunk.cu"),
+                                 sha="e607605762e19931", profile="profiles/in_proj_conv_T4096.md",
+                                 per="gdn_in_proj_conv + gdn_prefill_xhat at T=4096 (all of their kernels)"),
     "out_proj_batch": dict(bytes=18_900_224 + 0, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                            per="gdn_out_proj call at M=256"),
 }
@@ -104,10 +108,13 @@ def traffic(key):
     is the one the counters were taken on."""
     import hashlib
     t = TRAFFIC[key]
-    path = os.path.join(ROOT, "gated_deltanet_linear_02_gb300", "csrc", t["src"])
+    srcs = t["src"] if isinstance(t["src"], tuple) else (t["src"],)
+    h = hashlib.sha256()
     try:
-        with open(path, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        for src in srcs:                              # one hash over the sources, in order
+            with open(os.path.join(ROOT, "gated_deltanet_linear_02_gb300", "csrc", src), "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()[:16]
     except OSError:
         sha = None
     if t["bytes"] is None:
@@ -712,7 +719,9 @@ def profile_case(args):
     sequence of --T tokens; ``--case out_proj`` / ``--case in_proj``: the
     projection GEMMs on --T rows; ``--case attn``: gdn_attn_decode on --batch
     sequences with a --T position context; ``--case varlen``: gdn_prefill on
-    the 8-sequence varlen workload."""
+    the 8-sequence varlen workload; ``--case gated_out_proj``: the fused gated
+    norm + ssm_out GEMM on --T rows; ``--case in_proj_conv``: gdn_in_proj_conv
+    then gdn_prefill_xhat on --T tokens."""
     import torch
 
     from gated_deltanet_linear_02_gb300 import build as gbuild
@@ -766,6 +775,31 @@ def profile_case(args):
         for _ in range(n):
             ops.in_proj(h, w_in, *outs)
         assert ops.device_error() == ops.GDN_OK
+    elif args.case == "gated_out_proj":
+        w = I.out_proj_weight(I.seed_of(2), device=dev)
+        lp = I.layer_params(I.seed_of(2)).to(dev)
+        y = torch.randn(args.T, I.D_INNER, device=dev).to(torch.bfloat16)
+        z = torch.randn(args.T, I.D_INNER, device=dev).to(torch.bfloat16)
+        o = torch.empty(args.T, I.N_EMBD, dtype=torch.bfloat16, device=dev)
+        for _ in range(n):
+            ops.gated_out_proj(lp.norm_w, lp.norm_eps, y, z, w, o)
+        assert ops.device_error() == ops.GDN_OK
+    elif args.case == "in_proj_conv":
+        # gdn_in_proj_conv then gdn_prefill_xhat on one sequence of --T tokens
+        w_in = torch.cat(I.in_proj_weights(I.seed_of(2), device=dev), dim=0)
+        lp = I.layer_params(I.seed_of(2)).to(dev)
+        h = torch.randn(args.T, I.N_EMBD, device=dev).to(torch.bfloat16)
+        cu = I.cu_seqlens([args.T]).to(dev)
+        xh = torch.empty(args.T, I.C_CONV, dtype=torch.float16, device=dev)
+        z, al, be = (torch.empty(args.T, c, dtype=torch.bfloat16, device=dev) for c in (I.D_INNER, I.HV, I.HV))
+        cs = torch.empty(1, I.KCONV - 1, I.C_CONV, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(args.T, I.D_INNER, dtype=torch.bfloat16, device=dev)
+        S = torch.empty(1, I.HV, I.DV, I.DK, device=dev)
+        ws = None
+        for _ in range(n):
+            ops.in_proj_conv(lp, h, w_in, cu, xh, z, al, be, conv_state_out=cs)
+            ws = ops.prefill_xhat(lp, xh, z, al, be, cu, out, ssm_state_out=S, workspace=ws)
+        assert ops.device_error() == ops.GDN_OK
     elif args.case == "varlen":
         seed = I.seed_of(4)
         lens = I.varlen_lengths(seed)
@@ -804,7 +838,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["decode", "multi", "prefill", "varlen", "out_proj", "in_proj", "attn"],
+    ap.add_argument("--case", choices=["decode", "multi", "prefill", "varlen", "out_proj", "in_proj", "attn",
+                                       "gated_out_proj", "in_proj_conv"],
                     default=None,
                     help="profiling run of one path (see profile_case); prints no JSON line")
     ap.add_argument("--batch", type=int, default=64)
@@ -877,6 +912,7 @@ def main():
     op_tr, op_tr_note = traffic("out_proj")
     opb_tr, opb_tr_note = traffic("out_proj_batch")
     gp_tr, gp_tr_note = traffic("gated_out_proj")
+    f2_tr, f2_tr_note = traffic("in_proj_conv_prefill")
     PREFILL_BYTES = PREFILL_T * PREFILL_IO_BYTES_PER_TOKEN + PREFILL_END_STATE_BYTES + PREFILL_PARAM_BYTES
     pf_gbs = PREFILL_BYTES / (r["pf_ms"] / 1e3) / 1e9
     line = {
@@ -923,6 +959,8 @@ def main():
                   "gdn_in_proj_conv (conv, SiLU, q/k norms in the GEMM epilogue) + gdn_prefill_xhat",
             "us_per_call_unfused": r["f2"]["unfused"], "us_per_call_fused": r["f2"]["fused"],
             "hbm_bytes_saved_per_call": 2 * PREFILL_T * I_C_CONV * 2,
+            "traffic_fused": f2_tr, "traffic_fused_source": f2_tr_note,
+            "traffic_unfused": (None if ip_tr is None or pf_tr is None else ip_tr + pf_tr),
             "bytes_saved": "the raw q|k|v stream [T][8192] bf16, written by the projection and read back "
                            "by the mixer's conv", "l2": "flushed between timed calls"},
         "out_proj": {"workload": f"ssm_out_projection_M{PREFILL_T}_bf16", "op": "y = x w^T, 4096 -> 2048",
