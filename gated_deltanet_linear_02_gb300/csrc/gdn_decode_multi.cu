@@ -179,6 +179,42 @@ __device__ __forceinline__ float dot4(const float4 &v, const float4 &x, float ac
 // in five shuffles, halving the set at each step: lanes whose bit 3 is clear
 // keep p[0], p[1] and send p[2], p[3] to their partner, and so on. Returns the
 // total of p[g >> 2] (each total lands in four lanes).
+// Packed pairs of fp32 (fma.rn.f32x2: two fused multiply-adds per instruction,
+// each rounded as fmaf). A float4 is two pairs, (x, y) and (z, w).
+__device__ __forceinline__ uint64_t pk2(float a, float b)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// v0 . x0 + v1 . x1 over 8 elements, as two interleaved partial sums
+__device__ __forceinline__ float dot8x2(const float4 &v0, const float4 &v1, const float4 &x0, const float4 &x1)
+{
+    uint64_t acc = fma2(pk2(v0.x, v0.y), pk2(x0.x, x0.y), 0ull);
+    acc = fma2(pk2(v0.z, v0.w), pk2(x0.z, x0.w), acc);
+    acc = fma2(pk2(v1.x, v1.y), pk2(x1.x, x1.y), acc);
+    acc = fma2(pk2(v1.z, v1.w), pk2(x1.z, x1.w), acc);
+    float lo, hi;
+    upk2(acc, lo, hi);
+    return lo + hi;
+}
+// v += x s over a float4, as two pairs
+__device__ __forceinline__ void axpy4x2(float4 &v, const float4 &x, uint64_t ss)
+{
+    const uint64_t a = fma2(pk2(x.x, x.y), ss, pk2(v.x, v.y)), b = fma2(pk2(x.z, x.w), ss, pk2(v.z, v.w));
+    upk2(a, v.x, v.y);
+    upk2(b, v.z, v.w);
+}
 __device__ __forceinline__ float group16_reduce4(const float (&p)[4], int g)
 {
     const bool hi3 = g & 8, hi2 = g & 4;
@@ -381,7 +417,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
                 const float4 k0 = k4[0], k1 = k4[16];
                 float p[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) p[q] = dot4(st[q][1], k1, dot4(st[q][0], k0, 0.0f));
+                for (int q = 0; q < 4; ++q) p[q] = dot8x2(st[q][0], st[q][1], k0, k1);
                 const float pred = G * group16_reduce4(p, g);
                 const float dn = (sm.v[t][h][jown] - pred) * sm.gate[t][h][1] * iG;
                 float d[4];
@@ -391,9 +427,10 @@ __global__ void __launch_bounds__(MD_THREADS, 1) decode_multi_kernel(const Multi
                 float y[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    axpy4(st[q][0], k0, d[q]);
-                    axpy4(st[q][1], k1, d[q]);
-                    y[q] = dot4(st[q][1], q1, dot4(st[q][0], q0, 0.0f));
+                    const uint64_t dd = pk2(d[q], d[q]);
+                    axpy4x2(st[q][0], k0, dd);
+                    axpy4x2(st[q][1], k1, dd);
+                    y[q] = dot8x2(st[q][0], st[q][1], q0, q1);
                 }
                 if (t > 0 && (g & 3) == 0) sm.y[t - 1][h][jown] = y_prev * yscale_prev;
                 y_prev = group16_reduce4(y, g);
