@@ -105,33 +105,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// One producer thread's quarter of a head row (32 columns): the raw values of
-// y and z, loaded before the thread computes anything.
-template <typename TY>
-struct RowQuarter;
-template <>
-struct RowQuarter<bf16> {
-    uint4 y[4], z[4];
-    __device__ __forceinline__ void load(const bf16 *yr, const bf16 *zr)
-    {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) y[c] = __ldg(reinterpret_cast<const uint4 *>(yr) + c);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) z[c] = __ldg(reinterpret_cast<const uint4 *>(zr) + c);
-    }
-    __device__ __forceinline__ void zero()
-    {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) y[c] = z[c] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    __device__ __forceinline__ void get(int c, float (&yf)[8], float (&zf)[8]) const
-    {
-        bf16x8_to_f(y[c], yf);
-        bf16x8_to_f(z[c], zf);
-    }
-};
-template <>
-struct RowQuarter<float> {
+// fp32 y: one producer thread's quarter of a head row (32 columns) of y and z,
+// loaded into registers before the thread computes anything. (bf16 y arrives
+// by TMA in the operand slot instead.)
+struct RowQuarterF32 {
     float4 y[8], z[8];
     __device__ __forceinline__ void load(const float *yr, const float *zr)
     {
@@ -152,11 +129,6 @@ struct RowQuarter<float> {
         zf[0] = p.x; zf[1] = p.y; zf[2] = p.z; zf[3] = p.w; zf[4] = q.x; zf[5] = q.y; zf[6] = q.z; zf[7] = q.w;
     }
 };
-
-__device__ __forceinline__ void prefetch_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 template <typename TY, typename TO, int BN>
 __global__ void __launch_bounds__(GP_THREADS, 1) gated_proj_kernel(const __grid_constant__ CUtensorMap mw,
@@ -363,12 +335,13 @@ __global__ void __launch_bounds__(GP_THREADS, 1) gated_proj_kernel(const __grid_
             }
         } else {
             // fp32 y and z: both loaded into registers, the slot waited for here
-            const TY *ys = static_cast<const TY *>(a.y);
+            const float *ys = static_cast<const float *>(a.y);
+            const float *zf32 = static_cast<const float *>(a.z);
 #pragma unroll 1
             for (int i = 0; i < n_items && !aborted; ++i) {
                 const int m = row_of(i);
-                RowQuarter<TY> rq;
-                if (m < M) rq.load(ys + (size_t)m * DI + col_of(i), zs + (size_t)m * DI + col_of(i));
+                RowQuarterF32 rq;
+                if (m < M) rq.load(ys + (size_t)m * DI + col_of(i), zf32 + (size_t)m * DI + col_of(i));
                 else rq.zero();
                 float ss = 0.0f;
 #pragma unroll
