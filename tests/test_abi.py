@@ -245,3 +245,73 @@ def test_binding_refuses_cpu_tensors(ops):
     lp = inputs.layer_params(1)
     with pytest.raises(ValueError):
         ops.make_params(lp)           # CPU tensors: the binding only passes device memory
+
+
+def test_gated_out_proj_argument_checks_host(ops):
+    L = ops.lib()
+    call = lambda ptrs, M, act=ops.GDN_BF16, od=ops.GDN_F32, eps=1e-6: L.gdn_gated_out_proj(
+        ptrs[0], ctypes.c_float(eps), *ptrs[1:], M, act, od, None)
+    ok = [FAKE] * 5                     # norm_w, y, z, w, out
+    assert call(ok, 0) == ops.GDN_OK                                          # M == 0: no-op
+    assert call(ok, -1) == ops.GDN_ERR_INVALID_ARG
+    assert call(ok, (1 << 24) + 1) == ops.GDN_ERR_INVALID_ARG
+    assert call(ok, 4, act=2) == ops.GDN_ERR_INVALID_ARG
+    assert call(ok, 4, od=9) == ops.GDN_ERR_INVALID_ARG
+    assert call(ok, 4, eps=-1.0) == ops.GDN_ERR_INVALID_ARG
+    for i in range(5):
+        for badp in (0, MIS):
+            bad = list(ok)
+            bad[i] = badp
+            assert call(bad, 4) == ops.GDN_ERR_INVALID_ARG
+
+
+def test_in_proj_conv_argument_checks(ops):
+    L = ops.lib()
+    p = _params(ops)
+    # h, w_in, cu | N, M | cs_in, cs_out, xhat, z, alpha, beta
+    call = lambda pp, head, N, M, tail: L.gdn_in_proj_conv(
+        ctypes.byref(pp) if pp is not None else None, *head, N, M, *tail, None)
+    head, tail = [FAKE] * 3, [None, None] + [FAKE] * 4
+    assert call(p, head, 0, 0, tail) == ops.GDN_OK                            # no sequences: no-op
+    assert call(p, head, 0, 5, tail) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, head, -1, 0, tail) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, head, 2, -1, tail) == ops.GDN_ERR_INVALID_ARG
+    assert call(None, head, 2, 8, tail) == ops.GDN_ERR_INVALID_ARG
+    assert call(_params(ops, conv_w=MIS), head, 2, 8, tail) == ops.GDN_ERR_INVALID_ARG
+    assert call(_params(ops, l2_eps=-1.0), head, 2, 8, tail) == ops.GDN_ERR_INVALID_ARG
+    for i in range(3):
+        bad = list(head)
+        bad[i] = 0
+        assert call(p, bad, 2, 8, tail) == ops.GDN_ERR_INVALID_ARG
+    for i in range(2, 6):
+        bad = list(tail)
+        bad[i] = MIS
+        assert call(p, head, 2, 8, bad) == ops.GDN_ERR_INVALID_ARG
+    bad = list(tail)
+    bad[0] = MIS                                                              # a misaligned state
+    assert call(p, head, 2, 8, bad) == ops.GDN_ERR_INVALID_ARG
+    same = [FAKE, FAKE] + [FAKE] * 4                                          # in and out states overlap
+    assert call(p, head, 2, 8, same) == ops.GDN_ERR_INVALID_ARG
+    assert "overlap" in ops.last_error()
+
+
+def test_prefill_xhat_argument_checks(ops):
+    L = ops.lib()
+    p = _params(ops)
+    # xhat, z, alpha, beta, cu | N, T | S_in, S_out, out | out_dt, ws, ws_bytes
+    call = lambda pp, five, N, T, three, od=ops.GDN_F32, ws=FAKE * 16, wsb=1 << 30: L.gdn_prefill_xhat(
+        ctypes.byref(pp) if pp is not None else None, *five, N, T, *three, od, ws, wsb, None)
+    five, three = [FAKE] * 5, [None, None, FAKE]
+    assert call(p, five, 0, 0, three) == ops.GDN_OK                           # no sequences: no-op
+    assert call(p, five, 0, 3, three) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, five, 1, -1, three) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, five, 1, 64, three, od=4) == ops.GDN_ERR_INVALID_ARG
+    assert call(None, five, 1, 64, three) == ops.GDN_ERR_INVALID_ARG
+    for i in range(5):
+        bad = list(five)
+        bad[i] = 0
+        assert call(p, bad, 1, 64, three) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, five, 1, 64, [MIS, None, FAKE]) == ops.GDN_ERR_INVALID_ARG
+    assert call(p, five, 1, 64, three, ws=None) == ops.GDN_ERR_WORKSPACE
+    assert call(p, five, 1, 64, three, wsb=1024) == ops.GDN_ERR_WORKSPACE
+    assert call(p, five, 1, 64, three, ws=FAKE * 16 + 16) == ops.GDN_ERR_WORKSPACE   # not 256-byte aligned
