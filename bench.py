@@ -82,7 +82,7 @@ TRAFFIC = {
                    per="launch of decode_step_kernel at B=256"),
     "attn": dict(bytes=2_168_676_864 + 18_318_080, src="gdn_attn.cu", sha="c68c58d38f8812f9", profile="profiles/attn_decode_B256_ctx4096.md",
                  per="call (attn_block_kernel + attn_combine_kernel) at B=256, ctx 4096"),
-    "multi": dict(bytes=574_927_360 + 495_363_328, src="gdn_decode_multi.cu", sha="9724c9ac6f3ea2aa", profile="profiles/decode_multi_kernel_B256_T4.md",
+    "multi": dict(bytes=574_936_320 + 495_239_424, src="gdn_decode_multi.cu", sha="f4b811c1579705af", profile="profiles/decode_multi_kernel_B256_T4.md",
                   per="launch of decode_multi_kernel at B=256, T=4"),
     "prefill": dict(bytes=355_511_296 + 124_768_512, src="gdn_chunk.cu", sha="912edb772ce70df0", profile="profiles/chunk_prefill_T4096.md",
                     per="gdn_prefill call at T=4096 (all of its kernels)"),
@@ -92,7 +92,7 @@ TRAFFIC = {
                     per="gdn_in_proj call at M=4096"),
     "out_proj": dict(bytes=50_358_016 + 100_096, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                      per="gdn_out_proj call at M=4096"),
-    "gated_out_proj": dict(bytes=83_935_232 + 2_999_040, src="gdn_gated_proj.cu", sha="459ac59685a98db4",
+    "gated_out_proj": dict(bytes=83_939_072 + 2_929_408, src="gdn_gated_proj.cu", sha="f20dfeb1dda1398b",
                            profile="profiles/gated_proj_M4096.md",
                            per="gdn_gated_out_proj call at M=4096"),
     "in_proj_conv_prefill": dict(bytes=404_716_032 + 182_607_616, src=("gdn_in_conv.cu", "gdn_chunk.cu"),
