@@ -742,11 +742,11 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
 //   (E2) S^T -> fp16 copy for the next chunk's products; gamma_n(next) S^T back.
 //   (O)  y = scale (gamma_t Y1 + Y2) to shared memory as [t][j]; then one warp per
 //        token row: out = y rms(y)^-1 w silu(z)
-// Warps 0-7 run E1/E2 (lane quarter w % 4, half w / 4); warps 8-15 the output;
-// warp 16 loads operands; warps 17-19 issue MMAs. The issuers and the producer
-// take no part in CTA-wide barriers; every handoff is an mbarrier, and the
-// output warps meet at named barriers of their own.
-constexpr int CA_THREADS = 32 * 20;
+// Warps 0-7 run E1/E2 (lane quarter w % 4, half w / 4); warps 8-11 the output;
+// warp 12 loads operands; warps 13-15 issue MMAs. The issuers and the producer
+// take no part in CTA-wide barriers; every handoff is an mbarrier.
+constexpr int CA_THREADS = 32 * 16;
+constexpr int CA_PRODUCER = 12, CA_ISSUER0 = 13;       // warp 12: the blob copies; 13-15: the MMA issuers
 constexpr uint32_t ST_BLOB = 0;                         // the blob (W^T | U^T | P | K~ | Q~ | gamma_n)
 constexpr uint32_t STAGE_BYTES = BLOB_BYTES;
 constexpr uint32_t CA_SMALL = 2 * STAGE_BYTES;
@@ -834,7 +834,7 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
         mbar_init(smem_u32(&ss.vn), 8);
         mbar_init(smem_u32(&ss.s16), 8);
         mbar_init(smem_u32(&ss.dec), 8);
-        mbar_init(smem_u32(&ss.yfree), 8);
+        mbar_init(smem_u32(&ss.yfree), 4);
         for (int k = 0; k < 3; ++k) mbar_init(smem_u32(&ss.done[k]), 1);
         ss.abort = 0;
         fence_mbar_init();
@@ -849,7 +849,7 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
         return !aborted;
     };
 
-    if (warp == 16) {
+    if (warp == CA_PRODUCER) {
         // ---------------------------------------------------------- producer: one bulk copy per chunk
         if (lane == 0) {
             int issued = 0;
@@ -864,12 +864,12 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
             for (int c = max(0, issued - 2); c < issued; ++c)   // copies in flight land before the CTA exits
                 mbar_wait_sleep(smem_u32(&ss.full[c & 1]), (uint32_t)((c >> 1) & 1));
         }
-    } else if (warp >= 17) {
+    } else if (warp >= CA_ISSUER0) {
         // ---------------------------------------------------------- MMA issuers
-        // 17: (W S)^T keys 0-63, then the state update (the chain);
-        // 18: (W S)^T keys 64-127;  19: Y = Q~ S + P Vnew.
+        // 13: (W S)^T keys 0-63, then the state update (the chain);
+        // 14: (W S)^T keys 64-127;  15: Y = Q~ S + P Vnew.
         if (lane == 0) {
-            const int role = warp - 17;
+            const int role = warp - CA_ISSUER0;
             const uint32_t id_ws = tc::instr_desc(tc::FMT_F16, 128, CH) | tc::IDESC_B_MN;
             const uint32_t id_s = tc::instr_desc(tc::FMT_F16, 128, DK) | tc::IDESC_B_MN;
             const uint32_t id_y = tc::instr_desc(tc::FMT_F16, 128, CH);
@@ -1042,11 +1042,11 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
         }
     } else {
         // ---------------------------------------------------------- output: y to the buffer
-        // Warps 8-15 (lane quarter w % 4, token half (w - 8) / 4): y = scale Y of
-        // column j for 32 tokens, stored as fp16; a warp's store for one token
-        // covers 32 consecutive columns (64 bytes). The gated RMSNorm . silu(z)
-        // across each head's 128 columns runs as its own kernel over all SMs.
-        const int q = warp & 3, hh = (warp - 8) >> 2;
+        // Warps 8-11 (lane quarter w % 4): y = scale Y of column j for the
+        // chunk's 64 tokens, stored as fp16; a warp's store for one token covers
+        // 32 consecutive columns (64 bytes). The gated RMSNorm . silu(z) across
+        // each head's 128 columns runs as its own kernel over all SMs.
+        const int q = warp & 3;
         const int j = 32 * q + lane;
         const uint32_t lq = (uint32_t)(32 * q) << 16;
         const float scale = rsqrtf((float)DK);
@@ -1055,21 +1055,24 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
             const int nv = nv_of(c);
             if (!wait(ss.y, par)) break;
             tc::fence_after_sync();
-            float y[32];
-            tc::tmem_ld32(tm + lq + TC_Y + 32 * hh, y);
+            float y[2][32];
+            tc::tmem_ld32(tm + lq + TC_Y, y[0]);
+            tc::tmem_ld32(tm + lq + TC_Y + 32, y[1]);
             tc::wait_ld();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ss.yfree));
-            __half *yr = a.ybuf + (size_t)(fr.row_a + CH * c + 32 * hh - a.w0) * DI + (size_t)vh * DV + j;
+            __half *yr = a.ybuf + (size_t)(fr.row_a + CH * c - a.w0) * DI + (size_t)vh * DV + j;
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
-                if (32 * hh + t < nv) yr[(size_t)t * DI] = __float2half_rn(scale * y[t]);
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    if (32 * hh + t < nv) yr[(size_t)(32 * hh + t) * DI] = __float2half_rn(scale * y[hh][t]);
         }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp >= 17 && lane == 0) mbar_wait_sleep(smem_u32(&ss.done[warp - 17]), 0u);
+    if (warp >= CA_ISSUER0 && lane == 0) mbar_wait_sleep(smem_u32(&ss.done[warp - CA_ISSUER0]), 0u);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
