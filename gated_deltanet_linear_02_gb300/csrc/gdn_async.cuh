@@ -31,6 +31,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Ends an mbarrier's life, so that its word may be initialised again.
+__device__ __forceinline__ void mbar_inval(uint32_t bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Makes mbarrier initialisation visible to the async proxy (TMA) and the cluster.
 __device__ __forceinline__ void fence_mbar_init()
 {

@@ -47,6 +47,8 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstddef>
+#include <cstdlib>
 
 namespace gdn {
 
@@ -124,6 +126,7 @@ struct WyArgs {
     WyChunk *chunks;
     __half *xhat;                // [wlen][8192]
     int gates_only;              // x^ comes from the caller (gdn_in_proj_conv): act writes the gates only
+    int *flags;                  // [c_cap][16]: item (chunk, K-head) of prep done (one kernel: prep + carry), or NULL
     __half *ybuf;                // [wlen][4096]: y (scale applied) before the gated norm
     float *gates;                // [c_cap][32][4][64]: per (chunk, V-head) G, beta, gamma_t, exp(G_n - G_t)
     unsigned char *blobs;        // [c_cap][32] x BLOB_BYTES
@@ -179,6 +182,8 @@ __global__ void __launch_bounds__(1024) wy_plan_kernel(const WyArgs a)
         a.count->n_frag = min(part[0][31], a.f_cap);
         a.count->n_chunks = min(part[1][31], a.c_cap);
     }
+    if (a.flags)                                       // no item of this window is done yet
+        for (int i = tid; i < a.c_cap * HK; i += blockDim.x) a.flags[i] = 0;
     for (int n = lo; n < hi; ++n) {
         const int s0 = cu_clamp(a.cu, n, 0, a.T_total), s1 = cu_clamp(a.cu, n + 1, s0, a.T_total);
         const int fa = max(s0, e0), fb = min(s1, e1);
@@ -355,8 +360,8 @@ __device__ __forceinline__ unsigned char *smem_aligned1024(unsigned char *raw)
     return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
 }
 
-__global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_constant__ CUtensorMap xmap,
-                                                               const WyArgs a)
+// The prep work of CTA `cta` of `n_ctas` (items cta, cta + n_ctas, ..).
+__device__ __forceinline__ void wy_prep_body(const CUtensorMap &xmap, const WyArgs &a, int cta, int n_ctas)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = smem_aligned1024(smem_raw);
@@ -395,8 +400,8 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
         tc::tmem_alloc(smem_u32(&ss.tmem), TP_COLS);
         tc::tmem_relinquish();
     }
-    const int stride = (int)gridDim.x;
-    int item = (int)blockIdx.x;
+    const int stride = n_ctas;
+    int item = cta;
     if (tid == 0) {
         mbar_init(smem_u32(&ss.bar_x[0]), 1);
         mbar_init(smem_u32(&ss.bar_x[1]), 1);
@@ -716,7 +721,10 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
             }
         }
         tc::fence_before_sync();
+        if (a.flags) __threadfence();                  // the item's blob writes, before its flag
         __syncthreads();                               // TMEM, the gates and the T tiles are reused
+        if (a.flags && tid == 0 && !ss.abort)          // the carry CTAs of the one-kernel form may go on
+            asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(a.flags + item), "r"(1) : "memory");
         if (ss.abort) break;
     }
     // after an abort: a copy still in flight lands before the CTA exits
@@ -725,6 +733,12 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, TP_COLS);
     if (tid == 0 && ss.abort) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                               const WyArgs a)
+{
+    wy_prep_body(xmap, a, (int)blockIdx.x, (int)gridDim.x);
 }
 
 // ------------------------------------------------------------------ carry
@@ -751,6 +765,7 @@ constexpr uint32_t ST_BLOB = 0;                         // the blob (W^T | U^T |
 constexpr uint32_t STAGE_BYTES = BLOB_BYTES;
 constexpr uint32_t CA_SMALL = 2 * STAGE_BYTES;
 struct CaSmall {
+    // the mbarriers first: CA_NBAR words
     uint64_t full[2], free_[2];        // operand stages
     uint64_t m1a, m1b, m2, y;          // tensor-core completions
     uint64_t vn, s16, dec, yfree;      // epilogue handoffs
@@ -758,6 +773,8 @@ struct CaSmall {
     uint32_t tmem;
     int abort;
 };
+constexpr int CA_NBAR = 15;
+static_assert(offsetof(CaSmall, tmem) == CA_NBAR * sizeof(uint64_t), "the mbarriers lead CaSmall");
 constexpr size_t CA_SMEM = CA_SMALL + sizeof(CaSmall) + 1024;
 static_assert(CA_SMEM <= 232448, "carry shared memory");
 constexpr int CA_FREE_ARRIVALS = 3 + 8;                 // three issuer commits, E1 warps
@@ -794,19 +811,21 @@ template <> __device__ __forceinline__ void store_out4<bf16>(bf16 *p, float a, f
     store4(p, make_float4(a, b, c, d));
 }
 
-__global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
+// The chain of fragment f, V-head vh. Returns true when it gave up on a wait.
+// `again`: the CTA runs further chains after this one, so it keeps its right to
+// allocate tensor memory and ends its mbarriers' life on the way out.
+__device__ __forceinline__ bool wy_carry_body(const WyArgs &a, int f, int vh, bool again)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = smem_aligned1024(smem_raw);
     CaSmall &ss = *reinterpret_cast<CaSmall *>(sm + CA_SMALL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int f = blockIdx.x, vh = blockIdx.y;
     grid_dep_wait();                                   // blobs and tables come from the kernels ahead
     grid_dep_launch();
-    if (f >= a.count->n_frag) return;
+    if (f >= a.count->n_frag) return false;
     const WyFrag fr = a.frags[f];
     const int nc = fr.nchunks;
-    if (nc <= 0) return;
+    if (nc <= 0) return false;
     const uint32_t sb = smem_u32(sm);
     const float *S_src = (fr.flags & 1) ? (a.S_in ? a.S_in + ((size_t)fr.seq * HV + vh) * (DV * DK) : nullptr)
                                         : a.slot_in + (size_t)vh * (DV * DK);
@@ -820,7 +839,7 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
 
     if (warp == 0) {
         tc::tmem_alloc(smem_u32(&ss.tmem), TC_COLS);
-        tc::tmem_relinquish();
+        if (!again) tc::tmem_relinquish();
     }
     if (tid == 0) {
         for (int k = 0; k < 2; ++k) {
@@ -856,6 +875,24 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
             for (int c = 0; c < nc; ++c) {
                 const int st = c & 1, u = c >> 1;
                 if (u >= 1 && !wait(ss.free_[st], (uint32_t)((u - 1) & 1))) break;
+                if (a.flags) {
+                    // one-kernel form: the chunk's blob is written by a prep CTA of this
+                    // grid; wait for its flag (bounded), then let the copy (async
+                    // proxy) see those writes
+                    const int *fl = a.flags + (size_t)(fr.chunk0 + c) * HK + (vh % HK);
+                    uint64_t t0 = 0;
+                    bool ready = false;
+                    for (uint32_t it = 0;; ++it) {
+                        int v;
+                        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(fl) : "memory");
+                        if (v) { ready = true; break; }
+                        if (it == 0) t0 = global_timer_ns();
+                        else if (global_timer_ns() - t0 > WAIT_LIMIT_NS) break;
+                        __nanosleep(128);
+                    }
+                    if (!ready) { ss.abort = 1; break; }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 const uint32_t bar = smem_u32(&ss.full[st]);
                 mbar_arrive_expect_tx(bar, STAGE_BYTES);
                 bulk_g2s(sb + (uint32_t)st * STAGE_BYTES + ST_BLOB, blob_of(c), BLOB_BYTES, bar);
@@ -1077,7 +1114,39 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
     __syncthreads();
     tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tm, TC_COLS);
-    if (tid == 0 && ss.abort) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+    const bool gave_up = aborted;
+    if (tid == 0 && gave_up) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+    if (again && !gave_up && tid == 0)                 // every wait on them has ended (the barrier above)
+        for (int k = 0; k < CA_NBAR; ++k) mbar_inval(smem_u32(reinterpret_cast<uint64_t *>(&ss) + k));
+    return gave_up;
+}
+
+__global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
+{
+    wy_carry_body(a, (int)blockIdx.x, (int)blockIdx.y, false);
+}
+
+// One kernel for prep and the chains of a window. The first 32 G CTAs run the
+// chains, G = min(fragments, FU_GROUPS): CTA b takes V-head b % 32 of fragments
+// b / 32, b / 32 + G, .. one after the other; the other CTAs run the prep items
+// in chunk order. A chain takes a chunk's operands as soon as the prep CTA of
+// that (chunk, K-head) has flagged it, so prep and chains run side by side on
+// separate SMs. Launched cooperatively (every CTA resident at once): the chain
+// CTAs wait on flags the prep CTAs set, never the other way round.
+constexpr int FU_GROUPS = 2;
+static_assert(PR_THREADS == CA_THREADS, "one block size for both roles");
+__global__ void __launch_bounds__(PR_THREADS, 1) wy_fused_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                const WyArgs a)
+{
+    const int n_frag = a.count->n_frag;                // the plan kernel ahead has completed
+    const int groups = max(1, min(n_frag, FU_GROUPS));
+    const int nca = groups * HV, b = (int)blockIdx.x;
+    if (b < nca) {
+        for (int f = b / HV; f < n_frag; f += groups)
+            if (wy_carry_body(a, f, b % HV, true)) break;
+    } else {
+        wy_prep_body(xmap, a, b - nca, (int)gridDim.x - nca);
+    }
 }
 
 // The gated RMSNorm . silu(z) of section "Output path" over the window's rows:
@@ -1145,12 +1214,12 @@ static size_t rnd256(size_t x) { return (x + 255) & ~(size_t)255; }
 static size_t rnd1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
 struct WyLayout {
-    size_t count, frags, chunks, gates, xhat, ybuf, blobs, slots, total;
+    size_t count, frags, chunks, flags, gates, xhat, ybuf, blobs, slots, total;
     int W, f_cap, c_cap;
 };
 
 // Workspace of the chunked path for windows of W tokens (W a multiple of 64):
-// counts | fragments | chunks | gate records [c_cap][32] | x^ [W][8192] fp16 | y [W][4096] fp16 |
+// counts | fragments | chunks | prep flags [c_cap][16] | gate records [c_cap][32] | x^ [W][8192] fp16 | y [W][4096] fp16 |
 // blobs [c_cap][32] | two state slots.
 static WyLayout wy_layout(int N, int W)
 {
@@ -1161,7 +1230,8 @@ static WyLayout wy_layout(int N, int W)
     size_t o = 0;
     L.count = o;  o = rnd256(o + sizeof(WyCount));
     L.frags = o;  o = rnd256(o + (size_t)L.f_cap * sizeof(WyFrag));
-    L.chunks = o; o = rnd1024(o + (size_t)L.c_cap * sizeof(WyChunk));
+    L.chunks = o; o = rnd256(o + (size_t)L.c_cap * sizeof(WyChunk));
+    L.flags = o;  o = rnd1024(o + (size_t)L.c_cap * HK * sizeof(int));
     L.gates = o;  o = rnd1024(o + (size_t)L.c_cap * HV * GATE_FLOATS * sizeof(float));
     L.xhat = o;   o = rnd1024(o + (size_t)W * CC * sizeof(__half));
     L.ybuf = o;   o = rnd1024(o + (size_t)W * DI * sizeof(__half));
@@ -1198,11 +1268,25 @@ static int wy_window(int N, int T_total, size_t ws_bytes)
     return lo * CH;
 }
 
+// GDN_PREFILL_SPLIT=1 in the environment keeps prep and the chains in two
+// kernels (for a device share too small for a one-per-SM cooperative grid).
+static bool prefill_split_forced()
+{
+    static const bool forced = [] {
+        const char *v = std::getenv("GDN_PREFILL_SPLIT");
+        return v != nullptr && v[0] == '1';
+    }();
+    return forced;
+}
+
 static cudaError_t wy_setup()
 {
     cudaError_t e = cudaFuncSetAttribute(wy_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_SMEM);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(wy_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CA_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(wy_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)std::max(PR_SMEM, CA_SMEM));
     return e;
 }
 
@@ -1230,6 +1314,18 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
         a.count = reinterpret_cast<WyCount *>(ws + L.count);
         a.frags = reinterpret_cast<WyFrag *>(ws + L.frags);
         a.chunks = reinterpret_cast<WyChunk *>(ws + L.chunks);
+        // the one-kernel form when every CTA of a one-per-SM grid can be resident
+        // at once (a cooperative launch), else the prep and carry kernels apart
+        int coop = 0, per_sm = 0, dev = 0;
+        bool fused = n_sm > FU_GROUPS * HV && !prefill_split_forced();
+        if (fused)
+            fused = cudaGetDevice(&dev) == cudaSuccess &&
+                    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, wy_fused_kernel, PR_THREADS,
+                                                                  std::max(PR_SMEM, CA_SMEM)) == cudaSuccess &&
+                    per_sm >= 1;
+        cudaGetLastError();                            // a refused query only means: separate kernels
+        a.flags = fused ? reinterpret_cast<int *>(ws + L.flags) : nullptr;
         a.gates = reinterpret_cast<float *>(ws + L.gates);
         a.xhat = reinterpret_cast<__half *>(ws + L.xhat);
         a.gates_only = xhat_ext != nullptr;
@@ -1253,11 +1349,26 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
             if (e == cudaSuccess)
                 e = launch_pdl(wy_act_kernel, dim3((unsigned)L.c_cap, xhat_ext ? HK : CC / DK), dim3(ACT_THREADS), 0,
                                s, a);
-            if (e == cudaSuccess)
-                e = launch_pdl(wy_prep_kernel, dim3((unsigned)std::min(L.c_cap * HK, n_sm)), dim3(PR_THREADS),
-                               PR_SMEM, s, xmap, a);
-            if (e == cudaSuccess)
-                e = launch_pdl(wy_carry_kernel, dim3((unsigned)L.f_cap, HV), dim3(CA_THREADS), CA_SMEM, s, a);
+            if (fused) {
+                // prep and the chains in one cooperative grid, one CTA per SM
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3((unsigned)n_sm);
+                cfg.blockDim = dim3(PR_THREADS);
+                cfg.dynamicSmemBytes = std::max(PR_SMEM, CA_SMEM);
+                cfg.stream = s;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeCooperative;
+                attr[0].val.cooperative = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, wy_fused_kernel, xmap, a);
+            } else {
+                if (e == cudaSuccess)
+                    e = launch_pdl(wy_prep_kernel, dim3((unsigned)std::min(L.c_cap * HK, n_sm)), dim3(PR_THREADS),
+                                   PR_SMEM, s, xmap, a);
+                if (e == cudaSuccess)
+                    e = launch_pdl(wy_carry_kernel, dim3((unsigned)L.f_cap, HV), dim3(CA_THREADS), CA_SMEM, s, a);
+            }
             if (e == cudaSuccess) {
                 if (out_dt == GDN_F32)
                     e = launch_pdl(wy_norm_kernel<float>, dim3((unsigned)a.wlen), dim3(256), 0, s, a);

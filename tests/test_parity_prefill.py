@@ -227,3 +227,22 @@ def test_prefill_windows_small_workspace(ops, ws_tokens, alias):
     ref = oracle_varlen(lp, st, lengths, conv0, S0)
     check(f"windows of {ws_tokens}", got, ref, torch.bfloat16, torch.float32)
 
+
+
+def test_prefill_split_form_matches_oracle():
+    """GDN_PREFILL_SPLIT=1 runs prep and the chains as two kernels instead of
+    one cooperative kernel. The many-fragment, windowed and ragged cases above
+    must hold in that form too (run in a child process, which reads the switch
+    at its first prefill)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, GDN_PREFILL_SPLIT="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_parity_prefill.py", "-k",
+                        "ragged_and_empty or windows_small_workspace or fragment_continuity or T4096"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=1200)
+    print(r.stdout[-2000:])
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+    assert " 9 passed" in r.stdout or "9 passed" in r.stdout
