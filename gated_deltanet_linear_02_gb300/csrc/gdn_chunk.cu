@@ -72,6 +72,7 @@ struct WyChunk {
 };
 struct WyCount {
     int n_frag, n_chunks;
+    int norm_next;         // one kernel form: the next norm item to hand out
 };
 
 // Per (chunk, V-head) operand blob, 72 KiB. The tiles are stored exactly as
@@ -127,6 +128,8 @@ struct WyArgs {
     __half *xhat;                // [wlen][8192]
     int gates_only;              // x^ comes from the caller (gdn_in_proj_conv): act writes the gates only
     int *flags;                  // [c_cap][16]: item (chunk, K-head) of prep done (one kernel: prep + carry), or NULL
+    int *yflags;                 // [c_cap][32]: y of (chunk, V-head) written (one kernel form), or NULL
+    int out_f32;                 // out is fp32 (else bf16)
     __half *ybuf;                // [wlen][4096]: y (scale applied) before the gated norm
     float *gates;                // [c_cap][32][4][64]: per (chunk, V-head) G, beta, gamma_t, exp(G_n - G_t)
     unsigned char *blobs;        // [c_cap][32] x BLOB_BYTES
@@ -181,9 +184,12 @@ __global__ void __launch_bounds__(1024) wy_plan_kernel(const WyArgs a)
     if (tid == 0) {
         a.count->n_frag = min(part[0][31], a.f_cap);
         a.count->n_chunks = min(part[1][31], a.c_cap);
+        a.count->norm_next = 0;
     }
     if (a.flags)                                       // no item of this window is done yet
         for (int i = tid; i < a.c_cap * HK; i += blockDim.x) a.flags[i] = 0;
+    if (a.yflags)
+        for (int i = tid; i < a.c_cap * HV; i += blockDim.x) a.yflags[i] = 0;
     for (int n = lo; n < hi; ++n) {
         const int s0 = cu_clamp(a.cu, n, 0, a.T_total), s1 = cu_clamp(a.cu, n + 1, s0, a.T_total);
         const int fa = max(s0, e0), fb = min(s1, e1);
@@ -1082,7 +1088,9 @@ __device__ __forceinline__ bool wy_carry_body(const WyArgs &a, int f, int vh, bo
         // Warps 8-11 (lane quarter w % 4): y = scale Y of column j for the
         // chunk's 64 tokens, stored as fp16; a warp's store for one token covers
         // 32 consecutive columns (64 bytes). The gated RMSNorm . silu(z) across
-        // each head's 128 columns runs as its own kernel over all SMs.
+        // each head's 128 columns runs on other SMs: in the one-kernel form on the
+        // CTAs past their prep items, which wait for a flag per (chunk, V-head),
+        // else as its own kernel.
         const int q = warp & 3;
         const int j = 32 * q + lane;
         const uint32_t lq = (uint32_t)(32 * q) << 16;
@@ -1090,7 +1098,8 @@ __device__ __forceinline__ bool wy_carry_body(const WyArgs &a, int f, int vh, bo
         for (int c = 0; c < nc; ++c) {
             const uint32_t par = (uint32_t)(c & 1);
             const int nv = nv_of(c);
-            if (!wait(ss.y, par)) break;
+            const bool ok = wait(ss.y, par);
+            if (bar_red_or(1, 128, !ok)) break;        // the four warps leave together
             tc::fence_after_sync();
             float y[2][32];
             tc::tmem_ld32(tm + lq + TC_Y, y[0]);
@@ -1099,12 +1108,26 @@ __device__ __forceinline__ bool wy_carry_body(const WyArgs &a, int f, int vh, bo
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ss.yfree));
+            // one kernel form: the previous chunk's y of this head is complete (the
+            // barrier above follows the four warps' stores of it). One thread
+            // releases its flag, after Y is handed back, so that the release's
+            // fence stays off the chain; a chunk late, so that it finds those
+            // stores long done.
+            if (a.yflags && c > 0 && warp == 8 && lane == 0)
+                asm volatile("st.release.gpu.global.s32 [%0], %1;"
+                             ::"l"(a.yflags + (size_t)(fr.chunk0 + c - 1) * HV + vh), "r"(1) : "memory");
             __half *yr = a.ybuf + (size_t)(fr.row_a + CH * c - a.w0) * DI + (size_t)vh * DV + j;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int t = 0; t < 32; ++t)
                     if (32 * hh + t < nv) yr[(size_t)(32 * hh + t) * DI] = __float2half_rn(scale * y[hh][t]);
+            if (a.yflags && c == nc - 1) {             // the last chunk's y
+                bar_named(2, 128);
+                if (warp == 8 && lane == 0)
+                    asm volatile("st.release.gpu.global.s32 [%0], %1;"
+                                 ::"l"(a.yflags + (size_t)(fr.chunk0 + c) * HV + vh), "r"(1) : "memory");
+            }
         }
     }
     tc::fence_before_sync();
@@ -1126,6 +1149,109 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
     wy_carry_body(a, (int)blockIdx.x, (int)blockIdx.y, false);
 }
 
+// Norm items of the one-kernel form: the gated RMSNorm . silu(z) of section
+// "Output path", out = y (mean_j y^2 + eps)^-1/2 w_j silu(z) per token and
+// V-head, over items (chunk, 4 V-heads) handed out in chunk order from a
+// counter, so that a CTA past its prep items takes the next item whose y is
+// (about to be) written. One thread waits (bounded, with a back-off that keeps
+// the polling off the chains' way) for the item's four y flags, then brings the
+// item's y and z rows (64 x 512 columns each) into the shared memory prep has
+// left, by TMA: plain loads would have to stage through the little L1 that the
+// kernel's shared memory leaves. Warp w takes rows 4w..4w+3; lane l holds
+// columns 4l..4l+3 of a head, so the head's sum of squares is a warp sum.
+constexpr int NI_HEADS = 4;
+constexpr uint32_t NI_Y = 0, NI_Z = 65536, NI_BAR = 131072;   // two 64 x 256 boxes each
+static_assert(NI_BAR + 8 <= PR_SMALL, "the norm tiles fit below the prep block's mbarriers");
+template <typename TO>
+__device__ void wy_norm_items(const CUtensorMap &ymap, const CUtensorMap &zmap, const WyArgs &a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ int item_s;
+    unsigned char *sm = smem_aligned1024(smem_raw);
+    const uint32_t sb = smem_u32(sm), bar = sb + NI_BAR;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_items = a.count->n_chunks * (HV / NI_HEADS);
+    const bool has_w = a.norm_w != nullptr;
+    const float4 w = has_w ? __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane) : make_float4(1.f, 1.f, 1.f, 1.f);
+    int ticket = 0;                                    // thread 0: the next item to run
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        ticket = atomicAdd(&a.count->norm_next, 1);
+    }
+    __syncthreads();
+    for (uint32_t phase = 0;; phase ^= 1u) {
+        if (warp == 0) {
+            // lanes 0-3 wait for one head's y flag each; lane 0 then starts the copies
+            int item = __shfl_sync(0xffffffffu, ticket, 0);
+            if (item < n_items) {
+                const int g = item / (HV / NI_HEADS), h0 = NI_HEADS * (item % (HV / NI_HEADS));
+                bool ready = true;
+                if (lane < NI_HEADS) {
+                    const int *fl = a.yflags + (size_t)g * HV + h0 + lane;
+                    const uint64_t t0 = global_timer_ns();
+                    for (;;) {
+                        int v;
+                        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(fl) : "memory");
+                        if (v) break;
+                        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) { ready = false; break; }
+                        __nanosleep(500);
+                    }
+                }
+                if (!__all_sync(0xffffffffu, ready)) {
+                    if (lane == 0) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+                    item = -1;
+                } else if (lane == 0) {
+                    // the copies (async proxy) after the flags and after this CTA's
+                    // earlier generic accesses of the same shared memory
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    const WyChunk ck = a.chunks[g];
+                    mbar_arrive_expect_tx(bar, 4u * 32768u);
+                    tma_load_2d(sb + NI_Y, &ymap, h0 * DV, ck.row0 - a.w0, bar);
+                    tma_load_2d(sb + NI_Y + 32768, &ymap, h0 * DV + 256, ck.row0 - a.w0, bar);
+                    tma_load_2d(sb + NI_Z, &zmap, h0 * DV, ck.row0, bar);
+                    tma_load_2d(sb + NI_Z + 32768, &zmap, h0 * DV + 256, ck.row0, bar);
+                }
+            }
+            if (lane == 0) item_s = item;
+        }
+        __syncthreads();
+        const int item = item_s;
+        if (item < 0 || item >= n_items) return;       // uniform: every thread read item_s after the barrier
+        if (tid == 0) ticket = atomicAdd(&a.count->norm_next, 1);   // the next one, while this one runs
+        const int g = item / (HV / NI_HEADS), h0 = NI_HEADS * (item % (HV / NI_HEADS));
+        const WyChunk ck = a.chunks[g];
+        const bool ok = mbar_wait_sleep(bar, phase);
+        if (__syncthreads_or(!ok)) {                   // a copy that never landed: leave together
+            if (tid == 0) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+            return;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int r = 4 * warp + (u >> 2), hh = u & 3;
+            const uint32_t off = (uint32_t)r * 512u + (uint32_t)((hh & 1) * 128 + 4 * lane) * 2u + (uint32_t)(hh >> 1) * 32768u;
+            const uint2 yv = *reinterpret_cast<const uint2 *>(sm + NI_Y + off);
+            const uint2 zv = *reinterpret_cast<const uint2 *>(sm + NI_Z + off);
+            const float2 y01 = __half22float2(*reinterpret_cast<const __half2 *>(&yv.x));
+            const float2 y23 = __half22float2(*reinterpret_cast<const __half2 *>(&yv.y));
+            float o0 = y01.x, o1 = y01.y, o2 = y23.x, o3 = y23.y;
+            if (has_w) {
+                const float ms = warp_sum(o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3) * (1.0f / DV);
+                const float rs = rsqrtf(ms + a.norm_eps);
+                o0 *= rs * w.x * silu_gate(__uint_as_float(zv.x << 16));
+                o1 *= rs * w.y * silu_gate(__uint_as_float(zv.x & 0xFFFF0000u));
+                o2 *= rs * w.z * silu_gate(__uint_as_float(zv.y << 16));
+                o3 *= rs * w.w * silu_gate(__uint_as_float(zv.y & 0xFFFF0000u));
+            }
+            if (r < ck.nv)
+                store_out4<TO>(static_cast<TO *>(a.out) + (size_t)(ck.row0 + r) * DI + (size_t)(h0 + hh) * DV + 4 * lane,
+                               o0, o1, o2, o3);
+        }
+        __syncthreads();                               // the tiles are read before the next copies; item_s is free
+    }
+}
+
 // One kernel for prep and the chains of a window. The first 32 G CTAs run the
 // chains, G = min(fragments, FU_GROUPS): CTA b takes V-head b % 32 of fragments
 // b / 32, b / 32 + G, .. one after the other; the other CTAs run the prep items
@@ -1136,6 +1262,8 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
 constexpr int FU_GROUPS = 2;
 static_assert(PR_THREADS == CA_THREADS, "one block size for both roles");
 __global__ void __launch_bounds__(PR_THREADS, 1) wy_fused_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                const __grid_constant__ CUtensorMap ymap,
+                                                                const __grid_constant__ CUtensorMap zmap,
                                                                 const WyArgs a)
 {
     const int n_frag = a.count->n_frag;                // the plan kernel ahead has completed
@@ -1146,6 +1274,10 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_fused_kernel(const __grid_co
             if (wy_carry_body(a, f, b % HV, true)) break;
     } else {
         wy_prep_body(xmap, a, b - nca, (int)gridDim.x - nca);
+        // then the gated norm of the chunks whose y the chains have written
+        __syncthreads();                               // every prep access of the shared memory is done
+        if (a.out_f32) wy_norm_items<float>(ymap, zmap, a);
+        else wy_norm_items<bf16>(ymap, zmap, a);
     }
 }
 
@@ -1214,12 +1346,13 @@ static size_t rnd256(size_t x) { return (x + 255) & ~(size_t)255; }
 static size_t rnd1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
 struct WyLayout {
-    size_t count, frags, chunks, flags, gates, xhat, ybuf, blobs, slots, total;
+    size_t count, frags, chunks, flags, yflags, gates, xhat, ybuf, blobs, slots, total;
     int W, f_cap, c_cap;
 };
 
 // Workspace of the chunked path for windows of W tokens (W a multiple of 64):
-// counts | fragments | chunks | prep flags [c_cap][16] | gate records [c_cap][32] | x^ [W][8192] fp16 | y [W][4096] fp16 |
+// counts | fragments | chunks | prep flags [c_cap][16] | y flags [c_cap][32] | gate records [c_cap][32] |
+// x^ [W][8192] fp16 | y [W][4096] fp16 |
 // blobs [c_cap][32] | two state slots.
 static WyLayout wy_layout(int N, int W)
 {
@@ -1231,7 +1364,8 @@ static WyLayout wy_layout(int N, int W)
     L.count = o;  o = rnd256(o + sizeof(WyCount));
     L.frags = o;  o = rnd256(o + (size_t)L.f_cap * sizeof(WyFrag));
     L.chunks = o; o = rnd256(o + (size_t)L.c_cap * sizeof(WyChunk));
-    L.flags = o;  o = rnd1024(o + (size_t)L.c_cap * HK * sizeof(int));
+    L.flags = o;  o = rnd256(o + (size_t)L.c_cap * HK * sizeof(int));
+    L.yflags = o; o = rnd1024(o + (size_t)L.c_cap * HV * sizeof(int));
     L.gates = o;  o = rnd1024(o + (size_t)L.c_cap * HV * GATE_FLOATS * sizeof(float));
     L.xhat = o;   o = rnd1024(o + (size_t)W * CC * sizeof(__half));
     L.ybuf = o;   o = rnd1024(o + (size_t)W * DI * sizeof(__half));
@@ -1326,12 +1460,18 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
                     per_sm >= 1;
         cudaGetLastError();                            // a refused query only means: separate kernels
         a.flags = fused ? reinterpret_cast<int *>(ws + L.flags) : nullptr;
+        a.yflags = fused ? reinterpret_cast<int *>(ws + L.yflags) : nullptr;
+        a.out_f32 = out_dt == GDN_F32;
         a.gates = reinterpret_cast<float *>(ws + L.gates);
         a.xhat = reinterpret_cast<__half *>(ws + L.xhat);
         a.gates_only = xhat_ext != nullptr;
         a.ybuf = reinterpret_cast<__half *>(ws + L.ybuf);
         a.blobs = ws + L.blobs;
         float *slots = reinterpret_cast<float *>(ws + L.slots);
+        CUtensorMap ymap, zmap;                        // y of the window and z, in boxes of 64 rows x 256 columns
+        if (fused && (!make_bf16_plain_map(&ymap, a.ybuf, W, DI, 256, CH) ||
+                      !make_bf16_plain_map(&zmap, z, T_total, DI, 256, CH)))
+            return cudaErrorInvalidValue;
         int wi = 0;
         for (int w0 = 0; w0 < T_total && e == cudaSuccess; w0 += W, ++wi) {
             a.w0 = w0;
@@ -1361,7 +1501,7 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
                 attr[0].val.cooperative = 1;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
-                if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, wy_fused_kernel, xmap, a);
+                if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, wy_fused_kernel, xmap, ymap, zmap, a);
             } else {
                 if (e == cudaSuccess)
                     e = launch_pdl(wy_prep_kernel, dim3((unsigned)std::min(L.c_cap * HK, n_sm)), dim3(PR_THREADS),
@@ -1369,7 +1509,7 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
                 if (e == cudaSuccess)
                     e = launch_pdl(wy_carry_kernel, dim3((unsigned)L.f_cap, HV), dim3(CA_THREADS), CA_SMEM, s, a);
             }
-            if (e == cudaSuccess) {
+            if (e == cudaSuccess && !fused) {
                 if (out_dt == GDN_F32)
                     e = launch_pdl(wy_norm_kernel<float>, dim3((unsigned)a.wlen), dim3(256), 0, s, a);
                 else
