@@ -84,9 +84,9 @@ TRAFFIC = {
                  per="call (attn_block_kernel + attn_combine_kernel) at B=256, ctx 4096"),
     "multi": dict(bytes=574_936_320 + 495_239_424, src="gdn_decode_multi.cu", sha="f4b811c1579705af", profile="profiles/decode_multi_kernel_B256_T4.md",
                   per="launch of decode_multi_kernel at B=256, T=4"),
-    "prefill": dict(bytes=355_511_296 + 124_768_512, src="gdn_chunk.cu", sha="912edb772ce70df0", profile="profiles/chunk_prefill_T4096.md",
+    "prefill": dict(bytes=225_393_664 + 199_463_936, src="gdn_chunk.cu", sha="2cf047c824b94ac0", profile="profiles/chunk_prefill_T4096.md",
                     per="gdn_prefill call at T=4096 (all of its kernels)"),
-    "varlen": dict(bytes=6_169_870_080 + 2_176_316_160, src="gdn_chunk.cu", sha="912edb772ce70df0", profile="profiles/chunk_prefill_varlen8.md",
+    "varlen": dict(bytes=3_756_179_968 + 3_416_963_072, src="gdn_chunk.cu", sha="2cf047c824b94ac0", profile="profiles/chunk_prefill_varlen8.md",
                    per="gdn_prefill call on the 8-sequence varlen workload (all of its kernels)"),
     "in_proj": dict(bytes=109_801_728 + 76_413_184, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                     per="gdn_in_proj call at M=4096"),
@@ -944,8 +944,8 @@ def main():
                                  "algorithmic_flop_per_call": PREFILL_FLOP_PER_TOKEN * PREFILL_T,
                                  "algorithmic_bytes_per_call": PREFILL_BYTES,
                                  "traffic": pf_tr, "traffic_source": pf_tr_note,
-                                 "timed": "whole gdn_prefill call (plan, activation, prep, carry, gated norm, "
-                                          "conv_state kernels)"}},
+                                 "timed": "whole gdn_prefill call (plan, activation, the cooperative prep + chain + "
+                                          "gated norm kernel, conv_state kernels)"}},
         "in_proj": {"workload": f"input_projections_M{PREFILL_T}_bf16", "op": "qkv|z|alpha|beta = h w_in^T, 2048 -> 12352",
                     "us_per_call": r["ip"]["us"], "l2": "flushed between timed calls",
                     "roofline": {"bound": "tensor", "achieved": r["ip"]["tflops"], "peak": r["tc_peak"],

@@ -175,6 +175,11 @@ gdn_status gdn_decode_multi(const gdn_params *p, const void *qkv, const void *z,
  *                     gdn_prefill_workspace_size(N, 64, act, 64) (one 64-token
  *                     window) is accepted, and a larger one gives longer
  *                     windows.
+ * chunk_size 64 runs each window's prep, state chains and gated norm as one
+ * cooperative kernel of one CTA per SM, which occupies the whole device while it
+ * runs. Where such a grid cannot be resident (e.g. a share of the SMs), or with
+ * GDN_PREFILL_SPLIT=1 in the environment when the library first runs a prefill,
+ * the same work runs as separate kernels with the same results.
  * 0 <= N <= 65535, 0 <= T_total <= 2^24. cu_seqlens is read on the device only;
  * a cu_seqlens that breaks the rules above gives unspecified results for the
  * offending sequences but never touches memory outside the stated extents.
