@@ -130,8 +130,6 @@ struct WyArgs {
     int *flags;                  // [c_cap][16]: item (chunk, K-head) of prep done (one kernel: prep + carry), or NULL
     int *yflags;                 // [c_cap][32]: y of (chunk, V-head) written (one kernel form), or NULL
     int out_f32;                 // out is fp32 (else bf16)
-    int call_tail;               // one kernel form, last window: also the state passthrough and conv_state_out
-    bf16 *cs_out;                // conv_state_out, or NULL
     __half *ybuf;                // [wlen][4096]: y (scale applied) before the gated norm
     float *gates;                // [c_cap][32][4][64]: per (chunk, V-head) G, beta, gamma_t, exp(G_n - G_t)
     unsigned char *blobs;        // [c_cap][32] x BLOB_BYTES
@@ -1254,42 +1252,6 @@ __device__ void wy_norm_items(const CUtensorMap &ymap, const CUtensorMap &zmap, 
     }
 }
 
-// The end of the call, in the last window's cooperative kernel, on the CTAs past
-// their prep items (which would otherwise wait for the chains): sequences
-// without tokens pass their SSM state through (zeros without an input state),
-// and conv_state_out takes each sequence's last three conv inputs (rows of
-// conv_state_in where the sequence is shorter). One warp per sequence. Every
-// act kernel, the only other reader of conv_state_in, has completed; rows are
-// written in order 0, 1, 2 and row m reads row L + m >= m, so conv_state_out may
-// alias conv_state_in. The chains read the input state of non-empty sequences
-// only, so the passthrough does not meet them.
-__device__ void wy_call_tail(const WyArgs &a, int cta, int n_ctas)
-{
-    const int lane = threadIdx.x & 31;
-    const int nw = (int)(blockDim.x >> 5);
-    for (int n = cta * nw + (int)(threadIdx.x >> 5); n < a.N; n += n_ctas * nw) {
-        const int s0 = cu_clamp(a.cu, n, 0, a.T_total), s1 = cu_clamp(a.cu, n + 1, s0, a.T_total);
-        const int L = s1 - s0;
-        if (L == 0 && a.S_out != nullptr && a.S_out != a.S_in) {
-            const size_t base = (size_t)n * HV * (DV * DK) / 4;
-            for (int e = lane; e < HV * DV * DK / 4; e += 32)
-                reinterpret_cast<float4 *>(a.S_out)[base + e] =
-                    a.S_in ? reinterpret_cast<const float4 *>(a.S_in)[base + e] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (a.cs_out != nullptr) {
-#pragma unroll 1
-            for (int m = 0; m < KC - 1; ++m) {
-                const int pos = L - (KC - 1) + m;       // token of the sequence, or a conv_state_in row if < 0
-                uint4 *dst = reinterpret_cast<uint4 *>(a.cs_out + ((size_t)n * (KC - 1) + m) * CC);
-                const uint4 *src = pos >= 0 ? reinterpret_cast<const uint4 *>(a.qkv + (size_t)(s0 + pos) * CC)
-                                 : a.cs_in ? reinterpret_cast<const uint4 *>(a.cs_in + ((size_t)n * (KC - 1) + pos + KC - 1) * CC)
-                                           : nullptr;
-                for (int e = lane; e < CC / 8; e += 32) dst[e] = src ? src[e] : make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-    }
-}
-
 // One kernel for prep and the chains of a window. The first 32 G CTAs run the
 // chains, G = min(fragments, FU_GROUPS): CTA b takes V-head b % 32 of fragments
 // b / 32, b / 32 + G, .. one after the other; the other CTAs run the prep items
@@ -1312,7 +1274,6 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_fused_kernel(const __grid_co
             if (wy_carry_body(a, f, b % HV, true)) break;
     } else {
         wy_prep_body(xmap, a, b - nca, (int)gridDim.x - nca);
-        if (a.call_tail) wy_call_tail(a, b - nca, (int)gridDim.x - nca);
         // then the gated norm of the chunks whose y the chains have written
         __syncthreads();                               // every prep access of the shared memory is done
         if (a.out_f32) wy_norm_items<float>(ymap, zmap, a);
@@ -1470,7 +1431,6 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
 {
     cudaError_t e = wy_setup();
     if (e != cudaSuccess) return e;
-    bool tail_done = false;                            // the last window's cooperative kernel ended the call
     const int n_sm = sm_count();
     if (n_sm <= 0) return cudaErrorInvalidDevice;
     if (T_total > 0) {
@@ -1502,7 +1462,6 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
         a.flags = fused ? reinterpret_cast<int *>(ws + L.flags) : nullptr;
         a.yflags = fused ? reinterpret_cast<int *>(ws + L.yflags) : nullptr;
         a.out_f32 = out_dt == GDN_F32;
-        a.cs_out = static_cast<bf16 *>(cs_out);
         a.gates = reinterpret_cast<float *>(ws + L.gates);
         a.xhat = reinterpret_cast<__half *>(ws + L.xhat);
         a.gates_only = xhat_ext != nullptr;
@@ -1517,7 +1476,6 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
         for (int w0 = 0; w0 < T_total && e == cudaSuccess; w0 += W, ++wi) {
             a.w0 = w0;
             a.wlen = std::min(W, T_total - w0);
-            a.call_tail = fused && w0 + W >= T_total;  // the last window's kernel ends the call
             a.slot_in = slots + (size_t)((wi + 1) & 1) * HV * DV * DK;
             a.slot_out = slots + (size_t)(wi & 1) * HV * DV * DK;
             CUtensorMap xmap;                          // x^ rows of this window; rows past it read as zero
@@ -1544,7 +1502,6 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
                 if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, wy_fused_kernel, xmap, ymap, zmap, a);
-                if (e == cudaSuccess && a.call_tail) tail_done = true;
             } else {
                 if (e == cudaSuccess)
                     e = launch_pdl(wy_prep_kernel, dim3((unsigned)std::min(L.c_cap * HK, n_sm)), dim3(PR_THREADS),
@@ -1560,11 +1517,9 @@ cudaError_t launch_prefill_chunked(const gdn_params *p, const void *qkv, const v
             }
         }
     }
-    // the one-kernel form did these in its last window
-    if (e == cudaSuccess && N > 0 && !tail_done)
+    if (e == cudaSuccess && N > 0)
         e = launch_pdl(wy_passthrough_kernel, dim3((unsigned)N, HV), dim3(256), 0, s, cu, T_total, S_in, S_out);
-    if (e == cudaSuccess && cs_out && !tail_done)
-        e = launch_conv_state_out_bf16(cu, N, T_total, qkv, cs_in, cs_out, s, true);
+    if (e == cudaSuccess && cs_out) e = launch_conv_state_out_bf16(cu, N, T_total, qkv, cs_in, cs_out, s, true);
     return e;
 }
 
