@@ -95,8 +95,8 @@ TRAFFIC = {
     "gated_out_proj": dict(bytes=83_939_072 + 2_929_408, src="gdn_gated_proj.cu", sha="f20dfeb1dda1398b",
                            profile="profiles/gated_proj_M4096.md",
                            per="gdn_gated_out_proj call at M=4096"),
-    "in_proj_conv_prefill": dict(bytes=404_716_032 + 182_607_616, src=("gdn_in_conv.cu", "gdn_chunk.cu"),
-                                 sha="e607605762e19931", profile="profiles/in_proj_conv_T4096.md",
+    "in_proj_conv_prefill": dict(bytes=270_784_256 + 256_022_016, src=("gdn_in_conv.cu", "gdn_chunk.cu"),
+                                 sha="5c2ccf21ed58c583", profile="profiles/in_proj_conv_T4096.md",
                                  per="gdn_in_proj_conv + gdn_prefill_xhat at T=4096 (all of their kernels)"),
     "out_proj_batch": dict(bytes=18_900_224 + 0, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                            per="gdn_out_proj call at M=256"),
