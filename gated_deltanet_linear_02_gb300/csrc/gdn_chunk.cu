@@ -18,22 +18,28 @@
 // by the workspace the caller passes), so the scratch does not grow with the
 // prompt: a long prompt runs as a sequence of bounded fragments with the state
 // carried between them, as the Lily page does in "Limit temporary memory by
-// splitting the prompt into fragments". Per window, four kernels:
+// splitting the prompt into fragments". Per window:
 //  wy_plan   the window's sequence fragments and 64-token chunks (from
-//            cu_seqlens, on the device).
+//            cu_seqlens, on the device); clears the window's flags.
 //  wy_act    conv + SiLU over all 8192 channels and the L2 norm of q and k per
-//            head -> x^, fp16 [rows of the window][8192].
-//  wy_prep   one item per (chunk, K-head), for both V-heads of the GQA pair:
-//            the gates, K K^T and Q K^T (one M=128 product), P = Mask o Q K^T,
-//            the unit-lower triangular inverse for T, then U^T = V^T T^T and
-//            W^T = K^T (T diag(gamma))^T. It writes one operand blob per
-//            (chunk, V-head): W^T, U^T, P and the decays.
-//  wy_carry  one CTA per (fragment, V-head): the chain over the fragment's
-//            chunks. The state lives in tensor memory as S^T (lane = value
-//            column j), and its fp16 copy is the A operand of the next chunk's
-//            products, read from tensor memory, so nothing on the chain goes
-//            through shared memory. The gated RMSNorm . silu(z) runs in the
-//            same CTA and writes out.
+//            head -> x^, fp16 [rows of the window][8192]; the gate records.
+//  wy_fused  one cooperative grid, one CTA per SM, three roles:
+//   prep     (the CTAs past the chains) one item per (chunk, K-head), for both
+//            V-heads of the GQA pair, in chunk order: K K^T and Q K^T (one
+//            M=128 product), P = Mask o Q K^T, the unit-lower triangular
+//            inverse for T, then U^T = V^T T^T and W^T = K^T (T diag(gamma))^T.
+//            It writes one operand blob per (chunk, V-head) (W^T, U^T, P, K~^T,
+//            Q~) and then a flag.
+//   chain    one CTA per (fragment, V-head): the chain over the fragment's
+//            chunks, each taken as soon as its prep flag is set. The state
+//            lives in tensor memory as S^T (lane = value column j), and its fp16
+//            copy is the A operand of the next chunk's products, read from
+//            tensor memory, so nothing on the chain goes through shared memory.
+//            y goes out as fp16, with a flag per (chunk, V-head).
+//   norm     the prep CTAs once their items are done: the gated RMSNorm .
+//            silu(z) of (chunk, 4 V-heads) items whose y flags are set.
+// Where a one-per-SM cooperative grid cannot be resident, the three roles run as
+// the kernels wy_prep, wy_carry and wy_norm, one after the other.
 // Operand precision: every product takes fp16 operands (kind::f16) with fp32
 // accumulation. fp16 keeps 11 significant bits, the precision of tf32 rounded
 // to nearest, at the bf16 rate. The operands are unit-norm keys and queries,
@@ -76,7 +82,7 @@ struct WyCount {
 };
 
 // Per (chunk, V-head) operand blob, 72 KiB. The tiles are stored exactly as
-// the carry kernel's shared-memory operands, so one bulk copy moves the blob.
+// the chain's shared-memory operands, so one bulk copy moves the blob.
 constexpr uint32_t BL_WT = 0;          // W^T, fp16, MN-major (N = token t, K = key i),       16 KiB
 constexpr uint32_t BL_UT = 16384;      // U^T, fp16, same layout (t, value j),                 16 KiB
 constexpr uint32_t BL_P = 32768;       // P = Mask o Q K^T, fp16 K-major [t][s] (Kd 64),       8 KiB
@@ -748,20 +754,24 @@ __global__ void __launch_bounds__(PR_THREADS, 1) wy_prep_kernel(const __grid_con
 }
 
 // ------------------------------------------------------------------ carry
-// One CTA per (fragment, V-head vh). The state is kept transposed, S^T[j][i]
-// (lane = value column j, column = key i): then every product has the 128
-// value columns as its M dimension, and the fp16 state and the fp16 Vnew are A
-// operands read straight from tensor memory. Per chunk:
+// The chain of one (fragment, V-head vh): a CTA of the one-kernel form, or of
+// wy_carry. The state is kept transposed, S^T[j][i] (lane = value column j,
+// column = key i): then every product has the 128 value columns as its M
+// dimension, and the fp16 state and the fp16 Vnew are A operands read straight
+// from tensor memory. Per chunk, with K~ = diag(exp(G_n - G_t)) k^ and
+// Q~ = diag(gamma_t) q^ from prep:
 //   (1) (W S)^T[j][t] = sum_i S^T[j][i] W[t][i]   K = 128, split over two issuers
-//       Y1^T[j][t]    = sum_i S^T[j][i] q[t][i]    (times gamma_t afterwards; a third issuer)
-//   (E1) Vnew^T = U^T - (W S)^T, zero past the chunk's tokens, stored as fp16
-//       twice: times exp(G_n - G_t) (for the state) and plain (for y)
-//   (2) S^T[j][i] += sum_t Vnew^T[j][t] exp(G_n - G_t) k[t][i]    (tensor memory
-//       holds gamma_n S^T beforehand)
+//       Y1^T[j][t]    = sum_i S^T[j][i] Q~[t][i]  (a third issuer)
+//   (E1) Vnew^T = U^T - (W S)^T, zero past the chunk's tokens (their rows of U
+//       and W are zero), stored once as fp16 in tensor memory: the A operand of
+//       both products of (2)
+//   (2) S^T[j][i] += sum_t Vnew^T[j][t] K~[t][i]   (tensor memory holds gamma_n S^T
+//       beforehand)
 //       Y2^T[j][t]  = sum_s Vnew^T[j][s] P[t][s]
 //   (E2) S^T -> fp16 copy for the next chunk's products; gamma_n(next) S^T back.
-//   (O)  y = scale (gamma_t Y1 + Y2) to shared memory as [t][j]; then one warp per
-//        token row: out = y rms(y)^-1 w silu(z)
+//   (O)  y = scale (Y1 + Y2) as fp16 to the window's y buffer, off the chain. The
+//        gated RMSNorm . silu(z) runs on other SMs: the norm items of the one-kernel
+//        form, or wy_norm.
 // Warps 0-7 run E1/E2 (lane quarter w % 4, half w / 4); warps 8-11 the output;
 // warp 12 loads operands; warps 13-15 issue MMAs. The issuers and the producer
 // take no part in CTA-wide barriers; every handoff is an mbarrier.
