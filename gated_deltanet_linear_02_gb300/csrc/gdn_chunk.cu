@@ -1161,43 +1161,63 @@ __global__ void __launch_bounds__(CA_THREADS, 1) wy_carry_kernel(const WyArgs a)
 
 // Norm items of the one-kernel form: the gated RMSNorm . silu(z) of section
 // "Output path", out = y (mean_j y^2 + eps)^-1/2 w_j silu(z) per token and
-// V-head, over items (chunk, 4 V-heads) handed out in chunk order from a
+// V-head, over items (chunk, 2 V-heads) handed out in chunk order from a
 // counter, so that a CTA past its prep items takes the next item whose y is
-// (about to be) written. One thread waits (bounded, with a back-off that keeps
-// the polling off the chains' way) for the item's four y flags, then brings the
-// item's y and z rows (64 x 512 columns each) into the shared memory prep has
-// left, by TMA: plain loads would have to stage through the little L1 that the
-// kernel's shared memory leaves. Warp w takes rows 4w..4w+3; lane l holds
-// columns 4l..4l+3 of a head, so the head's sum of squares is a warp sum.
-constexpr int NI_HEADS = 4;
-constexpr uint32_t NI_Y = 0, NI_Z = 65536, NI_BAR = 131072;   // two 64 x 256 boxes each
-static_assert(NI_BAR + 8 <= PR_SMALL, "the norm tiles fit below the prep block's mbarriers");
+// (about to be) written. Warp 0 runs an item ahead: it takes a ticket, waits
+// (bounded, with a back-off that keeps the polling off the chains' way) for the
+// item's two y flags, and brings the item's y and z rows (64 x 256 columns each)
+// into one of two shared-memory buffers by TMA; plain loads would have to stage
+// through the little L1 that the kernel's shared memory leaves. Warps 1-15
+// normalise the item in the other buffer meanwhile, one (row, head) unit at a
+// time with the unit's loads issued first; lane l holds columns 4l..4l+3 of the
+// head, so the head's sum of squares is a warp sum. The two sides meet only
+// through mbarriers (bounded waits), never a CTA-wide barrier.
+constexpr int NI_HEADS = 2;
+constexpr uint32_t NI_TILE = CH * NI_HEADS * DV * 2;        // 32 KiB: 64 rows x 256 columns
+constexpr uint32_t NI_BUF = 2 * NI_TILE;                    // y, then z
+constexpr uint32_t NI_BAR = 2 * NI_BUF;                     // full[2], used[2], the items of the buffers
+static_assert(NI_BAR + 64 <= PR_SMALL, "the norm buffers fit below the prep block's mbarriers");
+constexpr int NI_WORKERS = PR_THREADS / 32 - 1;             // warps 1-15
+constexpr int NI_UNITS = CH * NI_HEADS;                     // (row, head) units of an item
+constexpr int NI_PER_WARP = (NI_UNITS + NI_WORKERS - 1) / NI_WORKERS;
 template <typename TO>
 __device__ void wy_norm_items(const CUtensorMap &ymap, const CUtensorMap &zmap, const WyArgs &a)
 {
     extern __shared__ unsigned char smem_raw[];
-    __shared__ int item_s;
     unsigned char *sm = smem_aligned1024(smem_raw);
-    const uint32_t sb = smem_u32(sm), bar = sb + NI_BAR;
+    const uint32_t sb = smem_u32(sm);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + NI_BAR);     // [2]: the buffer's copies landed
+    uint64_t *used = full + 2;                                       // [2]: the workers are done with it
+    int *item_of = reinterpret_cast<int *>(full + 4);                // [2]: its item, -1 to end
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_items = a.count->n_chunks * (HV / NI_HEADS);
-    const bool has_w = a.norm_w != nullptr;
-    const float4 w = has_w ? __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane) : make_float4(1.f, 1.f, 1.f, 1.f);
-    int ticket = 0;                                    // thread 0: the next item to run
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(smem_u32(&full[k]), 1);
+            mbar_init(smem_u32(&used[k]), NI_WORKERS);
+        }
         fence_mbar_init();
-        ticket = atomicAdd(&a.count->norm_next, 1);
     }
     __syncthreads();
-    for (uint32_t phase = 0;; phase ^= 1u) {
-        if (warp == 0) {
-            // lanes 0-3 wait for one head's y flag each; lane 0 then starts the copies
-            int item = __shfl_sync(0xffffffffu, ticket, 0);
-            if (item < n_items) {
+    if (warp == 0) {
+        // ---------------------------------------------------------- the item ahead
+        for (int n = 0;; ++n) {
+            const int buf = n & 1;
+            bool ok = true;
+            if (n >= 2 && lane == 0)                  // the workers are done with item n - 2
+                ok = mbar_wait_sleep(smem_u32(&used[buf]), (uint32_t)(((n >> 1) - 1) & 1));
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            int item = -1;
+            if (ok) {
+                int t = 0;
+                if (lane == 0) t = atomicAdd(&a.count->norm_next, 1);
+                item = __shfl_sync(0xffffffffu, t, 0);
+                if (item >= n_items) item = -1;
+            }
+            if (item >= 0) {
                 const int g = item / (HV / NI_HEADS), h0 = NI_HEADS * (item % (HV / NI_HEADS));
                 bool ready = true;
-                if (lane < NI_HEADS) {
+                if (lane < NI_HEADS) {                // one y flag per lane
                     const int *fl = a.yflags + (size_t)g * HV + h0 + lane;
                     const uint64_t t0 = global_timer_ns();
                     for (;;) {
@@ -1209,7 +1229,7 @@ __device__ void wy_norm_items(const CUtensorMap &ymap, const CUtensorMap &zmap, 
                     }
                 }
                 if (!__all_sync(0xffffffffu, ready)) {
-                    if (lane == 0) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+                    ok = false;
                     item = -1;
                 } else if (lane == 0) {
                     // the copies (async proxy) after the flags and after this CTA's
@@ -1217,48 +1237,68 @@ __device__ void wy_norm_items(const CUtensorMap &ymap, const CUtensorMap &zmap, 
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     const WyChunk ck = a.chunks[g];
-                    mbar_arrive_expect_tx(bar, 4u * 32768u);
-                    tma_load_2d(sb + NI_Y, &ymap, h0 * DV, ck.row0 - a.w0, bar);
-                    tma_load_2d(sb + NI_Y + 32768, &ymap, h0 * DV + 256, ck.row0 - a.w0, bar);
-                    tma_load_2d(sb + NI_Z, &zmap, h0 * DV, ck.row0, bar);
-                    tma_load_2d(sb + NI_Z + 32768, &zmap, h0 * DV + 256, ck.row0, bar);
+                    item_of[buf] = item;
+                    const uint32_t bar = smem_u32(&full[buf]);
+                    mbar_arrive_expect_tx(bar, NI_BUF);
+                    tma_load_2d(sb + buf * NI_BUF, &ymap, h0 * DV, ck.row0 - a.w0, bar);
+                    tma_load_2d(sb + buf * NI_BUF + NI_TILE, &zmap, h0 * DV, ck.row0, bar);
                 }
             }
-            if (lane == 0) item_s = item;
-        }
-        __syncthreads();
-        const int item = item_s;
-        if (item < 0 || item >= n_items) return;       // uniform: every thread read item_s after the barrier
-        if (tid == 0) ticket = atomicAdd(&a.count->norm_next, 1);   // the next one, while this one runs
-        const int g = item / (HV / NI_HEADS), h0 = NI_HEADS * (item % (HV / NI_HEADS));
-        const WyChunk ck = a.chunks[g];
-        const bool ok = mbar_wait_sleep(bar, phase);
-        if (__syncthreads_or(!ok)) {                   // a copy that never landed: leave together
-            if (tid == 0) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
-            return;
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int r = 4 * warp + (u >> 2), hh = u & 3;
-            const uint32_t off = (uint32_t)r * 512u + (uint32_t)((hh & 1) * 128 + 4 * lane) * 2u + (uint32_t)(hh >> 1) * 32768u;
-            const uint2 yv = *reinterpret_cast<const uint2 *>(sm + NI_Y + off);
-            const uint2 zv = *reinterpret_cast<const uint2 *>(sm + NI_Z + off);
-            const float2 y01 = __half22float2(*reinterpret_cast<const __half2 *>(&yv.x));
-            const float2 y23 = __half22float2(*reinterpret_cast<const __half2 *>(&yv.y));
-            float o0 = y01.x, o1 = y01.y, o2 = y23.x, o3 = y23.y;
-            if (has_w) {
-                const float ms = warp_sum(o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3) * (1.0f / DV);
-                const float rs = rsqrtf(ms + a.norm_eps);
-                o0 *= rs * w.x * silu_gate(__uint_as_float(zv.x << 16));
-                o1 *= rs * w.y * silu_gate(__uint_as_float(zv.x & 0xFFFF0000u));
-                o2 *= rs * w.z * silu_gate(__uint_as_float(zv.y << 16));
-                o3 *= rs * w.w * silu_gate(__uint_as_float(zv.y & 0xFFFF0000u));
+            if (item < 0) {                           // the end (or a wait that gave up)
+                if (lane == 0) {
+                    if (!ok) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+                    item_of[buf] = -1;
+                    mbar_arrive(smem_u32(&full[buf]));
+                }
+                break;
             }
-            if (r < ck.nv)
+        }
+    } else {
+        // ---------------------------------------------------------- the workers
+        const bool has_w = a.norm_w != nullptr;
+        const float4 w = has_w ? __ldg(reinterpret_cast<const float4 *>(a.norm_w) + lane) : make_float4(1.f, 1.f, 1.f, 1.f);
+        for (int n = 0;; ++n) {
+            const int buf = n & 1;
+            if (!mbar_wait_sleep(smem_u32(&full[buf]), (uint32_t)((n >> 1) & 1))) {
+                if (lane == 0) atomicExch(&g_chunk_error, (unsigned int)GDN_ERR_TIMEOUT);
+                break;
+            }
+            const int item = item_of[buf];
+            if (item < 0) break;
+            const int g = item / (HV / NI_HEADS), h0 = NI_HEADS * (item % (HV / NI_HEADS));
+            const WyChunk ck = a.chunks[g];
+            const unsigned char *yt = sm + buf * NI_BUF, *zt = yt + NI_TILE;
+            uint2 yv[NI_PER_WARP], zv[NI_PER_WARP];
+#pragma unroll
+            for (int k = 0; k < NI_PER_WARP; ++k) {
+                const int u = (warp - 1) + NI_WORKERS * k;
+                const uint32_t off = (uint32_t)(u >> 1) * (NI_HEADS * DV * 2) + (uint32_t)((u & 1) * DV + 4 * lane) * 2u;
+                if (u < NI_UNITS) {
+                    yv[k] = *reinterpret_cast<const uint2 *>(yt + off);
+                    zv[k] = *reinterpret_cast<const uint2 *>(zt + off);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < NI_PER_WARP; ++k) {
+                const int u = (warp - 1) + NI_WORKERS * k, r = u >> 1, hh = u & 1;
+                if (u >= NI_UNITS || r >= ck.nv) continue;   // uniform over the warp
+                const float2 y01 = __half22float2(*reinterpret_cast<const __half2 *>(&yv[k].x));
+                const float2 y23 = __half22float2(*reinterpret_cast<const __half2 *>(&yv[k].y));
+                float o0 = y01.x, o1 = y01.y, o2 = y23.x, o3 = y23.y;
+                if (has_w) {
+                    const float ms = warp_sum(o0 * o0 + o1 * o1 + o2 * o2 + o3 * o3) * (1.0f / DV);
+                    const float rs = rsqrtf(ms + a.norm_eps);
+                    o0 *= rs * w.x * silu_gate(__uint_as_float(zv[k].x << 16));
+                    o1 *= rs * w.y * silu_gate(__uint_as_float(zv[k].x & 0xFFFF0000u));
+                    o2 *= rs * w.z * silu_gate(__uint_as_float(zv[k].y << 16));
+                    o3 *= rs * w.w * silu_gate(__uint_as_float(zv[k].y & 0xFFFF0000u));
+                }
                 store_out4<TO>(static_cast<TO *>(a.out) + (size_t)(ck.row0 + r) * DI + (size_t)(h0 + hh) * DV + 4 * lane,
                                o0, o1, o2, o3);
+            }
+            __syncwarp();                             // the warp's reads of the buffer are done
+            if (lane == 0) mbar_arrive(smem_u32(&used[buf]));
         }
-        __syncthreads();                               // the tiles are read before the next copies; item_s is free
     }
 }
 
