@@ -84,9 +84,9 @@ TRAFFIC = {
                  per="call (attn_block_kernel + attn_combine_kernel) at B=256, ctx 4096"),
     "multi": dict(bytes=574_936_320 + 495_239_424, src="gdn_decode_multi.cu", sha="f4b811c1579705af", profile="profiles/decode_multi_kernel_B256_T4.md",
                   per="launch of decode_multi_kernel at B=256, T=4"),
-    "prefill": dict(bytes=224_269_056 + 199_894_016, src="gdn_chunk.cu", sha="add7a66c5f6e84be", profile="profiles/chunk_prefill_T4096.md",
+    "prefill": dict(bytes=226_213_376 + 202_119_424, src="gdn_chunk.cu", sha="2a906081f77dc1ab", profile="profiles/chunk_prefill_T4096.md",
                     per="gdn_prefill call at T=4096 (all of its kernels)"),
-    "varlen": dict(bytes=3_782_947_072 + 3_415_911_424, src="gdn_chunk.cu", sha="add7a66c5f6e84be", profile="profiles/chunk_prefill_varlen8.md",
+    "varlen": dict(bytes=3_851_810_304 + 3_453_916_416, src="gdn_chunk.cu", sha="2a906081f77dc1ab", profile="profiles/chunk_prefill_varlen8.md",
                    per="gdn_prefill call on the 8-sequence varlen workload (all of its kernels)"),
     "in_proj": dict(bytes=109_801_728 + 76_413_184, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                     per="gdn_in_proj call at M=4096"),
@@ -95,8 +95,8 @@ TRAFFIC = {
     "gated_out_proj": dict(bytes=83_939_072 + 2_929_408, src="gdn_gated_proj.cu", sha="f20dfeb1dda1398b",
                            profile="profiles/gated_proj_M4096.md",
                            per="gdn_gated_out_proj call at M=4096"),
-    "in_proj_conv_prefill": dict(bytes=276_695_040 + 256_400_896, src=("gdn_in_conv.cu", "gdn_chunk.cu"),
-                                 sha="f3b73c66bee7c3ca", profile="profiles/in_proj_conv_T4096.md",
+    "in_proj_conv_prefill": dict(bytes=279_962_112 + 257_320_960, src=("gdn_in_conv.cu", "gdn_chunk.cu"),
+                                 sha="53f131d97d3c07f6", profile="profiles/in_proj_conv_T4096.md",
                                  per="gdn_in_proj_conv + gdn_prefill_xhat at T=4096 (all of their kernels)"),
     "out_proj_batch": dict(bytes=18_900_224 + 0, src="gdn_gemm.cu", sha="e3474fe40a5549bd", profile="profiles/proj_gemm_M4096.md",
                            per="gdn_out_proj call at M=256"),
