@@ -40,3 +40,21 @@ def test_reference_arm_other_ranks_do_no_work():
     p = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert p.returncode == 0, p.stderr[-2000:]
     assert p.stdout.strip() == ""
+
+
+def test_traffic_figures_belong_to_the_current_kernels():
+    """Every DRAM-traffic figure the bench reports was captured on the kernel
+    source as it stands: its summary under profiles/ exists and quotes the
+    source's hash, and the bench resolves it (a figure whose source changed
+    since its capture would be reported as null)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    for key, t in bench.TRAFFIC.items():
+        path = os.path.join(ROOT, t["profile"])
+        assert os.path.isfile(path), (key, t["profile"])
+        with open(path) as f:
+            assert t["sha"] in f.read(), (key, "the summary does not quote the hash of its capture")
+        value, note = bench.traffic(key)
+        assert value == t["bytes"], (key, note)
